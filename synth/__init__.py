@@ -1,0 +1,103 @@
+"""Seeded synthetic inputs for the NVFP4 projection workloads.
+
+Shared by the tests, the smoke check and the bench: it draws random numbers and
+nothing else (no quantization, rounding or layout arithmetic lives here), so both
+the CUDA path and the CPU oracle can take their inputs from it.
+
+Workloads (shapes of the decode / MTP-verify / prefill / W4A4 cases of batch-one
+Qwen3.x serving; the fused gate+up projection doubles N):
+
+  name        M     K      N      y     seed  notes
+  tiny        1     512    256    f32   0
+  decode_a    1     5120   17408  bf16  1     0.1% of W entries x20 (outliers)
+  decode_b    1     17408  5120   bf16  2     same
+  verify_a    7     5120   34816  bf16  3
+  verify_b    7     5120   6144   bf16  3
+  prefill_a   512   5120   34816  bf16  4     x rows scaled by U(0.5, 4)
+  prefill_b   512   17408  5120   bf16  4     same
+  w4a4        2048  5120   17408  bf16  5     x quantized to NVFP4 inside the call
+
+Draw order with ``torch.Generator(device='cpu').manual_seed(seed)``: W ~ N(0, 0.02)
+fp32 first, then x ~ N(0, 1) fp32, then the outlier positions (uniform without
+replacement: sequential draws with repeats discarded; the entries keep their sign
+and are multiplied by 20), then the per-row x scales.  x is cast to bf16 last.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    K: int
+    N: int
+    y_dtype: str  # "f32" | "bf16"
+    seed: int
+    outliers: bool = False
+    row_scale: bool = False
+    w4a4: bool = False
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("tiny", 1, 512, 256, "f32", 0),
+        Workload("decode_a", 1, 5120, 17408, "bf16", 1, outliers=True),
+        Workload("decode_b", 1, 17408, 5120, "bf16", 2, outliers=True),
+        Workload("verify_a", 7, 5120, 34816, "bf16", 3),
+        Workload("verify_b", 7, 5120, 6144, "bf16", 3),
+        Workload("prefill_a", 512, 5120, 34816, "bf16", 4, row_scale=True),
+        Workload("prefill_b", 512, 17408, 5120, "bf16", 4, row_scale=True),
+        Workload("w4a4", 2048, 5120, 17408, "bf16", 5, w4a4=True),
+    ]
+}
+
+
+def _unique_positions(gen: torch.Generator, total: int, count: int) -> torch.Tensor:
+    """`count` distinct indices in [0, total): sequential uniform draws, repeats dropped."""
+    got = np.empty(0, dtype=np.int64)
+    while got.size < count:
+        cand = torch.randint(0, total, (2 * (count - got.size) + 16,), generator=gen,
+                             dtype=torch.int64).numpy()
+        allc = np.concatenate([got, cand])
+        _, first = np.unique(allc, return_index=True)
+        got = allc[np.sort(first)]
+    return torch.from_numpy(got[:count].copy())
+
+
+def make_inputs(M: int, K: int, N: int, seed: int, *, outliers: bool = False,
+                row_scale: bool = False, w_std: float = 0.02):
+    """Return (x bf16 [M,K], W fp32 [N,K]) on the CPU."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    w = torch.randn(N, K, generator=gen, dtype=torch.float32) * w_std
+    x = torch.randn(M, K, generator=gen, dtype=torch.float32)
+    if outliers:
+        count = max(1, round(0.001 * N * K))
+        pos = _unique_positions(gen, N * K, count)
+        w.view(-1)[pos] *= 20.0
+    if row_scale:
+        s = torch.rand(M, 1, generator=gen, dtype=torch.float32) * 3.5 + 0.5
+        x = x * s
+    return x.to(torch.bfloat16), w
+
+
+def workload_inputs(name: str, *, M: int | None = None):
+    """Inputs of a named workload; M may be overridden (fewer rows of x)."""
+    w = WORKLOADS[name]
+    return make_inputs(M if M is not None else w.M, w.K, w.N, w.seed,
+                       outliers=w.outliers, row_scale=w.row_scale)
+
+
+def random_x(M: int, K: int, seed: int, scale: float = 1.0) -> torch.Tensor:
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    return (torch.randn(M, K, generator=gen, dtype=torch.float32) * scale).to(torch.bfloat16)
+
+
+def random_w(N: int, K: int, seed: int, std: float = 0.02) -> torch.Tensor:
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    return torch.randn(N, K, generator=gen, dtype=torch.float32) * std
