@@ -1,0 +1,484 @@
+#!/usr/bin/env python
+"""Throughput of the NVFP4 projection on GB300 -- one JSON line on stdout (rank 0).
+
+Workload (the decode case the metric is quoted on): M = 1 W4A16 NVFP4 linear on the two
+decode shapes (K=5120, N=17408) and (K=17408, N=5120), y bf16, synthetic seeded data.
+One step = one call of each shape.  Metric: algorithmic GB/s = (packed nibbles + E4M3
+scales + x + y + global scale) bytes / time.  Inputs stay resident in HBM; the weights
+rotate over several copies (> 2x L2 in total) so every call streams from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the reference arm of this build) on a bounded
+sample of the same workload.  Under torchrun with N > 1 every rank runs an independent
+replica ("replicas only": the projection needs no exchange); value = all ranks' bytes
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 linear: GB/s (M≤16) & TFLOP/s (M≥512), % of GB300 roofline"
+DECODE = ("decode_a", "decode_b")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemv_w4a16_decode_traffic.txt")
+
+
+def algo_bytes(M, K, N, y_bytes=2):
+    return N * K // 2 + N * K // 16 + M * K * 2 + M * N * y_bytes + 4
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+# ---- clocks during the timed region ------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [p.strip() for p in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ---- our arm -----------------------------------------------------------------------------
+
+class DecodeSetup:
+    """Quantized weights (several copies), x and y for the two decode shapes."""
+
+    def __init__(self, nv, torch, copies: int):
+        from synth import WORKLOADS, workload_inputs
+        self.shapes = []
+        for name in DECODE:
+            wl = WORKLOADS[name]
+            x, w = workload_inputs(name)
+            packed, _, swz, g = nv.quantize_weight(w.cuda())
+            del w
+            cps = [(packed, swz)] + [(packed.clone(), swz.clone()) for _ in range(copies - 1)]
+            ys = [torch.empty(1, wl.N, dtype=torch.bfloat16, device="cuda") for _ in range(copies)]
+            self.shapes.append(dict(name=name, M=1, K=wl.K, N=wl.N, x=x.cuda(), x_host=x,
+                                    g=g, copies=cps, ys=ys))
+        torch.cuda.synchronize()
+        self.copies = copies
+        self.bytes_per_step = sum(algo_bytes(s["M"], s["K"], s["N"]) for s in self.shapes)
+        self.bytes_per_launch = [algo_bytes(s["M"], s["K"], s["N"]) for s in self.shapes]
+
+
+def capture(torch, fn, nsteps):
+    """CUDA graph of nsteps calls of fn(step_index)."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for i in range(nsteps):  # warm the path outside the capture
+            fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for i in range(nsteps):
+            fn(i)
+    torch.cuda.synchronize()
+    return g
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import nvfp4_weight_quantized_quantize_gb300 as nv
+    from nvfp4_weight_quantized_quantize_gb300 import build_lib
+
+    build_lib.build()
+    nv.load()
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    setup = DecodeSetup(nv, torch, args.copies)
+    S = setup.shapes
+
+    def step(i, events=None):
+        c = i % setup.copies
+        for j, s in enumerate(S):
+            if events is not None:
+                events[2 * j].record()
+            nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c])
+            if events is not None:
+                events[2 * j + 1].record()
+
+    # timed region: a CUDA graph of G steps replayed, then EV eager steps with CUDA events
+    # around every launch (per-launch kernel durations for the roofline)
+    EV = min(8, args.steps)
+    KG = args.steps - EV
+    G = min(KG, 64) if KG > 0 else 0
+    while G > 1 and KG % G:
+        G -= 1
+    graph = capture(torch, step, G) if G else None
+    reps = KG // G if G else 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(S))] for _ in range(EV)]
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    if graph:
+        graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch, dev)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.4)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        graph.replay()
+    for i in range(EV):
+        step(KG + i, ev[i])
+    t1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = t0.elapsed_time(t1)
+    launch_ms = [e[2 * j].elapsed_time(e[2 * j + 1]) for e in ev for j in range(len(S))]
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    total_bytes = setup.bytes_per_step * args.steps * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+
+    # end to end: host x -> device, both calls, y -> host, every step
+    e2e = run_e2e(torch, nv, setup, args)
+
+    out = None
+    if rank == 0:
+        pk, pk_src = peaks()
+        avg_launch_s = statistics.mean(launch_ms) * 1e-3
+        achieved = statistics.mean(setup.bytes_per_launch) / avg_launch_s / 1e9
+        traffic = read_traffic()
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0,1) x, N(0,0.02) W with 0.1% x20 outliers)",
+            "config": {"workload": "decode M=1 W4A16 NVFP4: (K=5120,N=17408) + "
+                                   "(K=17408,N=5120), y bf16",
+                       "operands": "e2m1 weights + e4m3 per-16 scales + fp32 global, bf16 x, "
+                                   "fp32 accumulate",
+                       "bytes_per_step": setup.bytes_per_step,
+                       "l2": "inputs larger than L2: %d rotating weight copies (%.0f MB)"
+                             % (setup.copies, setup.bytes_per_step * setup.copies / 1e6),
+                       "parallelism": "replicas only (dp%d)" % world,
+                       "timing": "CUDA graph of %d steps replayed %d times + %d eager "
+                                 "steps with per-launch CUDA events" % (G, reps, EV)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / pk["hbm_gbs"], 4),
+                         "traffic": traffic, "peak_source": pk_src,
+                         "kernel": "gemv_w4a16_kernel<1>",
+                         "launch_us": round(avg_launch_s * 1e6, 2)},
+            "e2e": e2e,
+            "gpu_launches": len(S) * args.steps,
+            "clocks": clocks,
+        }
+        if args.rows:
+            out["rows"] = measure_rows(torch, nv, setup)
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return out
+
+
+def run_e2e(torch, nv, setup, args):
+    S = setup.shapes
+    xh = [s["x_host"].pin_memory() for s in S]
+    yh = [torch.empty(1, s["N"], dtype=torch.bfloat16).pin_memory() for s in S]
+
+    def step(i):
+        c = i % setup.copies
+        for j, s in enumerate(S):
+            s["x"].copy_(xh[j], non_blocking=True)
+            nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c])
+            yh[j].copy_(s["ys"][c], non_blocking=True)
+
+    n = min(args.steps, 2048)
+    G = min(n, 32)
+    while n % G:
+        G -= 1
+    graph = capture(torch, step, G)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n // G):
+        graph.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    h2d = sum(s["x"].numel() * 2 for s in S)
+    d2h = sum(s["N"] * 2 for s in S)
+    return {"value": round(setup.bytes_per_step * n / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def time_graph(torch, fn, nsteps, reps):
+    g = capture(torch, fn, nsteps)
+    g.replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / (nsteps * reps)  # ms per call
+
+
+def measure_rows(torch, nv, setup):
+    """Per-row throughput of the other hot-path steps (outside the timed region)."""
+    from synth import WORKLOADS, workload_inputs
+    rows = {}
+    # a1 quantize (fp32 weights) and a2 repack, decode_a shape
+    s = setup.shapes[0]
+    _, w = workload_inputs("decode_a")
+    wd = w.cuda()
+    N, K = wd.shape
+    packed = torch.empty(N, K // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(N, K // 16, dtype=torch.uint8, device="cuda")
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(nv.nvfp4_workspace_bytes(0, N, K), dtype=torch.uint8, device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_quantize(wd, packed, scales, g, ws), 4, 5)
+    qbytes = N * K * 4 + N * K // 2 + N * K // 16 + 4
+    rows["a1_quantize_fp32_17408x5120"] = {"GB/s": round(qbytes / ms / 1e6, 1),
+                                           "us": round(ms * 1e3, 1)}
+    swz = torch.empty(nv.nvfp4_repack_bytes(N, K), dtype=torch.uint8, device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_repack(scales, K, swz), 8, 5)
+    rows["a2_repack_17408x5120"] = {"GB/s": round(2 * N * K / 16 / ms / 1e6, 1),
+                                    "us": round(ms * 1e3, 1)}
+    del wd
+    for sh in setup.shapes:
+        ms = time_graph(torch, lambda i, sh=sh: nv.nvfp4_linear(
+            sh["x"], sh["copies"][i % setup.copies][0], sh["copies"][i % setup.copies][1],
+            sh["g"], sh["ys"][i % setup.copies]), 4 * setup.copies, 50)
+        b = algo_bytes(1, sh["K"], sh["N"])
+        rows["a3_decode_%s_K%d_N%d" % (sh["name"], sh["K"], sh["N"])] = {
+            "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
+    # a4 verify M=7 (W quantized on the GPU; 3 copies of the large shape)
+    for name in ("verify_a", "verify_b"):
+        wl = WORKLOADS[name]
+        x, w = workload_inputs(name)
+        p, _, z, gg = nv.quantize_weight(w.cuda())
+        del w
+        ncp = 3 if wl.N > 10000 else 12
+        cps = [(p, z)] + [(p.clone(), z.clone()) for _ in range(ncp - 1)]
+        xd = x.cuda()
+        y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+        ms = time_graph(torch, lambda i: nv.nvfp4_linear(xd, cps[i % ncp][0], cps[i % ncp][1],
+                                                         gg, y), 2 * ncp, 20)
+        b = algo_bytes(wl.M, wl.K, wl.N)
+        rows["a4_verify_%s_M7_K%d_N%d" % (name, wl.K, wl.N)] = {
+            "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
+        del cps, p, z
+    torch.cuda.synchronize()
+    return rows
+
+
+def read_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current source of the GEMV kernel (else null)."""
+    try:
+        txt = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    src = open(os.path.join(ROOT, "nvfp4_weight_quantized_quantize_gb300", "csrc",
+                            "gemv.cu"), "rb").read()
+    digest = hashlib.sha256(src).hexdigest()[:16]
+    fields = dict(ln.split(":", 1) for ln in txt.splitlines() if ":" in ln)
+    if fields.get("gemv_source_sha256_16", "").strip() != digest:
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
+# ---- the CPU oracle (cpu_baseline leg and the reference arm) ------------------------------
+
+def oracle_decode_inputs():
+    import oracle
+    from synth import workload_inputs
+    out = []
+    for name in DECODE:
+        x, w = workload_inputs(name)
+        wq, ws, gw = oracle.quantize(w.numpy())
+        out.append((x, wq, ws, gw))
+    return out
+
+
+def cpu_baseline(seconds: float = 10.0):
+    import oracle
+    data = oracle_decode_inputs()
+    nbytes = sum(algo_bytes(1, x.shape[1], wq.shape[0]) for x, wq, _, _ in data)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for x, wq, ws, gw in data:
+            oracle.linear_w4a16(x, wq, ws, gw)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": round(nbytes * reps / el / 1e9, 3), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d full passes over both decode shapes (M=1, all N outputs, fp64)"
+                      % reps}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    data = oracle_decode_inputs()
+    rows_per_shape = 32
+    rng = np.random.default_rng(0)
+    picks = [rng.integers(0, wq.shape[0], rows_per_shape) for _, wq, _, _ in data]
+    nbytes = sum(algo_bytes(1, x.shape[1], rows_per_shape) for x, _, _, _ in data)
+
+    def step():
+        for (x, wq, ws, gw), pn in zip(data, picks):
+            oracle.linear_w4a16_pairs(x, wq, ws, gw, np.zeros_like(pn), pn)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = nbytes * args.steps / el / 1e9
+    sample = ("%d output rows of each decode shape per step (bytes of those rows: nibbles, "
+              "scales, x, y)" % rows_per_shape)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode M=1 W4A16 NVFP4: (K=5120,N=17408) + "
+                                   "(K=17408,N=5120), y bf16", "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle",
+                             "cores": oracle.num_threads(), "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=256)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--copies", type=int, default=4)
+    ap.add_argument("--rows", type=int, default=1, help="also measure the other rows")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as tdist
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            tdist.init_process_group("nccl")
+            dist = tdist
+        out = run_ours(args, rank, world, dist)
+        if dist:
+            dist.destroy_process_group()
+    if out is not None and rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

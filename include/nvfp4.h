@@ -1,0 +1,189 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 block-scaled projection library.
+ *
+ * The hot path of batch-one Qwen3.x serving is the NVFP4 weight projection
+ * y[M,N] = x[M,K] . W^T, run at decode (M = 1), MTP verify (M = K + 1 drafts) and on
+ * prefill chunks (Qwen3x-Orin README, Functional evaluation quick start:
+ * "--projection-backend sm87", "--prefill-chunk-size 512"; FlashRT
+ * docs/qwen36_usage.md, generate_own_speculative_KN_nvfp4 argument table and the
+ * per-step decode section).  The weights are NVFP4 ("compressed-tensors
+ * nvfp4-pack-quantized", FlashRT constructor argument table): E2M1 codes packed
+ * two per byte, one E4M3 scale per 16 consecutive K elements of a row, one FP32
+ * global scale.  The format is named, not defined, on those pages; this library
+ * uses its standard definition:
+ *   value(n, k) = e2m1(q[n,k]) * e4m3(s[n, k/16]) * g,   g = amax / (6 * 448).
+ *
+ * Conventions shared by every call
+ *   - All tensor arguments are device pointers into caller-owned memory of the
+ *     current CUDA device; the library allocates nothing and keeps no state other
+ *     than a per-device cache of the device's properties.
+ *   - Every pointer argument must be 16-byte aligned, except `global_scale`,
+ *     `w_global_scale` and `x_global_scale`, which need 4-byte alignment.
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream); no call
+ *     synchronizes.  Calls on distinct streams are thread-safe.
+ *   - Arguments are checked on the host before anything is enqueued; a failed
+ *     check returns its status and enqueues nothing.  A CUDA launch error is
+ *     returned as NVFP4_ERR_CUDA.
+ *   - The device must be compute capability 10.3 (GB300, sm_103a); otherwise
+ *     NVFP4_ERR_DEVICE.
+ *   - Layouts: x [M,K] bf16 row-major; packed weights [N, K/2] bytes row-major,
+ *     byte j of a row = code(2j) | code(2j+1) << 4; row-major scales [N, K/16]
+ *     E4M3 bytes; y [M,N] row-major fp32 or bf16.
+ *   - Workspace: a caller-owned device buffer of at least the size that
+ *     nvfp4_workspace_bytes() returns.  Its first 4 bytes are a sticky error word:
+ *     zero-fill the workspace once when it is allocated; kernels only OR error
+ *     bits into it (never clear it), see nvfp4_workspace_error().
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvfp4_stream_t; /* the same handle as cudaStream_t */
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_NULL = 1,        /* a required pointer is NULL */
+    NVFP4_ERR_SHAPE = 2,       /* a size is out of range or not a required multiple */
+    NVFP4_ERR_ALIGN = 3,       /* a pointer is not aligned as required */
+    NVFP4_ERR_DTYPE = 4,       /* unknown dtype or mode */
+    NVFP4_ERR_WORKSPACE = 5,   /* workspace missing or too small */
+    NVFP4_ERR_DEVICE = 6,      /* current device is not sm_103 */
+    NVFP4_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
+    NVFP4_ERR_TIMEOUT = 8,     /* a device-side bounded wait ran out (error word) */
+    NVFP4_ERR_UNSUPPORTED = 9  /* valid arguments, but no kernel for this case */
+} nvfp4_status;
+
+typedef enum { NVFP4_F32 = 0, NVFP4_BF16 = 1 } nvfp4_dtype;
+typedef enum { NVFP4_W4A16 = 0, NVFP4_W4A4 = 1 } nvfp4_mode;
+
+/* error-word bits (see nvfp4_workspace_error) */
+#define NVFP4_DEVERR_TIMEOUT 0x1u
+
+/*
+ * nvfp4_quantize -- FP32/BF16 weights to NVFP4.
+ *
+ * Defines: the load-time weight conversion to NVFP4 (FlashRT docs/qwen36_usage.md,
+ * constructor paragraph and env-var table FLASHRT_QWEN36_MTP_CKPT_DIR, FP8 -> BF16
+ * -> NVFP4 at load).  Steps, all in fp32 round-to-nearest-even:
+ *   1. amax = max |src|;  g = amax / 2688 (g = 1 when amax == 0).
+ *   2. per row and 16-element block: bmax = max |src|;  s = E4M3(bmax / (6 g)),
+ *      round to nearest even, saturating at 448.
+ *   3. d = e4m3(s) * g; code = E2M1(src / d) (nearest of {0,.5,1,1.5,2,3,4,6},
+ *      ties to the even code, |v| >= 6 -> 6, sign bit of the input kept);
+ *      d == 0 gives a signed zero code.
+ * Arguments:
+ *   src          [rows, cols] row-major, dtype src_dtype (NVFP4_F32 or NVFP4_BF16);
+ *                all values finite (non-finite input gives unspecified codes).
+ *   rows, cols   rows >= 1, cols >= 16, cols % 16 == 0.
+ *   packed       out [rows, cols/2] bytes.
+ *   scales       out [rows, cols/16] E4M3 bytes, row-major (nvfp4_repack makes the
+ *                kernel layout from it).
+ *   global_scale out, one float g (device memory).
+ *   workspace    >= nvfp4_workspace_bytes(0, rows, cols, 0, 0) bytes (amax
+ *                partials; contents need not be initialised).
+ * Two kernels are enqueued; the result is bit-exact with the CPU reference.
+ */
+nvfp4_status nvfp4_quantize(const void* src, nvfp4_dtype src_dtype, int64_t rows,
+                            int64_t cols, uint8_t* packed, uint8_t* scales,
+                            float* global_scale, void* workspace, size_t workspace_bytes,
+                            nvfp4_stream_t stream);
+
+/*
+ * nvfp4_repack -- row-major E4M3 scales to the kernels' swizzled layout.
+ *
+ * Defines: the load-time "NVFP4 swizzle" (FlashRT docs/qwen36_usage.md, constructor
+ * paragraph).  The target is the tensor-core block-scale layout for 16-element
+ * blocks: rows padded to Rp = 128*ceil(rows/128) and blocks to Cp = 4*ceil(Cb/4)
+ * (Cb = cols/16) with zero bytes; element (r, cb) goes to byte
+ *   ((r/128)*(Cp/4) + cb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + cb%4.
+ * Arguments:
+ *   scales_rowmajor  [rows, cols/16] bytes.  rows >= 1, cols >= 16, cols % 16 == 0.
+ *   scales_swizzled  out, exactly swizzled_bytes == nvfp4_repack_bytes(rows, cols).
+ * The output must not overlap the input.
+ */
+nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t cols,
+                          uint8_t* scales_swizzled, size_t swizzled_bytes,
+                          nvfp4_stream_t stream);
+
+/*
+ * nvfp4_linear -- y[M,N] = x[M,K] . W^T with NVFP4 W.
+ *
+ * Defines: the NVFP4 projection at decode, MTP verify and prefill (Qwen3x-Orin
+ * README, quick start; FlashRT docs/qwen36_usage.md, speculative and per-step decode
+ * sections), including the fused gate/up shape with one shared global scale
+ * (env-var table, FLASHRT_QWEN36_FUSE_MLP_GATE_UP) and NVFP4 activations
+ * (FLASHRT_QWEN36_FUSE_SILU_MUL_QUANT).
+ *   W4A16: y[m,n] = g_w * sum_b s[n,b] * sum_{k in b} x[m,k] * e2m1(q[n,k]).
+ *   W4A4:  x is first quantized like nvfp4_quantize (global scale = its amax / 2688,
+ *          or *x_global_scale when given) into the workspace; then
+ *          y = g_x g_w * sum_b sx[m,b] sw[n,b] sum_{k in b} e2m1(qx) e2m1(qw).
+ * Accumulation is fp32.  Expected accuracy: |y - y_ref| <= 1e-3 * sum_k |x_k w_k|
+ * + 2^-8 |y_ref| for bf16 y.
+ * Arguments:
+ *   x                  [M, K] bf16.  M >= 1, K >= 32, K % 32 == 0.
+ *   w_packed           [N, K/2] bytes (nvfp4_quantize output).  N >= 1.
+ *   w_scales_swizzled  nvfp4_repack_bytes(N, K) bytes (nvfp4_repack output).
+ *   w_global_scale     one float (device).
+ *   y                  out [M, N], dtype y_dtype (NVFP4_F32 or NVFP4_BF16).
+ *   mode               NVFP4_W4A16 or NVFP4_W4A4.
+ *   x_global_scale     W4A4 only: NULL = dynamic (amax of x), else one float
+ *                      (device, finite, > 0).  Must be NULL for W4A16.
+ *   workspace          >= nvfp4_workspace_bytes(1, M, K, N, mode) bytes, zero-filled
+ *                      once at allocation (sticky error word); may be NULL when that
+ *                      size is 0.  Calls that share a workspace must be ordered (one
+ *                      stream), since W4A4 keeps the quantized x there.
+ */
+nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K, const uint8_t* w_packed,
+                          const uint8_t* w_scales_swizzled, const float* w_global_scale,
+                          int64_t N, void* y, nvfp4_dtype y_dtype, nvfp4_mode mode,
+                          const float* x_global_scale, void* workspace,
+                          size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* ---- host-only helpers: no device work ---------------------------------------- */
+
+/* Bytes of the swizzled scale layout for a [rows, cols] tensor (0 on bad sizes). */
+size_t nvfp4_repack_bytes(int64_t rows, int64_t cols);
+
+/* Workspace bytes: op 0 = nvfp4_quantize(rows=M, cols=K), op 1 = nvfp4_linear(M, K,
+ * N, mode).  0 when no workspace is needed; (size_t)-1 on bad arguments. */
+size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N, nvfp4_mode mode);
+
+/* Where nvfp4_linear in W4A4 mode leaves the quantized activations inside its
+ * workspace: packed codes [M, K/2] at *xq_offset, swizzled scales
+ * (nvfp4_repack_bytes(M, K) bytes) at *xs_offset and g_x (one float) at
+ * *gx_offset.  They are valid once the call has completed.  Returns NVFP4_OK or
+ * NVFP4_ERR_SHAPE. */
+nvfp4_status nvfp4_w4a4_workspace_layout(int64_t M, int64_t K, size_t* xq_offset,
+                                         size_t* xs_offset, size_t* gx_offset);
+
+/* Reads (and then clears) the sticky error word of a workspace after `stream` has
+ * drained: synchronizes `stream`.  *bits gets NVFP4_DEVERR_* bits; returns
+ * NVFP4_ERR_TIMEOUT if any bit was set, NVFP4_OK otherwise. */
+nvfp4_status nvfp4_workspace_error(void* workspace, nvfp4_stream_t stream, uint32_t* bits);
+
+/* Human-readable name of a status. */
+const char* nvfp4_status_str(nvfp4_status status);
+
+/* ---- diagnostics -------------------------------------------------------------- */
+
+/*
+ * nvfp4_encode_elements -- the device's element rounding on its own: for each of n
+ * fp32 inputs, e2m1_out[i] = E2M1 code (as nvfp4_quantize step 3 rounds src/d) and
+ * e4m3_out[i] = E4M3 byte of max(in[i], 0) (as step 2 rounds a block scale).  It runs
+ * the same device functions the quantizer uses, so that their rounding can be
+ * checked over every fp32 bit pattern.  Either output may be NULL.  n >= 0.
+ */
+nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out,
+                                   uint8_t* e4m3_out, nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H_ */

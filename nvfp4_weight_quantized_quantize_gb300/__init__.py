@@ -1,0 +1,179 @@
+"""Python binding of libnvfp4.so (include/nvfp4.h) -- argument marshalling only.
+
+Every function has the name of the C entry point it calls, takes torch tensors (device
+memory of the current CUDA device) and raises ``Nvfp4Error`` on a non-OK status.  All
+compute runs in the library's CUDA kernels; there is no other path: if the library
+is missing, importing the functions' backend raises.
+
+  nvfp4_quantize(src, packed, scales, global_scale, workspace)      weights -> NVFP4
+  nvfp4_repack(scales, cols, out)                                   scale swizzle
+  nvfp4_linear(x, w_packed, w_scales_swizzled, w_global_scale, y,
+               mode="w4a16"|"w4a4", x_global_scale=None, workspace=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libnvfp4.so")
+
+NVFP4_F32, NVFP4_BF16 = 0, 1
+NVFP4_W4A16, NVFP4_W4A4 = 0, 1
+STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ERR_ALIGN",
+          4: "NVFP4_ERR_DTYPE", 5: "NVFP4_ERR_WORKSPACE", 6: "NVFP4_ERR_DEVICE",
+          7: "NVFP4_ERR_CUDA", 8: "NVFP4_ERR_TIMEOUT", 9: "NVFP4_ERR_UNSUPPORTED"}
+EXPORTS = ("nvfp4_quantize", "nvfp4_repack", "nvfp4_linear", "nvfp4_repack_bytes",
+           "nvfp4_workspace_bytes", "nvfp4_w4a4_workspace_layout", "nvfp4_workspace_error",
+           "nvfp4_status_str", "nvfp4_encode_elements")
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, STATUS.get(status, str(status))))
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libnvfp4.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libnvfp4.so is not built (%s); run "
+                           "`python -m nvfp4_weight_quantized_quantize_gb300.build_lib`" % path)
+    lib = ctypes.CDLL(path)
+    P, I64, SZ, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+    sig = {
+        "nvfp4_quantize": (I, [P, I, I64, I64, P, P, P, P, SZ, P]),
+        "nvfp4_repack": (I, [P, I64, I64, P, SZ, P]),
+        "nvfp4_linear": (I, [P, I64, I64, P, P, P, I64, P, I, I, P, P, SZ, P]),
+        "nvfp4_repack_bytes": (SZ, [I64, I64]),
+        "nvfp4_workspace_bytes": (SZ, [I, I64, I64, I64, I]),
+        "nvfp4_w4a4_workspace_layout": (I, [I64, I64, ctypes.POINTER(SZ), ctypes.POINTER(SZ),
+                                            ctypes.POINTER(SZ)]),
+        "nvfp4_workspace_error": (I, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
+        "nvfp4_status_str": (ctypes.c_char_p, [I]),
+        "nvfp4_encode_elements": (I, [P, I64, P, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise Nvfp4Error(st, where)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return NVFP4_F32
+    if dt == torch.bfloat16:
+        return NVFP4_BF16
+    raise ValueError("unsupported dtype %s" % dt)
+
+
+# ---- host helpers -------------------------------------------------------------------
+
+def nvfp4_status_str(status: int) -> str:
+    return load().nvfp4_status_str(status).decode()
+
+
+def nvfp4_repack_bytes(rows: int, cols: int) -> int:
+    return int(load().nvfp4_repack_bytes(rows, cols))
+
+
+def nvfp4_workspace_bytes(op: int, M: int, K: int, N: int = 0, mode: int = NVFP4_W4A16) -> int:
+    return int(load().nvfp4_workspace_bytes(op, M, K, N, mode))
+
+
+def nvfp4_w4a4_workspace_layout(M: int, K: int):
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().nvfp4_w4a4_workspace_layout(M, K, ctypes.byref(a), ctypes.byref(b),
+                                              ctypes.byref(c)), "nvfp4_w4a4_workspace_layout")
+    return a.value, b.value, c.value
+
+
+def nvfp4_workspace_error(workspace: torch.Tensor, stream=None) -> int:
+    bits = ctypes.c_uint32(0)
+    st = load().nvfp4_workspace_error(_p(workspace), _stream(stream), ctypes.byref(bits))
+    if st not in (0, 8):
+        _check(st, "nvfp4_workspace_error")
+    return bits.value
+
+
+# ---- the three calls -----------------------------------------------------------------
+
+def nvfp4_quantize(src: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                   global_scale: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    rows, cols = src.shape
+    st = load().nvfp4_quantize(_p(src), _dtype_code(src.dtype), rows, cols, _p(packed),
+                               _p(scales), _p(global_scale), _p(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nvfp4_quantize")
+
+
+def nvfp4_repack(scales: torch.Tensor, cols: int, out: torch.Tensor, stream=None) -> None:
+    rows = scales.shape[0]
+    st = load().nvfp4_repack(_p(scales), rows, cols, _p(out), out.numel() * out.element_size(),
+                             _stream(stream))
+    _check(st, "nvfp4_repack")
+
+
+def nvfp4_linear(x: torch.Tensor, w_packed: torch.Tensor, w_scales_swizzled: torch.Tensor,
+                 w_global_scale: torch.Tensor, y: torch.Tensor, mode: str = "w4a16",
+                 x_global_scale: torch.Tensor | None = None,
+                 workspace: torch.Tensor | None = None, stream=None) -> None:
+    M, K = x.shape
+    N = w_packed.shape[0]
+    m = {"w4a16": NVFP4_W4A16, "w4a4": NVFP4_W4A4}[mode]
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().nvfp4_linear(_p(x), M, K, _p(w_packed), _p(w_scales_swizzled),
+                             _p(w_global_scale), N, _p(y), _dtype_code(y.dtype), m,
+                             _p(x_global_scale), _p(workspace), wsb, _stream(stream))
+    _check(st, "nvfp4_linear")
+
+
+def nvfp4_encode_elements(inp: torch.Tensor, e2m1_out: torch.Tensor | None,
+                          e4m3_out: torch.Tensor | None, stream=None) -> None:
+    st = load().nvfp4_encode_elements(_p(inp), inp.numel(), _p(e2m1_out), _p(e4m3_out),
+                                      _stream(stream))
+    _check(st, "nvfp4_encode_elements")
+
+
+# ---- convenience: allocate outputs with torch and run the calls -----------------------
+
+def quantize_weight(w: torch.Tensor, stream=None):
+    """Quantize + repack a device weight [N, K]; returns (packed, scales_rowmajor,
+    scales_swizzled, global_scale)."""
+    N, K = w.shape
+    dev = w.device
+    packed = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(N, K // 16, dtype=torch.uint8, device=dev)
+    g = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = torch.empty(nvfp4_workspace_bytes(0, N, K), dtype=torch.uint8, device=dev)
+    nvfp4_quantize(w, packed, scales, g, ws, stream)
+    swz = torch.empty(nvfp4_repack_bytes(N, K), dtype=torch.uint8, device=dev)
+    nvfp4_repack(scales, K, swz, stream)
+    return packed, scales, swz, g

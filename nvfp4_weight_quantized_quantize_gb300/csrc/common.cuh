@@ -1,0 +1,110 @@
+// common.cuh -- device helpers shared by the NVFP4 kernels (sm_103a).
+//
+// Element formats (the pages name NVFP4 -- Qwen3x-Orin README, Repository map;
+// FlashRT docs/qwen36_usage.md, constructor argument table -- without defining it;
+// the standard definition is used): E2M1 codes s.e1e0.m with magnitudes
+// {0, .5, 1, 1.5, 2, 3, 4, 6}; E4M3 (OCP E4M3FN) block scales, bias 7, max 448.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+// ---- element rounding (the quantizer's steps 2 and 3) ----------------------------
+
+// E2M1 code of v: nearest magnitude, ties to the even code, |v| >= 6 -> 6, and the
+// sign bit of v.  The seven decision points are the midpoints between neighbouring
+// magnitudes; at a midpoint the comparison is strict when the lower neighbour has the
+// even code (0.25, 1.25, 2.5, 5) and inclusive when the upper one has (0.75, 1.75, 3.5).
+__device__ __forceinline__ uint32_t e2m1_encode(float v) {
+    const float a = fabsf(v);
+    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+                 (a >= 3.5f) + (a > 5.0f);
+    return c | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// E4M3 byte of a non-negative float: hardware round-to-nearest-even with saturation
+// to the largest finite value (448, 0x7E).  The low byte of the x2 result holds the
+// second source operand.
+__device__ __forceinline__ uint32_t e4m3_encode_nonneg(float s) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(s));
+    return (uint32_t)r & 0xFFu;
+}
+
+// Value of a non-negative finite E4M3 byte (0x00..0x7E), exact.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    return e ? __uint_as_float(((e + 120u) << 23) | (m << 20))
+             : (float)m * 0.001953125f;  // m * 2^-9
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+
+// fp32 -> bf16 bits, round to nearest even (inputs are finite).
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+    uint32_t u = __float_as_uint(f);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+// Global scale from the tensor's amax: amax / (6 * 448), or 1 for an all-zero tensor.
+__device__ __forceinline__ float global_scale_from_amax(float amax) {
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+}
+
+// Quantize one block of 16 fp32 values with global scale g.  Returns the E4M3 scale
+// byte; `lo`/`hi` get the 8 packed bytes (element 2j in the low nibble of byte j).
+// Every step is one correctly rounded fp32 operation, in the reference's order:
+// s_raw = bmax / (6 g), d = e4m3(s) * g, v = t / d.
+__device__ __forceinline__ uint32_t quantize_block16(const float (&t)[16], float g,
+                                                     uint32_t& lo, uint32_t& hi) {
+    float bmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(t[i]));
+    const float s_raw = __fdiv_rn(bmax, __fmul_rn(6.0f, g));
+    const uint32_t s8 = e4m3_encode_nonneg(s_raw);
+    const float d = __fmul_rn(e4m3_to_f32(s8), g);
+    lo = 0u;
+    hi = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t code = (d == 0.0f) ? ((__float_as_uint(t[i]) >> 28) & 8u)
+                                          : e2m1_encode(__fdiv_rn(t[i], d));
+        if (i < 8) lo |= code << (4 * i);
+        else hi |= code << (4 * (i - 8));
+    }
+    return s8;
+}
+
+// ---- swizzled scale layout ---------------------------------------------------------
+// Tensor-core block-scale layout for 16-element blocks: 512-byte atoms of 128 rows x 4
+// scale columns; line (r % 32) of 16 bytes holds rows r%32 + {0,32,64,96}, 4 bytes each;
+// atoms advance along K first.  cp4 = number of 4-column groups = ceil(Cb / 4).
+__host__ __device__ __forceinline__ int64_t swizzle_offset(int64_t r, int64_t cb,
+                                                           int64_t cp4) {
+    return ((r >> 7) * cp4 + (cb >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 +
+           (cb & 3);
+}
+
+// ---- loads ---------------------------------------------------------------------------
+
+// Streaming 16-byte load that bypasses L1 allocation (weights are read once).
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u16(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+}  // namespace nvfp4

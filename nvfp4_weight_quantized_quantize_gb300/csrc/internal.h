@@ -1,0 +1,45 @@
+// internal.h -- host-side launchers shared between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvfp4 {
+
+struct DevInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;  // max dynamic shared memory per block (opt-in)
+};
+
+// Number of amax partials the quantizer's first pass writes for `n_elems` inputs.
+int amax_partial_count(int64_t n_elems, int sm_count);
+
+// Quantizer: amax partials (skipped when given_g != nullptr), then one thread per
+// 16-element block.  Scales go row-major [rows, cols/16] or, with swizzled_scales,
+// to the swizzled layout (padding written as zero).  deq_bf16 (optional) receives
+// e2m1(code) * e4m3(scale) -- the dequantized value without the global scale -- as
+// bf16 [rows, cols].
+cudaError_t launch_quantize(const void* src, bool src_bf16, int64_t rows, int64_t cols,
+                            uint8_t* packed, uint8_t* scales, bool swizzled_scales,
+                            float* g_out, const float* given_g, float* partials,
+                            int npartials, uint16_t* deq_bf16, cudaStream_t stream,
+                            const DevInfo& dev);
+
+cudaError_t launch_repack(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out,
+                          cudaStream_t stream, const DevInfo& dev);
+
+cudaError_t launch_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out,
+                                   uint8_t* e4m3_out, cudaStream_t stream,
+                                   const DevInfo& dev);
+
+// Small-M (M <= 16) W4A16 GEMV / skinny GEMM.  y = (gx ? *gx : 1) * *gw * x . W^T.
+cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
+                              const uint8_t* wsz, const float* gw, const float* gx, int N,
+                              void* y, bool y_bf16, cudaStream_t stream, const DevInfo& dev);
+
+constexpr int kGemvMaxM = 16;
+
+}  // namespace nvfp4

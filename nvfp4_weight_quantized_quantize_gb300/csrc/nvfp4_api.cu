@@ -1,0 +1,248 @@
+// nvfp4_api.cu -- the C ABI (include/nvfp4.h): argument checks on the host, the
+// per-device property cache, workspace layout and kernel dispatch.  Nothing here
+// allocates device memory or synchronizes (except nvfp4_workspace_error, which says
+// so).
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/nvfp4.h"
+#include "internal.h"
+
+#define NVFP4_API extern "C" __attribute__((visibility("default")))
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kHeaderBytes = 256;      // sticky error word + reserved
+constexpr int kMaxPartials = 2048;        // amax partials (>= 8 per SM on any GPU here)
+
+std::mutex g_dev_mu;
+DevInfo g_dev[kMaxDevices];
+
+nvfp4_status current_device(DevInfo* out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (g_dev[dev].device != dev) {
+            DevInfo d;
+            d.device = dev;
+            int v = 0;
+            if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) !=
+                    cudaSuccess ||
+                cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                    cudaSuccess ||
+                cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                    cudaSuccess ||
+                cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                    cudaSuccess) {
+                cudaGetLastError();
+                return NVFP4_ERR_CUDA;
+            }
+            d.smem_optin = (size_t)v;
+            g_dev[dev] = d;
+        }
+        *out = g_dev[dev];
+    }
+    if (out->cc_major != 10 || out->cc_minor != 3) return NVFP4_ERR_DEVICE;
+    return NVFP4_OK;
+}
+
+inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+inline nvfp4_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return NVFP4_OK;
+    return NVFP4_ERR_CUDA;
+}
+
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t repack_bytes(int64_t rows, int64_t cols) {
+    const int64_t rp = (rows + 127) / 128 * 128;
+    const int64_t cp = (cols / 16 + 3) / 4 * 4;
+    return (size_t)(rp * cp);
+}
+
+int partial_count(int64_t n, const DevInfo& d) {
+    int p = amax_partial_count(n, d.sm_count);
+    return p > kMaxPartials ? kMaxPartials : p;
+}
+
+// W4A4 workspace: header | xq [M, K/2] | xs swizzled | gx (16 B) | partials | deq bf16
+struct W4A4Layout {
+    size_t xq, xs, gx, partials, deq, total;
+};
+
+W4A4Layout w4a4_layout(int64_t M, int64_t K) {
+    W4A4Layout L;
+    L.xq = kHeaderBytes;
+    L.xs = round_up(L.xq + (size_t)(M * K / 2), 256);
+    L.gx = round_up(L.xs + repack_bytes(M, K), 256);
+    L.partials = L.gx + 256;
+    L.deq = round_up(L.partials + (size_t)kMaxPartials * 4, 256);
+    L.total = L.deq + (M <= kGemvMaxM ? (size_t)(M * K * 2) : 0);
+    return L;
+}
+
+constexpr int64_t kMaxDim = (int64_t)1 << 30;
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+NVFP4_API const char* nvfp4_status_str(nvfp4_status s) {
+    switch (s) {
+        case NVFP4_OK: return "NVFP4_OK";
+        case NVFP4_ERR_NULL: return "NVFP4_ERR_NULL: a required pointer is NULL";
+        case NVFP4_ERR_SHAPE: return "NVFP4_ERR_SHAPE: a size is out of range";
+        case NVFP4_ERR_ALIGN: return "NVFP4_ERR_ALIGN: a pointer is misaligned";
+        case NVFP4_ERR_DTYPE: return "NVFP4_ERR_DTYPE: unknown dtype or mode";
+        case NVFP4_ERR_WORKSPACE: return "NVFP4_ERR_WORKSPACE: workspace missing or too small";
+        case NVFP4_ERR_DEVICE: return "NVFP4_ERR_DEVICE: the current device is not sm_103";
+        case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA: a CUDA call failed";
+        case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT: a device-side wait ran out";
+        case NVFP4_ERR_UNSUPPORTED: return "NVFP4_ERR_UNSUPPORTED: no kernel for this case";
+    }
+    return "unknown nvfp4_status";
+}
+
+NVFP4_API size_t nvfp4_repack_bytes(int64_t rows, int64_t cols) {
+    if (rows < 1 || cols < 16 || cols % 16 != 0 || rows > kMaxDim || cols > kMaxDim) return 0;
+    return repack_bytes(rows, cols);
+}
+
+NVFP4_API size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
+                                       nvfp4_mode mode) {
+    if (op == 0) {
+        if (M < 1 || K < 16 || K % 16 != 0) return (size_t)-1;
+        return kHeaderBytes + (size_t)kMaxPartials * 4;
+    }
+    if (op != 1 || M < 1 || K < 32 || K % 32 != 0 || N < 1) return (size_t)-1;
+    if (mode == NVFP4_W4A16) return M <= kGemvMaxM ? 0 : kHeaderBytes;
+    if (mode == NVFP4_W4A4) return w4a4_layout(M, K).total;
+    return (size_t)-1;
+}
+
+NVFP4_API nvfp4_status nvfp4_w4a4_workspace_layout(int64_t M, int64_t K, size_t* xq_offset,
+                                                   size_t* xs_offset, size_t* gx_offset) {
+    if (M < 1 || K < 32 || K % 32 != 0) return NVFP4_ERR_SHAPE;
+    const W4A4Layout L = w4a4_layout(M, K);
+    if (xq_offset) *xq_offset = L.xq;
+    if (xs_offset) *xs_offset = L.xs;
+    if (gx_offset) *gx_offset = L.gx;
+    return NVFP4_OK;
+}
+
+NVFP4_API nvfp4_status nvfp4_workspace_error(void* workspace, nvfp4_stream_t stream,
+                                             uint32_t* bits) {
+    if (!workspace || !bits) return NVFP4_ERR_NULL;
+    uint32_t w = 0;
+    cudaError_t e = cudaMemcpyAsync(&w, workspace, 4, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && w != 0) {
+        e = cudaMemsetAsync(workspace, 0, 4, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    }
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    *bits = w;
+    return w ? NVFP4_ERR_TIMEOUT : NVFP4_OK;
+}
+
+NVFP4_API nvfp4_status nvfp4_quantize(const void* src, nvfp4_dtype src_dtype, int64_t rows,
+                                      int64_t cols, uint8_t* packed, uint8_t* scales,
+                                      float* global_scale, void* workspace,
+                                      size_t workspace_bytes, nvfp4_stream_t stream) {
+    if (!src || !packed || !scales || !global_scale || !workspace) return NVFP4_ERR_NULL;
+    if (src_dtype != NVFP4_F32 && src_dtype != NVFP4_BF16) return NVFP4_ERR_DTYPE;
+    if (rows < 1 || cols < 16 || cols % 16 != 0 || rows > kMaxDim || cols > kMaxDim)
+        return NVFP4_ERR_SHAPE;
+    if (!aligned(src, 16) || !aligned(packed, 16) || !aligned(scales, 16) ||
+        !aligned(workspace, 16) || !aligned(global_scale, 4))
+        return NVFP4_ERR_ALIGN;
+    if (workspace_bytes < nvfp4_workspace_bytes(0, rows, cols, 0, NVFP4_W4A16))
+        return NVFP4_ERR_WORKSPACE;
+    DevInfo d;
+    nvfp4_status st = current_device(&d);
+    if (st != NVFP4_OK) return st;
+    float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kHeaderBytes);
+    return from_cuda(launch_quantize(src, src_dtype == NVFP4_BF16, rows, cols, packed, scales,
+                                     false, global_scale, nullptr, partials,
+                                     partial_count(rows * cols, d), nullptr, stream, d));
+}
+
+NVFP4_API nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t cols,
+                                    uint8_t* scales_swizzled, size_t swizzled_bytes,
+                                    nvfp4_stream_t stream) {
+    if (!scales_rowmajor || !scales_swizzled) return NVFP4_ERR_NULL;
+    if (rows < 1 || cols < 16 || cols % 16 != 0 || rows > kMaxDim || cols > kMaxDim)
+        return NVFP4_ERR_SHAPE;
+    if (swizzled_bytes != repack_bytes(rows, cols)) return NVFP4_ERR_SHAPE;
+    if (!aligned(scales_rowmajor, 16) || !aligned(scales_swizzled, 16)) return NVFP4_ERR_ALIGN;
+    DevInfo d;
+    nvfp4_status st = current_device(&d);
+    if (st != NVFP4_OK) return st;
+    return from_cuda(launch_repack(scales_rowmajor, rows, cols, scales_swizzled, stream, d));
+}
+
+NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
+                                    const uint8_t* w_packed, const uint8_t* w_scales_swizzled,
+                                    const float* w_global_scale, int64_t N, void* y,
+                                    nvfp4_dtype y_dtype, nvfp4_mode mode,
+                                    const float* x_global_scale, void* workspace,
+                                    size_t workspace_bytes, nvfp4_stream_t stream) {
+    if (!x || !w_packed || !w_scales_swizzled || !w_global_scale || !y) return NVFP4_ERR_NULL;
+    if (y_dtype != NVFP4_F32 && y_dtype != NVFP4_BF16) return NVFP4_ERR_DTYPE;
+    if (mode != NVFP4_W4A16 && mode != NVFP4_W4A4) return NVFP4_ERR_DTYPE;
+    if (mode == NVFP4_W4A16 && x_global_scale) return NVFP4_ERR_DTYPE;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return NVFP4_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(w_scales_swizzled, 16) ||
+        !aligned(y, 16) || !aligned(w_global_scale, 4) ||
+        (x_global_scale && !aligned(x_global_scale, 4)) || (workspace && !aligned(workspace, 16)))
+        return NVFP4_ERR_ALIGN;
+    const size_t need = nvfp4_workspace_bytes(1, M, K, N, mode);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return NVFP4_ERR_WORKSPACE;
+    DevInfo d;
+    nvfp4_status st = current_device(&d);
+    if (st != NVFP4_OK) return st;
+    const bool ybf = y_dtype == NVFP4_BF16;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+
+    if (mode == NVFP4_W4A16) {
+        if (M <= kGemvMaxM)
+            return from_cuda(launch_gemv_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                               w_global_scale, nullptr, (int)N, y, ybf, stream,
+                                               d));
+        return NVFP4_ERR_UNSUPPORTED;
+    }
+    // W4A4: quantize x into the workspace (bit-exact with nvfp4_quantize + nvfp4_repack)
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const W4A4Layout L = w4a4_layout(M, K);
+    float* gx = reinterpret_cast<float*>(ws + L.gx);
+    uint16_t* deq = M <= kGemvMaxM ? reinterpret_cast<uint16_t*>(ws + L.deq) : nullptr;
+    cudaError_t e = launch_quantize(x, true, M, K, ws + L.xq, ws + L.xs, true, gx,
+                                    x_global_scale, reinterpret_cast<float*>(ws + L.partials),
+                                    partial_count(M * K, d), deq, stream, d);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (M <= kGemvMaxM)
+        return from_cuda(launch_gemv_w4a16(deq, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                           w_global_scale, gx, (int)N, y, ybf, stream, d));
+    return NVFP4_ERR_UNSUPPORTED;
+}
+
+NVFP4_API nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out,
+                                             uint8_t* e4m3_out, nvfp4_stream_t stream) {
+    if (!in && n > 0) return NVFP4_ERR_NULL;
+    if (n < 0) return NVFP4_ERR_SHAPE;
+    if (!aligned(in, 4)) return NVFP4_ERR_ALIGN;
+    DevInfo d;
+    nvfp4_status st = current_device(&d);
+    if (st != NVFP4_OK) return st;
+    return from_cuda(launch_encode_elements(in, n, e2m1_out, e4m3_out, stream, d));
+}

@@ -1,0 +1,258 @@
+// quantize.cu -- NVFP4 quantizer (weights at load time, activations per call), the
+// scale repack into the tensor-core layout, and the element-rounding diagnostic.
+//
+// The load-time conversion to NVFP4 and its "NVFP4 swizzle" are named by FlashRT
+// docs/qwen36_usage.md (constructor paragraph; env-var table,
+// FLASHRT_QWEN36_MTP_CKPT_DIR: FP8 -> BF16 -> NVFP4 at load); NVFP4 activations by
+// the same table (FLASHRT_QWEN36_FUSE_SILU_MUL_QUANT).
+//
+// Pass 1 (amax_partial_kernel): grid-stride max |x| with 16-byte loads, one partial
+// per CTA.  Pass 2 (quantize_kernel): every CTA folds the partials into the global
+// scale itself (no inter-CTA counter, nothing to reset), then one thread quantizes
+// one 16-element block: 64 (fp32) or 32 (bf16) contiguous bytes in, 8 packed bytes
+// and one scale byte out.  Both passes are HBM-bound.
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kThreads)
+amax_partial_kernel(const uint4* __restrict__ src, int64_t nvec, float* __restrict__ partials) {
+    float m = 0.0f;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < nvec;
+         i += (int64_t)gridDim.x * kThreads) {
+        const uint4 v = __ldcs(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (kBF16) {
+                m = fmaxf(m, fabsf(bf16_to_f32(w[j] & 0xFFFFu)));
+                m = fmaxf(m, fabsf(bf16_to_f32(w[j] >> 16)));
+            } else {
+                m = fmaxf(m, fabsf(__uint_as_float(w[j])));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float red[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float r = red[0];
+#pragma unroll
+        for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
+        partials[blockIdx.x] = r;
+    }
+}
+
+// Global scale seen by every CTA: *given_g, or amax / 2688 from the partials.
+__device__ __forceinline__ float cta_global_scale(const float* __restrict__ given_g,
+                                                  const float* __restrict__ partials,
+                                                  int npartials) {
+    __shared__ float g_sh;
+    if (given_g) {
+        if (threadIdx.x == 0) g_sh = *given_g;
+    } else {
+        float m = 0.0f;
+        for (int i = threadIdx.x; i < npartials; i += blockDim.x) m = fmaxf(m, partials[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        __shared__ float red[kThreads / 32];
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float r = red[0];
+            for (int i = 1; i < (int)(blockDim.x / 32); ++i) r = fmaxf(r, red[i]);
+            g_sh = global_scale_from_amax(r);
+        }
+    }
+    __syncthreads();
+    return g_sh;
+}
+
+template <bool kBF16, bool kSwizzled>
+__global__ void __launch_bounds__(kThreads)
+quantize_kernel(const void* __restrict__ src, int64_t rows, int64_t cols,
+                const float* __restrict__ partials, int npartials,
+                const float* __restrict__ given_g, uint8_t* __restrict__ packed,
+                uint8_t* __restrict__ scales, float* __restrict__ g_out,
+                uint16_t* __restrict__ deq_bf16) {
+    const float g = cta_global_scale(given_g, partials, npartials);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+
+    const int64_t cb_n = cols >> 4;
+    const int64_t cp4 = (cb_n + 3) >> 2;
+    // with swizzled scales the grid also covers the padding (rows to 128, blocks to 4)
+    const int64_t rows_iter = kSwizzled ? ((rows + 127) >> 7) << 7 : rows;
+    const int64_t cb_iter = kSwizzled ? cp4 << 2 : cb_n;
+    const int64_t nblk = rows_iter * cb_iter;
+    for (int64_t b = blockIdx.x * (int64_t)kThreads + threadIdx.x; b < nblk;
+         b += (int64_t)gridDim.x * kThreads) {
+        const int64_t r = b / cb_iter, cb = b - r * cb_iter;
+        if (kSwizzled && (r >= rows || cb >= cb_n)) {
+            scales[swizzle_offset(r, cb, cp4)] = 0;
+            continue;
+        }
+        const int64_t e0 = r * cols + (cb << 4);
+        float t[16];
+        if (kBF16) {
+            const uint4* p = reinterpret_cast<const uint4*>(
+                static_cast<const uint16_t*>(src) + e0);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint4 v = __ldcs(p + q);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    t[q * 8 + 2 * j] = bf16_to_f32(w[j] & 0xFFFFu);
+                    t[q * 8 + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
+                }
+            }
+        } else {
+            const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + e0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = __ldcs(p + q);
+                t[4 * q] = v.x;
+                t[4 * q + 1] = v.y;
+                t[4 * q + 2] = v.z;
+                t[4 * q + 3] = v.w;
+            }
+        }
+        uint32_t lo, hi;
+        const uint32_t s8 = quantize_block16(t, g, lo, hi);
+        *reinterpret_cast<uint2*>(packed + (e0 >> 1)) = make_uint2(lo, hi);
+        if (kSwizzled) scales[swizzle_offset(r, cb, cp4)] = (uint8_t)s8;
+        else scales[r * cb_n + cb] = (uint8_t)s8;
+        if (deq_bf16) {
+            // e2m1 * e4m3 has at most 5 significant bits and lies in [2^-10, 2688]:
+            // exact in bf16.
+            const float s = e4m3_to_f32(s8);
+            uint32_t out[8];
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const uint32_t c0 = ((i < 8 ? lo : hi) >> (4 * (i & 7))) & 15u;
+                const uint32_t c1 = ((i < 8 ? lo : hi) >> (4 * ((i + 1) & 7))) & 15u;
+                const float m0 = (float)(c0 & 7u), m1 = (float)(c1 & 7u);
+                // magnitude of code c: c < 4 ? c / 2 : (c == 4 ? 2 : c == 5 ? 3 : c == 6 ? 4 : 6)
+                const float v0 = (c0 & 7u) < 4u ? 0.5f * m0 : (m0 == 7.0f ? 6.0f : m0 - 2.0f);
+                const float v1 = (c1 & 7u) < 4u ? 0.5f * m1 : (m1 == 7.0f ? 6.0f : m1 - 2.0f);
+                const float d0 = (c0 & 8u) ? -v0 * s : v0 * s;
+                const float d1 = (c1 & 8u) ? -v1 * s : v1 * s;
+                out[i / 2] = (uint32_t)f32_to_bf16_rne(d0) | ((uint32_t)f32_to_bf16_rne(d1) << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(deq_bf16 + e0);
+            dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        }
+    }
+}
+
+// One thread per 16-byte line of the swizzled layout: line i of atom (rb, ka) holds
+// rows rb*128 + i + {0, 32, 64, 96}, scale columns ka*4 .. ka*4+3.
+__global__ void __launch_bounds__(kThreads)
+repack_kernel(const uint8_t* __restrict__ s, int64_t rows, int64_t cb_n, int64_t cp4,
+              uint4* __restrict__ out, int64_t nlines) {
+    for (int64_t l = blockIdx.x * (int64_t)kThreads + threadIdx.x; l < nlines;
+         l += (int64_t)gridDim.x * kThreads) {
+        const int64_t atom = l >> 5, i = l & 31;
+        const int64_t rb = atom / cp4, ka = atom - rb * cp4;
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t r = rb * 128 + j * 32 + i;
+            uint32_t v = 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int64_t cb = ka * 4 + c;
+                if (r < rows && cb < cb_n) v |= (uint32_t)s[r * cb_n + cb] << (8 * c);
+            }
+            w[j] = v;
+        }
+        out[l] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+encode_elements_kernel(const float* __restrict__ in, int64_t n, uint8_t* __restrict__ e2m1,
+                       uint8_t* __restrict__ e4m3) {
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * kThreads) {
+        const float v = in[i];
+        if (e2m1) e2m1[i] = (uint8_t)e2m1_encode(v);
+        if (e4m3) e4m3[i] = (uint8_t)e4m3_encode_nonneg(v > 0.0f ? v : 0.0f);
+    }
+}
+
+int grid_for(int64_t items, const DevInfo& dev, int ctas_per_sm) {
+    const int64_t need = (items + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)dev.sm_count * ctas_per_sm;
+    return (int)(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+}  // namespace
+
+int amax_partial_count(int64_t n_elems, int sm_count) {
+    // 16-byte vectors of the smaller dtype bound the useful CTA count
+    const int64_t nvec = (n_elems + 7) / 8;
+    const int64_t need = (nvec + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)sm_count * 8;
+    return (int)(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+cudaError_t launch_quantize(const void* src, bool src_bf16, int64_t rows, int64_t cols,
+                            uint8_t* packed, uint8_t* scales, bool swizzled_scales,
+                            float* g_out, const float* given_g, float* partials,
+                            int npartials, uint16_t* deq_bf16, cudaStream_t stream,
+                            const DevInfo& dev) {
+    const int64_t n = rows * cols;
+    if (!given_g) {
+        const int64_t nvec = n * (src_bf16 ? 2 : 4) / 16;
+        if (src_bf16)
+            amax_partial_kernel<true><<<npartials, kThreads, 0, stream>>>(
+                static_cast<const uint4*>(src), nvec, partials);
+        else
+            amax_partial_kernel<false><<<npartials, kThreads, 0, stream>>>(
+                static_cast<const uint4*>(src), nvec, partials);
+    }
+    const int64_t cb_n = cols / 16;
+    const int64_t nblk = swizzled_scales ? ((rows + 127) / 128 * 128) * ((cb_n + 3) / 4 * 4)
+                                         : rows * cb_n;
+    const int grid = grid_for(nblk, dev, 8);
+#define NVFP4_Q(B, S)                                                                   \
+    quantize_kernel<B, S><<<grid, kThreads, 0, stream>>>(src, rows, cols, partials,     \
+                                                         npartials, given_g, packed,    \
+                                                         scales, g_out, deq_bf16)
+    if (src_bf16) {
+        if (swizzled_scales) NVFP4_Q(true, true); else NVFP4_Q(true, false);
+    } else {
+        if (swizzled_scales) NVFP4_Q(false, true); else NVFP4_Q(false, false);
+    }
+#undef NVFP4_Q
+    return cudaGetLastError();
+}
+
+cudaError_t launch_repack(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out,
+                          cudaStream_t stream, const DevInfo& dev) {
+    const int64_t cb_n = cols / 16, cp4 = (cb_n + 3) / 4;
+    const int64_t nlines = ((rows + 127) / 128) * cp4 * 32;
+    repack_kernel<<<grid_for(nlines, dev, 8), kThreads, 0, stream>>>(
+        scales, rows, cb_n, cp4, reinterpret_cast<uint4*>(out), nlines);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out,
+                                   uint8_t* e4m3_out, cudaStream_t stream,
+                                   const DevInfo& dev) {
+    if (n == 0) return cudaSuccess;
+    encode_elements_kernel<<<grid_for(n, dev, 16), kThreads, 0, stream>>>(in, n, e2m1_out,
+                                                                          e4m3_out);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,46 @@
+"""Shared test helpers: moving oracle outputs to the device and the linear tolerance."""
+import numpy as np
+import torch
+
+import oracle
+
+# |y - y_ref| <= 1e-3 * sum_k |x_k w_k| + 2^-8 |y_ref|  (x_k, w_k the dequantized operands)
+TOL_ABS = 1e-3
+TOL_REL = 2.0 ** -8
+
+
+def to_dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def y_to_f64(y: torch.Tensor) -> np.ndarray:
+    if y.dtype == torch.bfloat16:
+        return y.float().cpu().numpy().astype(np.float64)
+    return y.cpu().numpy().astype(np.float64)
+
+
+def check_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, absdot: np.ndarray, what=""):
+    err = np.abs(y_gpu - y_ref)
+    bound = TOL_ABS * absdot + TOL_REL * np.abs(y_ref)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError("%s: %d outputs out of tolerance; worst at %s: gpu %r ref %r "
+                             "bound %r" % (what, int(bad.sum()), i, y_gpu[i], y_ref[i], bound[i]))
+    return float((err / np.maximum(absdot, 1e-300)).max())
+
+
+def oracle_weights(w_cpu: torch.Tensor):
+    """Oracle-quantized weights: (wq, ws_rowmajor, gw) as numpy."""
+    return oracle.quantize(w_cpu.numpy())
+
+
+def upload_weights(wq: np.ndarray, ws: np.ndarray, gw: float, K: int):
+    """Device copies of oracle-quantized weights, scales swizzled by the library."""
+    import nvfp4_weight_quantized_quantize_gb300 as nv
+    d_wq = to_dev(wq)
+    d_ws = to_dev(ws)
+    d_swz = torch.empty(nv.nvfp4_repack_bytes(wq.shape[0], K), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_repack(d_ws, K, d_swz)
+    d_g = torch.tensor([gw], dtype=torch.float32, device="cuda")
+    return d_wq, d_swz, d_g

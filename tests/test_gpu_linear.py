@@ -1,0 +1,126 @@
+"""GPU parity of nvfp4_linear against the oracle (through the C ABI).
+
+Weights are quantized by the oracle on the CPU and uploaded; the oracle computes the
+reference from the same bytes in fp64.  Each output must satisfy
+|y - y_ref| <= 1e-3 * sum_k |x_k w_k| + 2^-8 |y_ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_weight_quantized_quantize_gb300 as nv
+import oracle
+from helpers import check_tolerance, to_dev, upload_weights, y_to_f64
+from synth import WORKLOADS, make_inputs, random_x, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def run_linear(x, wq, ws, gw, K, y_dtype, mode="w4a16", gx=None):
+    M = x.shape[0]
+    N = wq.shape[0]
+    d_wq, d_swz, d_g = upload_weights(wq, ws, gw, K)
+    d_x = x.cuda()
+    y = torch.empty(M, N, dtype=y_dtype, device="cuda")
+    wsb = nv.nvfp4_workspace_bytes(1, M, K, N, nv.NVFP4_W4A4 if mode == "w4a4" else nv.NVFP4_W4A16)
+    ws_t = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda") if wsb else None
+    d_gx = None if gx is None else torch.tensor([gx], dtype=torch.float32, device="cuda")
+    nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, mode=mode, x_global_scale=d_gx, workspace=ws_t)
+    torch.cuda.synchronize()
+    return y, ws_t
+
+
+@pytest.mark.parametrize("M,K,N,ydt", [
+    (1, 32, 1, torch.float32), (1, 64, 3, torch.bfloat16), (1, 96, 257, torch.float32),
+    (2, 160, 100, torch.bfloat16), (3, 512, 1000, torch.float32), (7, 1056, 333, torch.bfloat16),
+    (8, 4096, 130, torch.float32), (11, 640, 77, torch.bfloat16), (16, 2048, 64, torch.float32),
+    (5, 32, 9, torch.bfloat16), (13, 96, 200, torch.float32),
+])
+def test_ragged_w4a16(M, K, N, ydt):
+    x, w = make_inputs(M, K, N, seed=100 + M + K + N, outliers=True)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, _ = run_linear(x, wq, ws, gw, K, ydt)
+    y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+    check_tolerance(y_to_f64(y), y_ref, ab, "M%d K%d N%d" % (M, K, N))
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_a", "decode_b"])
+def test_workload_full(name):
+    wl = WORKLOADS[name]
+    x, w = workload_inputs(name)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    ydt = torch.float32 if wl.y_dtype == "f32" else torch.bfloat16
+    y, _ = run_linear(x, wq, ws, gw, wl.K, ydt)
+    y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+    check_tolerance(y_to_f64(y), y_ref, ab, name)
+
+
+@pytest.mark.parametrize("name", ["verify_a", "verify_b"])
+def test_verify_sampled(name):
+    wl = WORKLOADS[name]
+    x, w = workload_inputs(name)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, _ = run_linear(x, wq, ws, gw, wl.K, torch.bfloat16)
+    rng = np.random.default_rng(0)
+    pm = rng.integers(0, wl.M, 4096)
+    pn = rng.integers(0, wl.N, 4096)
+    # plus two full output rows
+    pm = np.concatenate([pm, np.zeros(wl.N, np.int64), np.full(wl.N, wl.M - 1)])
+    pn = np.concatenate([pn, np.arange(wl.N), np.arange(wl.N)])
+    y_ref, ab = oracle.linear_w4a16_pairs(x, wq, ws, gw, pm, pn)
+    check_tolerance(y_to_f64(y)[pm, pn], y_ref, ab, name)
+
+
+def test_zero_weights_and_zero_x():
+    M, K, N = 3, 64, 40
+    x, _ = make_inputs(M, K, N, 7)
+    w = torch.zeros(N, K)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, _ = run_linear(x, wq, ws, gw, K, torch.float32)
+    assert not y.any()
+    x0 = torch.zeros(M, K, dtype=torch.bfloat16)
+    _, w = make_inputs(M, K, N, 8)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, _ = run_linear(x0, wq, ws, gw, K, torch.float32)
+    assert not y.any()
+
+
+@pytest.mark.parametrize("M,K,N,gx", [(1, 512, 256, None), (7, 1024, 300, None),
+                                      (4, 96, 50, 0.003), (16, 5120, 128, None)])
+def test_w4a4_small_m(M, K, N, gx):
+    x, w = make_inputs(M, K, N, seed=200 + M)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, ws_t = run_linear(x, wq, ws, gw, K, torch.bfloat16, mode="w4a4", gx=gx)
+    y_ref, ab, xq, xs, gxo = oracle.linear_w4a4(x, wq, ws, gw, gx)
+    # the in-call activation quantization is bit-exact: codes, swizzled scales, g_x
+    o_xq, o_xs, o_gx = nv.nvfp4_w4a4_workspace_layout(M, K)
+    wsh = ws_t.cpu().numpy()
+    np.testing.assert_array_equal(wsh[o_xq:o_xq + M * K // 2].reshape(M, K // 2), xq)
+    nb = nv.nvfp4_repack_bytes(M, K)
+    np.testing.assert_array_equal(wsh[o_xs:o_xs + nb], oracle.repack(xs, K))
+    assert wsh[o_gx:o_gx + 4].view(np.float32)[0] == np.float32(gxo)
+    check_tolerance(y_to_f64(y), y_ref, ab, "w4a4 M%d" % M)
+
+
+def test_repeated_calls_are_deterministic():
+    M, K, N = 7, 5120, 6144
+    x, w = make_inputs(M, K, N, 3)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y1, _ = run_linear(x, wq, ws, gw, K, torch.bfloat16)
+    y2, _ = run_linear(x, wq, ws, gw, K, torch.bfloat16)
+    assert torch.equal(y1, y2)
+
+
+def test_tiny_config_on_a_side_stream():
+    x, w = workload_inputs("tiny")
+    wq, ws, gw = oracle.quantize(w.numpy())
+    d_wq, d_swz, d_g = upload_weights(wq, ws, gw, 512)
+    s = torch.cuda.Stream()
+    y = torch.empty(1, 256, dtype=torch.float32, device="cuda")
+    d_x = x.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y)
+    s.synchronize()
+    y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+    check_tolerance(y_to_f64(y), y_ref, ab, "side stream")

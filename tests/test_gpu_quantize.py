@@ -1,0 +1,141 @@
+"""GPU parity of the quantizer, the repack and the element rounding, against the
+oracle, bit for bit (all calls go through the C ABI)."""
+import json
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_weight_quantized_quantize_gb300 as nv
+import oracle
+from conftest import GOLDEN
+from helpers import to_dev
+from synth import make_inputs, random_w, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_quantize(src: torch.Tensor):
+    rows, cols = src.shape
+    d = src.cuda()
+    packed = torch.empty(rows, cols // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows, cols // 16, dtype=torch.uint8, device="cuda")
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(nv.nvfp4_workspace_bytes(0, rows, cols), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_quantize(d, packed, scales, g, ws)
+    torch.cuda.synchronize()
+    return packed.cpu().numpy(), scales.cpu().numpy(), float(g.item())
+
+
+def assert_same_quantization(src: torch.Tensor):
+    p, s, g = gpu_quantize(src)
+    src_o = src if src.dtype == torch.bfloat16 else src.numpy()
+    po, so, go = oracle.quantize(src_o)
+    assert g == go
+    np.testing.assert_array_equal(s, so)
+    np.testing.assert_array_equal(p, po)
+
+
+def test_hand_worked_tensor():
+    h = json.load(open(os.path.join(GOLDEN, "hand_quantize.json")))
+    t = torch.tensor([[float(v) for v in r] for r in h["input"]], dtype=torch.float32)
+    p, s, g = gpu_quantize(t)
+    assert g == float(h["expected_global_scale"])
+    np.testing.assert_array_equal(s, [[int(v, 16) for v in r] for r in h["expected_scales_hex"]])
+    np.testing.assert_array_equal(p, [[int(v, 16) for v in r] for r in h["expected_packed_hex"]])
+
+
+@pytest.mark.parametrize("rows,cols,seed", [(1, 16, 0), (3, 48, 1), (129, 80, 2),
+                                            (256, 512, 3), (1000, 1040, 4)])
+def test_ragged_shapes_fp32(rows, cols, seed):
+    assert_same_quantization(random_w(rows, cols, seed, std=0.5))
+
+
+@pytest.mark.parametrize("rows,cols,seed", [(1, 16, 5), (7, 5120, 6), (300, 96, 7)])
+def test_bf16_input(rows, cols, seed):
+    assert_same_quantization(random_w(rows, cols, seed).to(torch.bfloat16))
+
+
+def test_round_trip_tensor_every_code_every_scale():
+    rng = np.random.default_rng(11)
+    g = 2.0 ** -8
+    rows = []
+    for s in [126] + list(range(1, 126)):
+        codes = rng.permutation(16)
+        rows.append([oracle.e2m1_value(c) * oracle.e4m3_value(s) * g for c in codes])
+    assert_same_quantization(torch.tensor(np.array(rows), dtype=torch.float32))
+
+
+def test_zero_and_tiny_blocks():
+    t = torch.zeros(5, 64)
+    t[1, 5] = -0.0
+    assert_same_quantization(t)  # all-zero tensor: g = 1, signed zero codes
+    t[2, :16] = torch.linspace(-3, 3, 16)
+    t[3, 16:32] = 1e-8
+    t[4, 48:] = -1e-30
+    assert_same_quantization(t)
+
+
+def test_outliers_and_extreme_ranges():
+    for scale in (1e-30, 1e-3, 1.0, 1e30):
+        assert_same_quantization(random_w(64, 256, 12, std=scale))
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_a", "decode_b", "verify_b"])
+def test_workload_weights(name):
+    _, w = workload_inputs(name, M=1)
+    assert_same_quantization(w)
+
+
+@pytest.mark.parametrize("rows,cols,seed", [(1, 16, 0), (128, 64, 1), (130, 80, 2),
+                                            (17408, 5120, 3)])
+def test_repack_matches_oracle(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    s = rng.integers(0, 127, size=(rows, cols // 16), dtype=np.uint8)
+    out = torch.full((nv.nvfp4_repack_bytes(rows, cols),), 0xAB, dtype=torch.uint8,
+                     device="cuda")
+    nv.nvfp4_repack(to_dev(s), cols, out)
+    np.testing.assert_array_equal(out.cpu().numpy(), oracle.repack(s, cols))
+
+
+def _oracle_encode_chunked(fn, x: np.ndarray, workers: int = 16) -> np.ndarray:
+    parts = np.array_split(x, workers)
+    with ThreadPoolExecutor(workers) as ex:
+        return np.concatenate(list(ex.map(fn, parts)))
+
+
+def test_e2m1_rounding_every_fp32_pattern():
+    chunk = 1 << 27
+    for start in range(0, 1 << 32, chunk):
+        bits = torch.arange(start, start + chunk, dtype=torch.int64, device="cuda")
+        f = bits.to(torch.int32).view(torch.float32)
+        out = torch.empty(chunk, dtype=torch.uint8, device="cuda")
+        nv.nvfp4_encode_elements(f, out, None)
+        host = np.arange(start, start + chunk, dtype=np.uint64).astype(np.uint32)
+        finite = ((host >> 23) & 0xFF) != 0xFF
+        want = _oracle_encode_chunked(oracle.e2m1_encode, host.view(np.float32))
+        got = out.cpu().numpy()
+        bad = np.nonzero((got != want) & finite)[0]
+        assert bad.size == 0, "pattern 0x%08x: gpu %d oracle %d" % (
+            host[bad[0]], got[bad[0]], want[bad[0]])
+
+
+def test_e4m3_rounding_window_and_strided():
+    lo, hi = (127 - 12) << 23, (127 + 10) << 23
+    for start in range(lo, hi, 1 << 26):
+        n = min(1 << 26, hi - start)
+        host = np.arange(start, start + n, dtype=np.uint32)
+        d = torch.from_numpy(host.view(np.int32)).cuda().view(torch.float32)
+        out = torch.empty(n, dtype=torch.uint8, device="cuda")
+        nv.nvfp4_encode_elements(d, None, out)
+        want = _oracle_encode_chunked(oracle.e4m3_encode, host.view(np.float32))
+        np.testing.assert_array_equal(out.cpu().numpy(), want)
+    host = (np.arange(0, 1 << 32, 251, dtype=np.uint64)).astype(np.uint32)
+    host = host[((host >> 23) & 0xFF) != 0xFF]
+    d = torch.from_numpy(host.view(np.int32)).cuda().view(torch.float32)
+    out = torch.empty(host.size, dtype=torch.uint8, device="cuda")
+    nv.nvfp4_encode_elements(d, None, out)
+    want = _oracle_encode_chunked(oracle.e4m3_encode, host.view(np.float32))
+    np.testing.assert_array_equal(out.cpu().numpy(), want)
