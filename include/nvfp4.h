@@ -95,6 +95,32 @@ nvfp4_status nvfp4_quantize(const void* src, nvfp4_dtype src_dtype, int64_t rows
                             nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_noalloc -- nvfp4_quantize for callers that cannot allocate.
+ *
+ * No counterpart on the pages: it exists for callers that may not allocate device
+ * memory once they are running -- serving runtimes that plan every allocation at
+ * start-up, code under a fixed memory budget with no scratch pool to lend, and
+ * latency-critical paths where cudaMalloc/cudaFree would wait on the device.  It
+ * computes exactly what nvfp4_quantize computes (same kernels, same results) but takes
+ * no workspace: its scratch (one float per first-pass CTA, at most 2048 floats = 8 KiB)
+ * is a fixed array in device memory owned by the library, which every GPU that loads
+ * the library keeps until the process exits.  Arguments are those of nvfp4_quantize
+ * without the workspace.
+ *   - The first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress with that device current) and caches it; make that first
+ *     call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents behind;
+ *     nothing in it has to start at zero.  Calls whose kernels overlap on the GPU
+ *     (on different streams, or from different threads) race on it: order them.
+ *   - A call that would need more than 2048 first-pass partials returns
+ *     NVFP4_ERR_WORKSPACE (not reachable on GPUs with fewer than 256 SMs).
+ *   - It calls no allocating function (no cudaMalloc, no cudaFree).
+ */
+nvfp4_status nvfp4_quantize_noalloc(const void* src, nvfp4_dtype src_dtype, int64_t rows,
+                                    int64_t cols, uint8_t* packed, uint8_t* scales,
+                                    float* global_scale, nvfp4_stream_t stream);
+
+/*
  * nvfp4_repack -- row-major E4M3 scales to the kernels' swizzled layout.
  *
  * Defines: the load-time "NVFP4 swizzle" (FlashRT docs/qwen36_usage.md, constructor

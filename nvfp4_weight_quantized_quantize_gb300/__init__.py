@@ -27,7 +27,7 @@ STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ER
           7: "NVFP4_ERR_CUDA", 8: "NVFP4_ERR_TIMEOUT", 9: "NVFP4_ERR_UNSUPPORTED"}
 EXPORTS = ("nvfp4_quantize", "nvfp4_repack", "nvfp4_linear", "nvfp4_repack_bytes",
            "nvfp4_workspace_bytes", "nvfp4_w4a4_workspace_layout", "nvfp4_workspace_error",
-           "nvfp4_status_str", "nvfp4_encode_elements")
+           "nvfp4_status_str", "nvfp4_encode_elements", "nvfp4_quantize_noalloc")
 
 
 class Nvfp4Error(RuntimeError):
@@ -60,6 +60,7 @@ def load(path: str = LIB_PATH):
         "nvfp4_workspace_error": (I, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
         "nvfp4_status_str": (ctypes.c_char_p, [I]),
         "nvfp4_encode_elements": (I, [P, I64, P, P, P]),
+        "nvfp4_quantize_noalloc": (I, [P, I, I64, I64, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -132,6 +133,17 @@ def nvfp4_quantize(src: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor
                                _p(scales), _p(global_scale), _p(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nvfp4_quantize")
+
+
+def nvfp4_quantize_noalloc(src: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                           global_scale: torch.Tensor, stream=None) -> None:
+    """nvfp4_quantize without a workspace, for callers that cannot allocate: its scratch
+    is a fixed array inside the library, shared by every call on the device (order
+    calls that could overlap on the GPU)."""
+    rows, cols = src.shape
+    st = load().nvfp4_quantize_noalloc(_p(src), _dtype_code(src.dtype), rows, cols, _p(packed),
+                                       _p(scales), _p(global_scale), _stream(stream))
+    _check(st, "nvfp4_quantize_noalloc")
 
 
 def nvfp4_repack(scales: torch.Tensor, cols: int, out: torch.Tensor, stream=None) -> None:

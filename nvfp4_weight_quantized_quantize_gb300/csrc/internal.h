@@ -42,4 +42,8 @@ cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
 
 constexpr int kGemvMaxM = 16;
 
+// The current device's cached properties; NVFP4_ERR_DEVICE unless it is sm_103
+// (the status is returned as an int holding an nvfp4_status).
+int query_device(DevInfo* out);
+
 }  // namespace nvfp4

@@ -94,6 +94,10 @@ constexpr int64_t kMaxDim = (int64_t)1 << 30;
 }  // namespace
 }  // namespace nvfp4
 
+namespace nvfp4 {
+int query_device(DevInfo* out) { return (int)current_device(out); }
+}  // namespace nvfp4
+
 using namespace nvfp4;
 
 NVFP4_API const char* nvfp4_status_str(nvfp4_status s) {

@@ -11,6 +11,9 @@
 // scale itself (no inter-CTA counter, nothing to reset), then one thread quantizes
 // one 16-element block: 64 (fp32) or 32 (bf16) contiguous bytes in, 8 packed bytes
 // and one scale byte out.  Both passes are HBM-bound.
+#include <mutex>
+
+#include "../../include/nvfp4.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -256,3 +259,73 @@ cudaError_t launch_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out
 }
 
 }  // namespace nvfp4
+
+// ---- allocation-free quantizer -----------------------------------------------------------
+// Some callers cannot hand the quantizer a workspace: runtimes that plan every device
+// allocation at start-up and forbid later ones, code that runs under a fixed memory
+// budget with no scratch pool to lend, and latency-critical paths where cudaMalloc /
+// cudaFree would stall on a device synchronization.  nvfp4_quantize_noalloc serves them
+// with the same two kernels, taking the amax partials from a fixed array in device
+// memory that this library owns.
+
+namespace nvfp4 {
+namespace {
+
+// Scratch of the allocation-free quantizer: one float per pass-1 CTA.  Every GPU that
+// loads the library holds these 8 KiB until the process exits.  Pass 1 writes every
+// slot that pass 2 then reads, so nothing has to start at zero; calls share the array
+// and keep the last call's contents.
+constexpr int kNoAllocPartials = 2048;
+static __device__ __align__(256) float g_noalloc_partials[kNoAllocPartials];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[64] = {};
+
+// Device address of g_noalloc_partials on `device` (the current device).  In host code
+// the array's name only stands in for the symbol; the address a kernel can use comes
+// from cudaGetSymbolAddress, looked up once per device and cached.
+cudaError_t noalloc_scratch(int device, float** out) {
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[device]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_partials);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[device] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[device];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" __attribute__((visibility("default"))) nvfp4_status nvfp4_quantize_noalloc(
+    const void* src, nvfp4_dtype src_dtype, int64_t rows, int64_t cols, uint8_t* packed,
+    uint8_t* scales, float* global_scale, nvfp4_stream_t stream) {
+    using namespace nvfp4;
+    if (!src || !packed || !scales || !global_scale) return NVFP4_ERR_NULL;
+    if (src_dtype != NVFP4_F32 && src_dtype != NVFP4_BF16) return NVFP4_ERR_DTYPE;
+    if (rows < 1 || cols < 16 || cols % 16 != 0 || rows > ((int64_t)1 << 30) ||
+        cols > ((int64_t)1 << 30))
+        return NVFP4_ERR_SHAPE;
+    if (((uintptr_t)src | (uintptr_t)packed | (uintptr_t)scales) % 16 != 0 ||
+        (uintptr_t)global_scale % 4 != 0)
+        return NVFP4_ERR_ALIGN;
+    DevInfo d;
+    const nvfp4_status st = (nvfp4_status)query_device(&d);
+    if (st != NVFP4_OK) return st;
+    // pass 1 runs one CTA per partial; a call that would need more partials than the
+    // array holds is refused (it cannot happen below 256 SMs)
+    const int np = amax_partial_count(rows * cols, d.sm_count);
+    if (np > kNoAllocPartials) return NVFP4_ERR_WORKSPACE;
+    float* partials = nullptr;
+    if (noalloc_scratch(d.device, &partials) != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    const cudaError_t e = launch_quantize(src, src_dtype == NVFP4_BF16, rows, cols, packed,
+                                          scales, false, global_scale, nullptr, partials, np,
+                                          nullptr, stream, d);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
