@@ -129,8 +129,10 @@ class DecodeSetup:
             del w
             cps = [(packed, swz)] + [(packed.clone(), swz.clone()) for _ in range(copies - 1)]
             ys = [torch.empty(1, wl.N, dtype=torch.bfloat16, device="cuda") for _ in range(copies)]
+            ws = torch.zeros(nv.nvfp4_workspace_bytes(1, 1, wl.K, wl.N), dtype=torch.uint8,
+                             device="cuda")
             self.shapes.append(dict(name=name, M=1, K=wl.K, N=wl.N, x=x.cuda(), x_host=x,
-                                    g=g, copies=cps, ys=ys))
+                                    g=g, copies=cps, ys=ys, ws=ws))
         torch.cuda.synchronize()
         self.copies = copies
         self.bytes_per_step = sum(algo_bytes(s["M"], s["K"], s["N"]) for s in self.shapes)
@@ -172,7 +174,8 @@ def run_ours(args, rank, world, dist):
         for j, s in enumerate(S):
             if events is not None:
                 events[2 * j].record()
-            nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c])
+            nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c],
+                            workspace=s["ws"])
             if events is not None:
                 events[2 * j + 1].record()
 
@@ -250,7 +253,7 @@ def run_ours(args, rank, world, dist):
                          "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / pk["hbm_gbs"], 4),
                          "traffic": traffic, "peak_source": pk_src,
-                         "kernel": "gemv_w4a16_kernel<1>",
+                         "kernel": "gemv_m1_pipe_kernel",
                          "launch_us": round(avg_launch_s * 1e6, 2)},
             "e2e": e2e,
             "gpu_launches": len(S) * args.steps,
@@ -272,7 +275,8 @@ def run_e2e(torch, nv, setup, args):
         c = i % setup.copies
         for j, s in enumerate(S):
             s["x"].copy_(xh[j], non_blocking=True)
-            nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c])
+            nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c],
+                            workspace=s["ws"])
             yh[j].copy_(s["ys"][c], non_blocking=True)
 
     n = min(args.steps, 2048)
@@ -336,7 +340,7 @@ def measure_rows(torch, nv, setup):
     for sh in setup.shapes:
         ms = time_graph(torch, lambda i, sh=sh: nv.nvfp4_linear(
             sh["x"], sh["copies"][i % setup.copies][0], sh["copies"][i % setup.copies][1],
-            sh["g"], sh["ys"][i % setup.copies]), 4 * setup.copies, 50)
+            sh["g"], sh["ys"][i % setup.copies], workspace=sh["ws"]), 4 * setup.copies, 50)
         b = algo_bytes(1, sh["K"], sh["N"])
         rows["a3_decode_%s_K%d_N%d" % (sh["name"], sh["K"], sh["N"])] = {
             "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
@@ -350,8 +354,10 @@ def measure_rows(torch, nv, setup):
         cps = [(p, z)] + [(p.clone(), z.clone()) for _ in range(ncp - 1)]
         xd = x.cuda()
         y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+        wsv = torch.zeros(nv.nvfp4_workspace_bytes(1, wl.M, wl.K, wl.N), dtype=torch.uint8,
+                          device="cuda")
         ms = time_graph(torch, lambda i: nv.nvfp4_linear(xd, cps[i % ncp][0], cps[i % ncp][1],
-                                                         gg, y), 2 * ncp, 20)
+                                                         gg, y, workspace=wsv), 2 * ncp, 20)
         b = algo_bytes(wl.M, wl.K, wl.N)
         rows["a4_verify_%s_M7_K%d_N%d" % (name, wl.K, wl.N)] = {
             "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}

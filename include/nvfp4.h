@@ -124,10 +124,14 @@ nvfp4_status nvfp4_quantize_noalloc(const void* src, nvfp4_dtype src_dtype, int6
  * nvfp4_repack -- row-major E4M3 scales to the kernels' swizzled layout.
  *
  * Defines: the load-time "NVFP4 swizzle" (FlashRT docs/qwen36_usage.md, constructor
- * paragraph).  The target is the tensor-core block-scale layout for 16-element
- * blocks: rows padded to Rp = 128*ceil(rows/128) and blocks to Cp = 4*ceil(Cb/4)
- * (Cb = cols/16) with zero bytes; element (r, cb) goes to byte
- *   ((r/128)*(Cp/4) + cb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + cb%4.
+ * paragraph).  The buffer holds two copies of the scales:
+ *   1. at byte 0, the tensor-core block-scale layout for 16-element blocks, read by the
+ *      tensor-core kernels: rows padded to Rp = 128*ceil(rows/128) and blocks to
+ *      Cp = 4*ceil(Cb/4) (Cb = cols/16) with zero bytes; element (r, cb) goes to byte
+ *        ((r/128)*(Cp/4) + cb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + cb%4;
+ *   2. at byte A = Rp*Cp, the row-major scales [rows, Cb] unchanged, read by the
+ *      small-M kernels (which stream a row's scales next to its codes), then zero
+ *      bytes up to a multiple of 16 and 16 more.
  * Arguments:
  *   scales_rowmajor  [rows, cols/16] bytes.  rows >= 1, cols >= 16, cols % 16 == 0.
  *   scales_swizzled  out, exactly swizzled_bytes == nvfp4_repack_bytes(rows, cols).
@@ -160,9 +164,9 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *   mode               NVFP4_W4A16 or NVFP4_W4A4.
  *   x_global_scale     W4A4 only: NULL = dynamic (amax of x), else one float
  *                      (device, finite, > 0).  Must be NULL for W4A16.
- *   workspace          >= nvfp4_workspace_bytes(1, M, K, N, mode) bytes, zero-filled
- *                      once at allocation (sticky error word); may be NULL when that
- *                      size is 0.  Calls that share a workspace must be ordered (one
+ *   workspace          >= nvfp4_workspace_bytes(1, M, K, N, mode) bytes (at least the
+ *                      256-byte header holding the sticky error word), zero-filled once
+ *                      at allocation.  Calls that share a workspace must be ordered (one
  *                      stream), since W4A4 keeps the quantized x there.
  */
 nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K, const uint8_t* w_packed,
@@ -181,9 +185,9 @@ size_t nvfp4_repack_bytes(int64_t rows, int64_t cols);
 size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N, nvfp4_mode mode);
 
 /* Where nvfp4_linear in W4A4 mode leaves the quantized activations inside its
- * workspace: packed codes [M, K/2] at *xq_offset, swizzled scales
- * (nvfp4_repack_bytes(M, K) bytes) at *xs_offset and g_x (one float) at
- * *gx_offset.  They are valid once the call has completed.  Returns NVFP4_OK or
+ * workspace: packed codes [M, K/2] at *xq_offset, the scales in the tensor-core
+ * layout (part 1 of nvfp4_repack's layout, Rp*Cp bytes) at *xs_offset and g_x (one
+ * float) at *gx_offset.  They are valid once the call has completed.  Returns NVFP4_OK or
  * NVFP4_ERR_SHAPE. */
 nvfp4_status nvfp4_w4a4_workspace_layout(int64_t M, int64_t K, size_t* xq_offset,
                                          size_t* xs_offset, size_t* gx_offset);
@@ -197,6 +201,10 @@ nvfp4_status nvfp4_workspace_error(void* workspace, nvfp4_stream_t stream, uint3
 const char* nvfp4_status_str(nvfp4_status status);
 
 /* ---- diagnostics -------------------------------------------------------------- */
+
+/* The CUDA error behind the last NVFP4_ERR_CUDA this thread got from the library
+ * (cudaGetErrorString text; "no error" if there was none).  Host-only. */
+const char* nvfp4_last_cuda_error(void);
 
 /*
  * nvfp4_encode_elements -- the device's element rounding on its own: for each of n

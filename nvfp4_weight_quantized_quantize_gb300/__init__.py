@@ -27,7 +27,8 @@ STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ER
           7: "NVFP4_ERR_CUDA", 8: "NVFP4_ERR_TIMEOUT", 9: "NVFP4_ERR_UNSUPPORTED"}
 EXPORTS = ("nvfp4_quantize", "nvfp4_repack", "nvfp4_linear", "nvfp4_repack_bytes",
            "nvfp4_workspace_bytes", "nvfp4_w4a4_workspace_layout", "nvfp4_workspace_error",
-           "nvfp4_status_str", "nvfp4_encode_elements", "nvfp4_quantize_noalloc")
+           "nvfp4_status_str", "nvfp4_encode_elements", "nvfp4_quantize_noalloc",
+           "nvfp4_last_cuda_error")
 
 
 class Nvfp4Error(RuntimeError):
@@ -61,6 +62,7 @@ def load(path: str = LIB_PATH):
         "nvfp4_status_str": (ctypes.c_char_p, [I]),
         "nvfp4_encode_elements": (I, [P, I64, P, P, P]),
         "nvfp4_quantize_noalloc": (I, [P, I, I64, I64, P, P, P, P]),
+        "nvfp4_last_cuda_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -84,6 +86,8 @@ def _p(t):
 
 def _check(st: int, where: str):
     if st != 0:
+        if st == 7:
+            where = "%s (%s)" % (where, load().nvfp4_last_cuda_error().decode())
         raise Nvfp4Error(st, where)
 
 

@@ -36,9 +36,11 @@ cudaError_t launch_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out
                                    const DevInfo& dev);
 
 // Small-M (M <= 16) W4A16 GEMV / skinny GEMM.  y = (gx ? *gx : 1) * *gw * x . W^T.
+// err: the workspace's sticky error word (bounded waits OR bits into it).
 cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz, const float* gw, const float* gx, int N,
-                              void* y, bool y_bf16, cudaStream_t stream, const DevInfo& dev);
+                              void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
+                              const DevInfo& dev);
 
 constexpr int kGemvMaxM = 16;
 

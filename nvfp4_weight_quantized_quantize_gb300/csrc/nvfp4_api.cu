@@ -55,17 +55,25 @@ nvfp4_status current_device(DevInfo* out) {
 
 inline bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 inline nvfp4_status from_cuda(cudaError_t e) {
     if (e == cudaSuccess) return NVFP4_OK;
+    t_last_cuda_error = e;
     return NVFP4_ERR_CUDA;
 }
 
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-size_t repack_bytes(int64_t rows, int64_t cols) {
+// the tensor-core atom part, then a row-major copy (padded to 16 bytes, plus 16 bytes)
+size_t repack_atom_bytes(int64_t rows, int64_t cols) {
     const int64_t rp = (rows + 127) / 128 * 128;
     const int64_t cp = (cols / 16 + 3) / 4 * 4;
     return (size_t)(rp * cp);
+}
+
+size_t repack_bytes(int64_t rows, int64_t cols) {
+    return repack_atom_bytes(rows, cols) + (size_t)((rows * (cols / 16) + 15) / 16 * 16) + 16;
 }
 
 int partial_count(int64_t n, const DevInfo& d) {
@@ -82,7 +90,7 @@ W4A4Layout w4a4_layout(int64_t M, int64_t K) {
     W4A4Layout L;
     L.xq = kHeaderBytes;
     L.xs = round_up(L.xq + (size_t)(M * K / 2), 256);
-    L.gx = round_up(L.xs + repack_bytes(M, K), 256);
+    L.gx = round_up(L.xs + repack_atom_bytes(M, K), 256);
     L.partials = L.gx + 256;
     L.deq = round_up(L.partials + (size_t)kMaxPartials * 4, 256);
     L.total = L.deq + (M <= kGemvMaxM ? (size_t)(M * K * 2) : 0);
@@ -128,7 +136,7 @@ NVFP4_API size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
         return kHeaderBytes + (size_t)kMaxPartials * 4;
     }
     if (op != 1 || M < 1 || K < 32 || K % 32 != 0 || N < 1) return (size_t)-1;
-    if (mode == NVFP4_W4A16) return M <= kGemvMaxM ? 0 : kHeaderBytes;
+    if (mode == NVFP4_W4A16) return kHeaderBytes;
     if (mode == NVFP4_W4A4) return w4a4_layout(M, K).total;
     return (size_t)-1;
 }
@@ -221,8 +229,8 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
     if (mode == NVFP4_W4A16) {
         if (M <= kGemvMaxM)
             return from_cuda(launch_gemv_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
-                                               w_global_scale, nullptr, (int)N, y, ybf, stream,
-                                               d));
+                                               w_global_scale, nullptr, (int)N, y, ybf,
+                                               static_cast<uint32_t*>(workspace), stream, d));
         return NVFP4_ERR_UNSUPPORTED;
     }
     // W4A4: quantize x into the workspace (bit-exact with nvfp4_quantize + nvfp4_repack)
@@ -233,10 +241,11 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
     cudaError_t e = launch_quantize(x, true, M, K, ws + L.xq, ws + L.xs, true, gx,
                                     x_global_scale, reinterpret_cast<float*>(ws + L.partials),
                                     partial_count(M * K, d), deq, stream, d);
-    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (e != cudaSuccess) return from_cuda(e);
     if (M <= kGemvMaxM)
         return from_cuda(launch_gemv_w4a16(deq, (int)M, (int)K, w_packed, w_scales_swizzled,
-                                           w_global_scale, gx, (int)N, y, ybf, stream, d));
+                                           w_global_scale, gx, (int)N, y, ybf,
+                                           reinterpret_cast<uint32_t*>(ws), stream, d));
     return NVFP4_ERR_UNSUPPORTED;
 }
 
@@ -249,4 +258,8 @@ NVFP4_API nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t
     nvfp4_status st = current_device(&d);
     if (st != NVFP4_OK) return st;
     return from_cuda(launch_encode_elements(in, n, e2m1_out, e4m3_out, stream, d));
+}
+
+NVFP4_API const char* nvfp4_last_cuda_error(void) {
+    return cudaGetErrorString(t_last_cuda_error);
 }

@@ -240,12 +240,37 @@ cudaError_t launch_quantize(const void* src, bool src_bf16, int64_t rows, int64_
     return cudaGetLastError();
 }
 
+// The row-major copy that follows the atom part: `n` scale bytes, then zero padding up to
+// `padded` bytes (a multiple of 16).  Source reads stay inside the n source bytes.
+__global__ void __launch_bounds__(kThreads)
+rowmajor_copy_kernel(const uint8_t* __restrict__ s, int64_t n, uint4* __restrict__ out,
+                     int64_t nvec) {
+    for (int64_t v = blockIdx.x * (int64_t)kThreads + threadIdx.x; v < nvec;
+         v += (int64_t)gridDim.x * kThreads) {
+        const int64_t b = v * 16;
+        uint4 r = make_uint4(0u, 0u, 0u, 0u);
+        if (b + 16 <= n) {
+            r = *reinterpret_cast<const uint4*>(s + b);
+        } else if (b < n) {
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            for (int64_t i = b; i < n; ++i) w[(i - b) >> 2] |= (uint32_t)s[i] << (8 * ((i - b) & 3));
+            r = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        out[v] = r;
+    }
+}
+
 cudaError_t launch_repack(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out,
                           cudaStream_t stream, const DevInfo& dev) {
     const int64_t cb_n = cols / 16, cp4 = (cb_n + 3) / 4;
     const int64_t nlines = ((rows + 127) / 128) * cp4 * 32;
     repack_kernel<<<grid_for(nlines, dev, 8), kThreads, 0, stream>>>(
         scales, rows, cb_n, cp4, reinterpret_cast<uint4*>(out), nlines);
+    const int64_t atom_bytes = nlines * 16;
+    const int64_t n = rows * cb_n;
+    const int64_t nvec = (n + 15) / 16 + 1;  // the copy, padded to 16 bytes, plus 16 bytes
+    rowmajor_copy_kernel<<<grid_for(nvec, dev, 8), kThreads, 0, stream>>>(
+        scales, n, reinterpret_cast<uint4*>(out + atom_bytes), nvec);
     return cudaGetLastError();
 }
 

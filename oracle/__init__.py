@@ -81,6 +81,7 @@ def _load():
             "orc_round_bf16_array": (None, [P, I64, P]),
             "orc_quantize": (ctypes.c_int, [P, ctypes.c_int, I64, I64, P, P, P, P]),
             "orc_repack_bytes": (I64, [I64, I64]),
+            "orc_repack_atom_bytes": (I64, [I64, I64]),
             "orc_swizzle_offset": (I64, [I64, I64, I64]),
             "orc_repack": (ctypes.c_int, [P, I64, I64, P, I64]),
             "orc_dequantize": (None, [P, P, F, I64, I64, P]),
@@ -187,6 +188,10 @@ def quantize(src, global_scale: float | None = None):
 
 def repack_bytes(rows: int, cols: int) -> int:
     return int(_load().orc_repack_bytes(rows, cols))
+
+
+def repack_atom_bytes(rows: int, cols: int) -> int:
+    return int(_load().orc_repack_atom_bytes(rows, cols))
 
 
 def swizzle_offset(r: int, cb: int, cols: int) -> int:

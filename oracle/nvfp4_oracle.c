@@ -38,10 +38,13 @@
  *       448 (0x7E).  Scales are never negative.
  *   R6  packing: byte j of a row holds element 2j in its low nibble and element
  *       2j+1 in its high nibble.
- *   R7  swizzled scale layout: the 128-row x 4-block atoms of the tensor-core block
- *       scale layout, element (r, cb) at byte
+ *   R7  swizzled scale layout ("NVFP4 swizzle" at load): first the 128-row x 4-block
+ *       atoms of the tensor-core block scale layout, element (r, cb) at byte
  *          ((r/128)*(Cp/4) + cb/4)*512 + (r%32)*16 + ((r%128)/32)*4 + cb%4,
- *       rows padded to a multiple of 128 and blocks to a multiple of 4 with zero.
+ *       rows padded to a multiple of 128 and blocks to a multiple of 4 with zero
+ *       (A = Rp*Cp bytes); then, at byte A, the row-major scales [R, C/16] once more
+ *       (for the GEMV, which streams a row's scales next to its codes), zero-padded to
+ *       a multiple of 16 bytes plus 16 bytes.
  *   R8  linear: y[m,n] = sum_k x[m,k] * e2m1(q[n,k]) * e4m3(s[n,k/16]) * g_w summed
  *       in fp64; for activations quantized to NVFP4 (W4A4), x is replaced by its
  *       dequantized value.
@@ -242,11 +245,16 @@ ORC_EXPORT int orc_quantize(const void* src, int src_is_bf16, int64_t rows, int6
 /* Swizzled scale layout (R7)                                                */
 /* ------------------------------------------------------------------------- */
 
-ORC_EXPORT int64_t orc_repack_bytes(int64_t rows, int64_t cols) {
+/* bytes of the atom part of the swizzled layout */
+ORC_EXPORT int64_t orc_repack_atom_bytes(int64_t rows, int64_t cols) {
     int64_t rp = (rows + 127) / 128 * 128;
     int64_t cb = cols / 16;
     int64_t cp = (cb + 3) / 4 * 4;
     return rp * cp;
+}
+
+ORC_EXPORT int64_t orc_repack_bytes(int64_t rows, int64_t cols) {
+    return orc_repack_atom_bytes(rows, cols) + (rows * (cols / 16) + 15) / 16 * 16 + 16;
 }
 
 ORC_EXPORT int64_t orc_swizzle_offset(int64_t r, int64_t cb, int64_t cols) {
@@ -256,7 +264,7 @@ ORC_EXPORT int64_t orc_swizzle_offset(int64_t r, int64_t cb, int64_t cols) {
 }
 
 /* scales [rows, cols/16] row-major -> swizzled bytes (out_bytes must equal
- * orc_repack_bytes); padding bytes are zero. */
+ * orc_repack_bytes): the atom part, then the row-major copy; padding bytes are zero. */
 ORC_EXPORT int orc_repack(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out,
                           int64_t out_bytes) {
     if (cols % 16 != 0 || out_bytes != orc_repack_bytes(rows, cols)) return -1;
@@ -264,6 +272,7 @@ ORC_EXPORT int orc_repack(const uint8_t* scales, int64_t rows, int64_t cols, uin
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t cb = 0; cb < cols / 16; ++cb)
             out[orc_swizzle_offset(r, cb, cols)] = scales[r * (cols / 16) + cb];
+    memcpy(out + orc_repack_atom_bytes(rows, cols), scales, (size_t)(rows * (cols / 16)));
     return 0;
 }
 

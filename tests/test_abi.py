@@ -50,16 +50,16 @@ def test_status_strings(lib):
 
 
 def test_size_helpers(lib):
-    assert nv.nvfp4_repack_bytes(17408, 5120) == 17408 * 320
-    assert nv.nvfp4_repack_bytes(1, 16) == 512
-    assert nv.nvfp4_repack_bytes(129, 80) == 256 * 8
+    assert nv.nvfp4_repack_bytes(17408, 5120) == 2 * 17408 * 320 + 16
+    assert nv.nvfp4_repack_bytes(1, 16) == 512 + 16 + 16
+    assert nv.nvfp4_repack_bytes(129, 80) == 256 * 8 + 656 + 16
     assert nv.nvfp4_repack_bytes(0, 16) == 0 and nv.nvfp4_repack_bytes(4, 24) == 0
-    assert nv.nvfp4_workspace_bytes(1, 1, 5120, 17408, nv.NVFP4_W4A16) == 0
+    assert nv.nvfp4_workspace_bytes(1, 1, 5120, 17408, nv.NVFP4_W4A16) == 256
     assert nv.nvfp4_workspace_bytes(1, 512, 5120, 34816, nv.NVFP4_W4A16) > 0
     assert nv.nvfp4_workspace_bytes(0, 10, 48) > 0
     assert nv.nvfp4_workspace_bytes(1, 1, 48, 4, nv.NVFP4_W4A16) == 2 ** 64 - 1  # K % 32
     xq, xs, gx = nv.nvfp4_w4a4_workspace_layout(2048, 5120)
-    assert xq >= 4 and xs >= xq + 2048 * 2560 and gx >= xs + nv.nvfp4_repack_bytes(2048, 5120)
+    assert xq >= 4 and xs >= xq + 2048 * 2560 and gx >= xs + 2048 * 320
     assert xq % 16 == 0 and xs % 16 == 0 and gx % 4 == 0
     total = nv.nvfp4_workspace_bytes(1, 2048, 5120, 17408, nv.NVFP4_W4A4)
     assert total >= gx + 4
@@ -125,7 +125,9 @@ def test_linear_rejects(lib):
     assert _l(lib, gw=66) == ALIGN
     assert _l(lib, mode=1) == WORKSPACE        # W4A4 needs its workspace
     assert _l(lib, mode=1, ws=4096, wsb=64) == WORKSPACE
-    assert _l(lib, M=512, K=64, N=8) == WORKSPACE  # tensor-core path needs the error word
+    assert _l(lib, M=512, K=64, N=8) == WORKSPACE  # every path needs the error word
+    assert _l(lib, M=1, K=64, N=8) == WORKSPACE
+    assert _l(lib, M=1, K=64, N=8, ws=4096, wsb=255) == WORKSPACE
 
 
 def test_encode_elements_rejects(lib):

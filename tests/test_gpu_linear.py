@@ -27,6 +27,7 @@ def run_linear(x, wq, ws, gw, K, y_dtype, mode="w4a16", gx=None):
     d_gx = None if gx is None else torch.tensor([gx], dtype=torch.float32, device="cuda")
     nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, mode=mode, x_global_scale=d_gx, workspace=ws_t)
     torch.cuda.synchronize()
+    assert nv.nvfp4_workspace_error(ws_t) == 0
     return y, ws_t
 
 
@@ -96,8 +97,8 @@ def test_w4a4_small_m(M, K, N, gx):
     o_xq, o_xs, o_gx = nv.nvfp4_w4a4_workspace_layout(M, K)
     wsh = ws_t.cpu().numpy()
     np.testing.assert_array_equal(wsh[o_xq:o_xq + M * K // 2].reshape(M, K // 2), xq)
-    nb = nv.nvfp4_repack_bytes(M, K)
-    np.testing.assert_array_equal(wsh[o_xs:o_xs + nb], oracle.repack(xs, K))
+    nb = oracle.repack_atom_bytes(M, K)
+    np.testing.assert_array_equal(wsh[o_xs:o_xs + nb], oracle.repack(xs, K)[:nb])
     assert wsh[o_gx:o_gx + 4].view(np.float32)[0] == np.float32(gxo)
     check_tolerance(y_to_f64(y), y_ref, ab, "w4a4 M%d" % M)
 
@@ -118,9 +119,41 @@ def test_tiny_config_on_a_side_stream():
     s = torch.cuda.Stream()
     y = torch.empty(1, 256, dtype=torch.float32, device="cuda")
     d_x = x.cuda()
+    work = torch.zeros(nv.nvfp4_workspace_bytes(1, 1, 512, 256), dtype=torch.uint8,
+                       device="cuda")
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
-        nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y)
+        nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, workspace=work)
     s.synchronize()
     y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
     check_tolerance(y_to_f64(y), y_ref, ab, "side stream")
+
+
+@pytest.mark.parametrize("M,K", [(1, 320), (1, 4096), (3, 320), (9, 320), (16, 320),
+                                 (7, 2048)])
+def test_x_with_wide_dynamic_range(M, K):
+    # a few elements far below their row's largest magnitude are not exact in fp16 after
+    # the kernels' power-of-two rescale; the exact residual path must keep the result
+    N = 70
+    x, w = make_inputs(M, K, N, seed=300 + M)
+    xf = x.float()
+    xf[:, ::7] *= 1e-12
+    xf[:, 5] = 3.0e4
+    xf[0, 9] = -2.0e-30
+    x = xf.to(torch.bfloat16)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    for ydt in (torch.float32, torch.bfloat16):
+        y, _ = run_linear(x, wq, ws, gw, K, ydt)
+        y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+        check_tolerance(y_to_f64(y), y_ref, ab, "wide range M%d" % M)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 20480, 300), (8, 12288, 200), (16, 6144, 100),
+                                   (1, 2048, 1000), (1, 65536, 40), (1, 98304, 20)])
+def test_multiple_k_chunks(M, K, N):
+    # K larger than one shared-memory chunk of x
+    x, w = make_inputs(M, K, N, seed=400 + M)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, _ = run_linear(x, wq, ws, gw, K, torch.float32)
+    y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+    check_tolerance(y_to_f64(y), y_ref, ab, "chunks M%d K%d" % (M, K))

@@ -1,10 +1,10 @@
 """Pins of the oracle's swizzled scale layout.
 
-The layout is the tensor-core block-scale layout for 16-element blocks: atoms of
+The layout starts with the tensor-core block-scale layout for 16-element blocks: atoms of
 128 rows x 4 scale columns stored as 512 contiguous bytes, 32 lines of 16 bytes, line
 i holding rows i, i+32, i+64, i+96 (4 bytes each, one per scale column); atoms follow
-each other along K first, then along rows.  The offsets below are worked out by hand
-from that description.  The GPU W4A4 tensor-core result is the second pin: it reads
+each other along K first, then along rows; a plain row-major copy of the scales follows
+(for the GEMV).  The offsets below are worked out by hand from that description.  The GPU W4A4 tensor-core result is the second pin: it reads
 scales in this layout.
 """
 import numpy as np
@@ -24,10 +24,16 @@ def test_hand_derived_offsets():
 
 
 def test_sizes_and_padding():
-    assert oracle.repack_bytes(128, 64) == 512
-    assert oracle.repack_bytes(1, 16) == 512          # 1 row, 1 block -> one atom
-    assert oracle.repack_bytes(129, 80) == 256 * 8    # 5 blocks pad to 8
-    assert oracle.repack_bytes(17408, 5120) == 17408 * 320
+    # atom part: rows padded to 128, blocks to 4
+    assert oracle.repack_atom_bytes(128, 64) == 512
+    assert oracle.repack_atom_bytes(1, 16) == 512          # 1 row, 1 block -> one atom
+    assert oracle.repack_atom_bytes(129, 80) == 256 * 8    # 5 blocks pad to 8
+    assert oracle.repack_atom_bytes(17408, 5120) == 17408 * 320
+    # then the row-major copy, padded to 16 bytes, plus 16 bytes
+    assert oracle.repack_bytes(128, 64) == 512 + 512 + 16
+    assert oracle.repack_bytes(1, 16) == 512 + 16 + 16
+    assert oracle.repack_bytes(129, 80) == 2048 + 656 + 16   # 645 -> 656
+    assert oracle.repack_bytes(17408, 5120) == 2 * 17408 * 320 + 16
 
 
 def test_bijection_and_zero_padding():
@@ -40,8 +46,13 @@ def test_bijection_and_zero_padding():
                          for r in range(rows)])
         assert len(np.unique(offs)) == offs.size      # injective
         np.testing.assert_array_equal(out[offs], s)   # the inverse recovers the scales
+        atom = oracle.repack_atom_bytes(rows, cols)
+        assert offs.max() < atom
+        # the row-major copy follows the atom part
+        np.testing.assert_array_equal(out[atom:atom + s.size].reshape(s.shape), s)
         mask = np.ones(out.size, dtype=bool)
         mask[offs.ravel()] = False
+        mask[atom:atom + s.size] = False
         assert not out[mask].any()                    # padding is zero
 
 
