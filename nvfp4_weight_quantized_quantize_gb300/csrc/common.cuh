@@ -181,6 +181,22 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// L2 prefetch of a global range (16-byte aligned start, size a multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: the next kernel on the stream may be scheduled once every
+// CTA of this grid has issued launch_dependents; wait_prior_grid blocks until the grid
+// before this one has completed and its memory writes are visible (a no-op when the
+// kernel was launched without the programmatic attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // wall-time limit of every device-side wait: far beyond any legitimate wait
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

@@ -241,7 +241,8 @@ gemv_m1_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict_
                     const uint16_t* xr = x + kc0 + 32 * c;
 #pragma unroll 4
                     for (int k = 0; k < 32; ++k) {
-                        const uint32_t code = (w[k >> 3] >> (4 * (k & 7))) & 15u;
+                        const uint32_t wk = k < 16 ? (k < 8 ? w[0] : w[1]) : (k < 24 ? w[2] : w[3]);
+                        const uint32_t code = (wk >> (4 * (k & 7))) & 15u;
                         const float r = residual(xr[k], e) * e2m1_to_f32(code);
                         if (k < 16) q0 += r; else q1 += r;
                     }
@@ -288,12 +289,6 @@ gemv_m1_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict_
 constexpr int kPipeMaxThreads = 1024;
 constexpr int kPipeStageTarget = 32 * 1024;  // bytes of codes per stage (whole rows)
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 // exact x * 2^e for a bf16 value (two multiplies keep 2^e representable for any e)
 __device__ __forceinline__ float pow2_scale(float v, float f1, float f2) { return v * f1 * f2; }
 
@@ -335,6 +330,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     const int nst = (nrows + rps - 1) / rps;
     const int64_t rowb = K >> 1, rows_sb = K >> 4;  // code and scale bytes per row
 
+    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
@@ -349,6 +345,13 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     if (warp == ngroups) {
         // ---- producer ----
         if (lane == 0) {
+            // the first ring's worth of codes heads for L2 while the previous kernel on the
+            // stream may still run (a prefetch cannot observe stale data: L2 is the point of
+            // coherence); every read that lands in shared memory comes after the wait
+            for (int it = 0; it < min(nst, stages); ++it)
+                prefetch_l2(wq + (r0 + (int64_t)it * rps) * rowb,
+                            (uint32_t)(min(rps, nrows - it * rps) * rowb));
+            pdl_wait_prior_grid();
             int issued = 0;
             for (int it = 0; it < nst; ++it) {
                 const int s = it % stages;
@@ -379,6 +382,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     }
 
     // ---- consumers: the amax of x, then this lane's 32 values of x in registers ----
+    pdl_wait_prior_grid();
     float am = 0.0f;
     const uint32_t* xw = reinterpret_cast<const uint32_t*>(x);
     for (int i = threadIdx.x; i < (K >> 1); i += nthreads_c) {
@@ -464,7 +468,8 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                     const uint16_t* xrow = x + 32 * c;
 #pragma unroll 1
                     for (int k = 0; k < 32; ++k) {
-                        const uint32_t code = (w[k >> 3] >> (4 * (k & 7))) & 15u;
+                        const uint32_t wk = k < 16 ? (k < 8 ? w[0] : w[1]) : (k < 24 ? w[2] : w[3]);
+                        const uint32_t code = (wk >> (4 * (k & 7))) & 15u;
                         const float xv32 = bf16_to_f32(xrow[k]);
                         const float hi = __half2float(__float2half_rn(pow2_scale(xv32, f1, f2)));
                         const float r = (ldexpf(xv32, e) - hi) * e2m1_to_f32(code);
@@ -697,7 +702,8 @@ gemv_mma_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* __r
                                 const uint16_t* xr = x + (int64_t)m * K + kc0 + 32 * ch;
                                 float q0 = 0.0f, q1 = 0.0f;
                                 for (int k = 0; k < 32; ++k) {
-                                    const uint32_t code = (ww[k >> 3] >> (4 * (k & 7))) & 15u;
+                                    const uint32_t wk = k < 16 ? (k < 8 ? ww[0] : ww[1]) : (k < 24 ? ww[2] : ww[3]);
+                                    const uint32_t code = (wk >> (4 * (k & 7))) & 15u;
                                     const float r = residual(xr[k], e_sh[m]) * e2m1_to_f32(code);
                                     if (k < 16) q0 += r; else q1 += r;
                                 }
@@ -806,10 +812,22 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     static std::atomic<uint64_t> configured{0};
     cudaError_t e = opt_in_smem(gemv_m1_pipe_kernel<G>, dev, configured);
     if (e != cudaSuccess) return e;
-    gemv_m1_pipe_kernel<G><<<grid, (ngroups + 1) * 32, smem, stream>>>(
-        x, K, wq, wrm, gw, gx, N, y, y_bf16 ? 1 : 0, rows_max, rps, stages, err);
+    // launched as a programmatic dependent: its prologue and first L2 prefetches overlap
+    // the tail of the kernel before it on the stream
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((ngroups + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G>, x, K, wq, wrm, gw, gx, N, y,
+                           y_bf16 ? 1 : 0, rows_max, rps, stages, err);
     *launched = true;
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_m1(const uint16_t* x, int K, const uint8_t* wq, const uint8_t* wsz,
