@@ -108,6 +108,15 @@ __device__ __forceinline__ uint32_t ld_nc_u16(const void* p) {
 }
 
 
+// four bytes of E2M1 code pairs -> four f16x2 (exact; element 2i in the low half)
+__device__ __forceinline__ void cvt8(uint32_t w, uint32_t (&h)[4]) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
 // ---- mbarriers, bulk copies, bounded waits (sm_90+ / sm_100 PTX) ---------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

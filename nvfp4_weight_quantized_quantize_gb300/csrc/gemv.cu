@@ -43,16 +43,6 @@ constexpr int kXSmemBytesMma = 88 * 1024;  // the same for the mma path (K = 512
 
 // ---- element helpers -----------------------------------------------------------------
 
-// 8 codes of a word (element 2i in the low nibble of byte i) -> 4 f16x2 (element 2i in
-// the low half of h[i]).
-__device__ __forceinline__ void cvt8(uint32_t w, uint32_t (&h)[4]) {
-    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-        : "r"(w));
-}
-
 // two codes (one byte, element 2i in the low nibble) -> f16x2
 __device__ __forceinline__ uint32_t cvt2(uint32_t byte_in_low_bits) {
     uint32_t h;

@@ -44,6 +44,12 @@ cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
 
 constexpr int kGemvMaxM = 16;
 
+// M > 16 W4A16 GEMM on the tensor cores (tcgen05, TMA).  wsz: the atom part of the
+// repacked scales (offset 0 of the repacked buffer).  y = *gw * x . W^T.
+cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
+                              const uint8_t* wsz, const float* gw, int N, void* y, bool y_bf16,
+                              uint32_t* err, cudaStream_t stream, const DevInfo& dev);
+
 // The current device's cached properties; NVFP4_ERR_DEVICE unless it is sm_103
 // (the status is returned as an int holding an nvfp4_status).
 int query_device(DevInfo* out);

@@ -231,7 +231,9 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
             return from_cuda(launch_gemv_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
                                                w_global_scale, nullptr, (int)N, y, ybf,
                                                static_cast<uint32_t*>(workspace), stream, d));
-        return NVFP4_ERR_UNSUPPORTED;
+        return from_cuda(launch_gemm_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                           w_global_scale, (int)N, y, ybf,
+                                           static_cast<uint32_t*>(workspace), stream, d));
     }
     // W4A4: quantize x into the workspace (bit-exact with nvfp4_quantize + nvfp4_repack)
     uint8_t* ws = static_cast<uint8_t*>(workspace);
