@@ -375,6 +375,25 @@ def measure_rows(torch, nv, setup):
         rows["a4_verify_%s_M7_K%d_N%d" % (name, wl.K, wl.N)] = {
             "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
         del cps, p, z
+    # a5 prefill M=512 W4A16 on the tensor cores (2 weight copies, inputs > L2)
+    pk, _ = peaks()
+    for name in ("prefill_a", "prefill_b"):
+        wl = WORKLOADS[name]
+        x, w = workload_inputs(name)
+        p, _, z, gg = nv.quantize_weight(w.cuda())
+        del w
+        cps = [(p, z), (p.clone(), z.clone())]
+        xd = x.cuda()
+        y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+        wsv = torch.zeros(nv.nvfp4_workspace_bytes(1, wl.M, wl.K, wl.N), dtype=torch.uint8,
+                          device="cuda")
+        ms = time_graph(torch, lambda i: nv.nvfp4_linear(xd, cps[i % 2][0], cps[i % 2][1],
+                                                         gg, y, workspace=wsv), 4, 5)
+        tf = 2.0 * wl.M * wl.N * wl.K / (ms * 1e-3) / 1e12
+        rows["a5_prefill_%s_M%d_K%d_N%d" % (name, wl.M, wl.K, wl.N)] = {
+            "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
+            "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4)}
+        del cps, p, z
     torch.cuda.synchronize()
     return rows
 

@@ -22,6 +22,15 @@
 //   warps 6-13  dequantize: each thread one (W row, 32-wide K half) per step, e2m1 ->
 //               f16 (hardware converter) -> f32 x scale -> bf16, written in the 128-byte
 //               swizzled K-major layout the MMA descriptor names.
+// Work split: tiles beyond the last full wave (all tiles when there are fewer tiles than
+// SMs) go stream-K: their (tile, K step) iterations are cut into equal contiguous ranges,
+// one per CTA, so every SM gets the same number of MMAs.  A range that covers a tile only
+// in part leaves an fp32 partial tile in one of the CTA's two workspace slots; per quarter
+// of the tile (one epilogue warp each), the warp whose arrival completes the count
+// (atomicInc on a per-quarter counter, which wraps back to zero) adds the partials in
+// segment order -- a fixed order, so results are deterministic -- and writes y.  No CTA
+// or warp waits for another.  The remaining full waves of
+// tiles are split plainly, one tile at a time.
 // Ring of kStages stages (mbarriers: full = TMA bytes landed, afull = dequantized tile
 // written, empty = the stage's MMAs completed); accumulators double-buffered so the
 // epilogue of one tile overlaps the main loop of the next.  Out-of-range rows and K
@@ -65,6 +74,8 @@ constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffLut = (kOffMisc + 16 + 15) & ~15u;
 constexpr uint32_t kSmemUsed = kOffLut + 128 * 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+constexpr int kMaxSkCtas = 160;                     // CTAs in the stream-K part, at most
+constexpr size_t kSlotFloats = (size_t)kBN * kBM;   // one fp32 partial tile
 
 // ---- tcgen05 / TMA wrappers ------------------------------------------------------------
 
@@ -170,11 +181,64 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// The CTA's work: first its stream-K range of (tile, K step) iterations over the first
+// ntiles_sk tiles, cut at tile boundaries, then whole tiles ntiles_sk + c, + grid, ...
+struct WorkIter {
+    int64_t i, i_end;
+    int dp, ntiles, nkb, stride;
+    __device__ bool next(int& tile, int& kb0, int& kb1) {
+        if (i < i_end) {
+            tile = (int)(i / nkb);
+            kb0 = (int)(i - (int64_t)tile * nkb);
+            const int64_t left = i_end - i;
+            kb1 = left < (int64_t)(nkb - kb0) ? kb0 + (int)left : nkb;
+            i += kb1 - kb0;
+            return true;
+        }
+        if (dp < ntiles) {
+            tile = dp;
+            kb0 = 0;
+            kb1 = nkb;
+            dp += stride;
+            return true;
+        }
+        return false;
+    }
+};
+
+__device__ __forceinline__ WorkIter make_iter(int ntiles, int nkb, int ntiles_sk, int p_sk,
+                                              int64_t tsk) {
+    WorkIter w;
+    const int c = blockIdx.x;
+    if (c < p_sk) {
+        w.i = (int64_t)c * tsk / p_sk;
+        w.i_end = (int64_t)(c + 1) * tsk / p_sk;
+    } else {
+        w.i = w.i_end = 0;
+    }
+    w.dp = ntiles_sk + c;
+    w.ntiles = ntiles;
+    w.nkb = nkb;
+    w.stride = gridDim.x;
+    return w;
+}
+
+// stream-K bookkeeping: the CTA whose range holds iteration i, and the slot CTA c uses for
+// its partial of the tile starting at iteration t0 (2c: its first segment, 2c + 1: its last)
+__device__ __forceinline__ int sk_cta_of(int64_t i, int p_sk, int64_t tsk) {
+    return (int)(((i + 1) * p_sk - 1) / tsk);
+}
+__device__ __forceinline__ int sk_slot(int c, int64_t t0, int p_sk, int64_t tsk) {
+    return 2 * c + ((int64_t)c * tsk / p_sk < t0 ? 1 : 0);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                   const __grid_constant__ CUtensorMap tmap_w, const uint8_t* __restrict__ wsz,
                   const float* __restrict__ gw, void* __restrict__ y, int y_bf16, int M, int N,
-                  int nkb, int ntiles_m, int ntiles, uint32_t* __restrict__ err) {
+                  int nkb, int ntiles_m, int ntiles, int ntiles_sk, int p_sk, int64_t tsk,
+                  uint32_t* __restrict__ err, uint32_t* __restrict__ counters,
+                  float* __restrict__ slots) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -219,9 +283,11 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             int it = 0, issued = 0;
-            for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x) {
+            WorkIter wi = make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
+            int tile, kb0, kb1;
+            while (!*abort_flag && wi.next(tile, kb0, kb1)) {
                 const int nb = tile / ntiles_m, mb = tile % ntiles_m;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     if (it >= kStages &&
                         !wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err))
@@ -248,14 +314,16 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             int it = 0, lt = 0;
-            for (int tile = blockIdx.x; tile < ntiles && !*abort_flag; tile += gridDim.x, ++lt) {
+            WorkIter wi = make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
+            int tile, kb0, kb1;
+            for (; !*abort_flag && wi.next(tile, kb0, kb1); ++lt) {
                 const int b = lt & 1;
                 if (lt >= 2 && !wait_or_abort(accempty(b), ((lt >> 1) - 1) & 1, abort_flag, err))
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * kBM);
                 bool ok = true;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
                     if (!wait_or_abort(full(s), ph, abort_flag, err) ||
@@ -269,7 +337,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16(d, sw128_desc(a_s + kk * 32), sw128_desc(x_s + kk * 32), kIdesc,
-                                 (kb | kk) != 0);
+                                 (kb != kb0 || kk != 0) ? 1u : 0u);
                     mma_commit(empty(s));
                 }
                 if (!ok) break;
@@ -283,21 +351,34 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
     } else if (warp < kEpiWarp0 + 4) {
         // ---------------- epilogue ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int nl = q * 32 + lane;                   // W row of the tile (TMEM lane)
         const float g = *gw;
         int lt = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++lt) {
+        WorkIter wi = make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
+        int tile, kb0, kb1;
+        for (; wi.next(tile, kb0, kb1); ++lt) {
             const int b = lt & 1;
             const bool ok = __all_sync(0xffffffffu,
                                        wait_or_abort(accfull(b), (lt >> 1) & 1, abort_flag, err));
             if (!ok) break;
             tc_fence_after();
             const int nb = tile / ntiles_m, mb = tile % ntiles_m;
-            const int64_t n = (int64_t)nb * kBN + q * 32 + lane;
+            const int64_t n = (int64_t)nb * kBN + nl;
             const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kBM);
+            const bool whole = kb0 == 0 && kb1 == nkb;
+            const int64_t t0 = (int64_t)tile * nkb;
+            float* mine = whole ? nullptr
+                                : slots + (size_t)sk_slot(blockIdx.x, t0, p_sk, tsk) * kSlotFloats;
 #pragma unroll 1
             for (int c0 = 0; c0 < kBM; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(taddr + c0, v);
+                if (!whole) {
+                    // partial tile: fp32 slot, [m within tile][W row within tile]
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mine[(c0 + j) * kBN + nl] = __uint_as_float(v[j]);
+                    continue;
+                }
                 const int64_t m0 = (int64_t)mb * kBM + c0;
                 if (n < N) {
                     if (y_bf16) {
@@ -314,18 +395,68 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     }
                 }
             }
+            // the accumulator is free for the tile after next
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(accempty(b))));
+            if (lane == 0)
+                mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(accempty(b))));
+            if (whole) continue;
+            // count this warp's quarter of the segment in (one counter per tile quarter, so
+            // no epilogue warp ever waits for another); the arrival that completes the
+            // quarter sums it
+            const int cf = sk_cta_of(t0, p_sk, tsk), cl = sk_cta_of(t0 + nkb - 1, p_sk, tsk);
+            const unsigned nseg = (unsigned)(cl - cf + 1);
+            __threadfence();
+            __syncwarp();
+            unsigned old = 0;
+            if (lane == 0) old = atomicInc(&counters[tile * 4 + q], nseg - 1);
+            const bool last = __shfl_sync(0xffffffffu, old, 0) == nseg - 1;
+            if (!last) continue;
+            __threadfence();
+            // 32 rows of the quarter at a time, every partial's 32 loads in flight together;
+            // the partials are added in segment order
+#pragma unroll 1
+            for (int c0 = 0; c0 < kBM; c0 += 32) {
+                const int64_t m0 = (int64_t)mb * kBM + c0;
+                if (m0 >= M) break;
+                float acc[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+                for (int cs = cf; cs <= cl; ++cs) {
+                    const float* sp =
+                        slots + (size_t)sk_slot(cs, t0, p_sk, tsk) * kSlotFloats + c0 * kBN + nl;
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __ldcg(sp + j * kBN);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[j] += v[j];
+                }
+                if (n < N) {
+                    if (y_bf16) {
+                        uint16_t* yp = static_cast<uint16_t*>(y) + m0 * N + n;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (m0 + j < M) yp[(int64_t)j * N] = f32_to_bf16_rne(acc[j] * g);
+                    } else {
+                        float* yp = static_cast<float*>(y) + m0 * N + n;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (m0 + j < M) yp[(int64_t)j * N] = acc[j] * g;
+                    }
+                }
+            }
         }
     } else {
         // ---------------- dequantize ----------------
         const int t = threadIdx.x - kDequantWarp0 * 32;  // 0 .. 255
         const int r = t & (kBN - 1), h = t >> 7;         // W row in the tile, K half
         int it = 0;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        WorkIter wi = make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
+        int tile, kb0, kb1;
+        while (wi.next(tile, kb0, kb1)) {
             bool ok = true;
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % kStages;
                 if (!__all_sync(0xffffffffu,
                                 wait_or_abort(full(s), (it / kStages) & 1, abort_flag, err))) {
@@ -409,10 +540,50 @@ cudaError_t make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType t
 
 }  // namespace
 
+GemmPlan gemm_w4a16_plan(int64_t M, int64_t K, int64_t N, int sm_count) {
+    GemmPlan p;
+    p.nkb = (int)((K + kBK - 1) / kBK);
+    p.ntiles_m = (int)((M + kBM - 1) / kBM);
+    p.ntiles = (int)((N + kBN - 1) / kBN) * p.ntiles_m;
+    // the tiles of the last, partial wave (all of them when fewer than the SMs) go stream-K
+    int sk = p.ntiles >= sm_count ? p.ntiles % sm_count : p.ntiles;
+    const int64_t tsk = (int64_t)sk * p.nkb;
+    // at least 4 K steps per CTA, at most 3 CTAs' worth per tile, at most kMaxSkCtas
+    int64_t psk = sm_count;
+    if (psk > 3 * (int64_t)sk) psk = 3 * (int64_t)sk;
+    if (psk > tsk / 4) psk = tsk / 4;
+    if (psk > kMaxSkCtas) psk = kMaxSkCtas;
+    if (psk < 2) {
+        sk = 0;
+        psk = 0;
+    }
+    p.ntiles_sk = sk;
+    p.p_sk = (int)psk;
+    p.tsk = (int64_t)sk * p.nkb;
+    const int dp = p.ntiles - sk;
+    int grid = dp < sm_count ? dp : sm_count;
+    if (grid < p.p_sk) grid = p.p_sk;
+    p.grid = grid;
+    return p;
+}
+
+size_t gemm_w4a16_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+    // a bound over every SM count: the plan never uses more stream-K CTAs than this
+    const int64_t nkb = (K + kBK - 1) / kBK;
+    const int64_t ntiles = ((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
+    int64_t psk = kMaxSkCtas;
+    if (psk > 3 * ntiles) psk = 3 * ntiles;
+    if (psk > ntiles * nkb / 4) psk = ntiles * nkb / 4;
+    if (psk < 2) psk = 0;
+    const size_t counters = ((size_t)ntiles * 16 + 255) / 256 * 256;
+    return kGemmHeaderBytes + counters + (size_t)(2 * psk) * kSlotFloats * 4;
+}
+
 cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz, const float* gw, int N, void* y, bool y_bf16,
-                              uint32_t* err, cudaStream_t stream, const DevInfo& dev) {
+                              uint8_t* workspace, cudaStream_t stream, const DevInfo& dev) {
     if (dev.smem_optin < kSmemBytes) return cudaErrorInvalidConfiguration;
+    const GemmPlan p = gemm_w4a16_plan(M, K, N, dev.sm_count);
     CUtensorMap mx, mw;
     cudaError_t e = make_map_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K,
                                 (uint64_t)M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -428,12 +599,13 @@ cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    const int nkb = (K + kBK - 1) / kBK;
-    const int ntiles_n = (N + kBN - 1) / kBN, ntiles_m = (M + kBM - 1) / kBM;
-    const int ntiles = ntiles_n * ntiles_m;
-    const int grid = ntiles < dev.sm_count ? ntiles : dev.sm_count;
-    gemm_w4a16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mx, mw, wsz, gw, y, y_bf16 ? 1 : 0,
-                                                              M, N, nkb, ntiles_m, ntiles, err);
+    uint32_t* err = reinterpret_cast<uint32_t*>(workspace);
+    uint32_t* counters = reinterpret_cast<uint32_t*>(workspace + kGemmHeaderBytes);
+    float* slots = reinterpret_cast<float*>(
+        workspace + kGemmHeaderBytes + ((size_t)p.ntiles * 16 + 255) / 256 * 256);
+    gemm_w4a16_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(
+        mx, mw, wsz, gw, y, y_bf16 ? 1 : 0, M, N, p.nkb, p.ntiles_m, p.ntiles, p.ntiles_sk, p.p_sk,
+        p.tsk, err, counters, slots);
     return cudaGetLastError();
 }
 

@@ -46,9 +46,18 @@ constexpr int kGemvMaxM = 16;
 
 // M > 16 W4A16 GEMM on the tensor cores (tcgen05, TMA).  wsz: the atom part of the
 // repacked scales (offset 0 of the repacked buffer).  y = *gw * x . W^T.
+// Workspace: the 256-byte header (error word) | stream-K counters, 4 per tile (zero before
+// the first call; every completed call leaves them zero) | fp32 partial-tile slots.
+constexpr size_t kGemmHeaderBytes = 256;
+struct GemmPlan {
+    int nkb = 0, ntiles_m = 0, ntiles = 0, ntiles_sk = 0, p_sk = 0, grid = 0;
+    int64_t tsk = 0;
+};
+GemmPlan gemm_w4a16_plan(int64_t M, int64_t K, int64_t N, int sm_count);
+size_t gemm_w4a16_workspace_bytes(int64_t M, int64_t K, int64_t N);
 cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz, const float* gw, int N, void* y, bool y_bf16,
-                              uint32_t* err, cudaStream_t stream, const DevInfo& dev);
+                              uint8_t* workspace, cudaStream_t stream, const DevInfo& dev);
 
 // The current device's cached properties; NVFP4_ERR_DEVICE unless it is sm_103
 // (the status is returned as an int holding an nvfp4_status).

@@ -136,7 +136,8 @@ NVFP4_API size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
         return kHeaderBytes + (size_t)kMaxPartials * 4;
     }
     if (op != 1 || M < 1 || K < 32 || K % 32 != 0 || N < 1) return (size_t)-1;
-    if (mode == NVFP4_W4A16) return kHeaderBytes;
+    if (mode == NVFP4_W4A16)
+        return M <= kGemvMaxM ? kHeaderBytes : gemm_w4a16_workspace_bytes(M, K, N);
     if (mode == NVFP4_W4A4) return w4a4_layout(M, K).total;
     return (size_t)-1;
 }
@@ -233,7 +234,7 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
                                                static_cast<uint32_t*>(workspace), stream, d));
         return from_cuda(launch_gemm_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
                                            w_global_scale, (int)N, y, ybf,
-                                           static_cast<uint32_t*>(workspace), stream, d));
+                                           static_cast<uint8_t*>(workspace), stream, d));
     }
     // W4A4: quantize x into the workspace (bit-exact with nvfp4_quantize + nvfp4_repack)
     uint8_t* ws = static_cast<uint8_t*>(workspace);

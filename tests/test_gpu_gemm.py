@@ -79,3 +79,27 @@ def test_gemm_repeated_calls_are_deterministic():
     y1 = run_gemm(x, wq, ws, gw, K, torch.float32)
     y2 = run_gemm(x, wq, ws, gw, K, torch.float32)
     assert torch.equal(y1, y2)
+
+
+def test_stream_k_reuses_its_workspace():
+    # 10 tiles on a 152-SM part: every tile is split over several CTAs (stream-K); the
+    # per-quarter counters must come back to zero so the same workspace serves again
+    M, K, N = 512, 1024, 640
+    x, w = make_inputs(M, K, N, seed=9)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    d_wq, d_swz, d_g = upload_weights(wq, ws, gw, K)
+    xd = x.cuda()
+    work = torch.zeros(nv.nvfp4_workspace_bytes(1, M, K, N, nv.NVFP4_W4A16), dtype=torch.uint8,
+                       device="cuda")
+    ys = []
+    for _ in range(3):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        nv.nvfp4_linear(xd, d_wq, d_swz, d_g, y, workspace=work)
+        torch.cuda.synchronize()
+        assert nv.nvfp4_workspace_error(work) == 0
+        ntiles = ((N + 127) // 128) * ((M + 255) // 256)
+        assert not work[256:256 + 16 * ntiles].any()
+        ys.append(y)
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[1], ys[2])
+    y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+    check_tolerance(y_to_f64(ys[0]), y_ref, ab, "stream-K reuse")
