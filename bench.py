@@ -485,6 +485,34 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_one_workload(name: str, calls: int = 3):
+    """A few nvfp4_linear calls on one workload and nothing else: the command that ncu
+    captures a single kernel from (no timing, no JSON line)."""
+    import torch
+
+    import nvfp4_weight_quantized_quantize_gb300 as nv
+    from nvfp4_weight_quantized_quantize_gb300 import build_lib
+    from synth import WORKLOADS, workload_inputs
+
+    build_lib.build()
+    nv.load()
+    wl = WORKLOADS[name]
+    x, w = workload_inputs(name)
+    packed, _, swz, g = nv.quantize_weight(w.cuda())
+    del w
+    mode = nv.NVFP4_W4A4 if wl.w4a4 else nv.NVFP4_W4A16
+    xd = x.cuda()
+    y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+    work = torch.zeros(nv.nvfp4_workspace_bytes(1, wl.M, wl.K, wl.N, mode), dtype=torch.uint8,
+                       device="cuda")
+    for _ in range(calls):
+        nv.nvfp4_linear(xd, packed, swz, g, y, mode="w4a4" if wl.w4a4 else "w4a16",
+                        workspace=work)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_workspace_error(work) == 0
+    print("ran %d calls of %s" % (calls, name), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -495,7 +523,12 @@ def main():
     ap.add_argument("--rows", type=int, default=1, help="also measure the other rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only-workload", default=None,
+                    help="run a few calls of one workload and exit (for ncu captures)")
     args = ap.parse_args()
+    if args.only_workload:
+        run_one_workload(args.only_workload)
+        return
     if args.warmup < 3:
         args.warmup = 3
 

@@ -71,8 +71,7 @@ constexpr uint32_t kOffScale = kOffCode + kStages * kCodeBytes;
 constexpr uint32_t kOffBar = kOffScale + kStages * kScaleBytes;
 constexpr uint32_t kNumBars = 3 * kStages + 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffLut = (kOffMisc + 16 + 15) & ~15u;
-constexpr uint32_t kSmemUsed = kOffLut + 128 * 4;
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 constexpr int kMaxSkCtas = 160;                     // CTAs in the stream-K part, at most
 constexpr size_t kSlotFloats = (size_t)kBN * kBM;   // one fp32 partial tile
@@ -160,9 +159,22 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             ((uint32_t)(kBM >> 3) << 17) | ((uint32_t)(kBN >> 4) << 24);
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+// two e4m3 bytes (low 16 bits) -> f16x2, exact
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t b2) {
     uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
+        : "=r"(d) : "r"(b2));
+    return d;
+}
+
+// f16x2 codes times an f16 scale -> bf16x2: the products (mixed f16 x f16 -> f32 FMA with a
+// zero addend) are exact in f32, and in bf16 (at most 5 significant bits, in [2^-10, 2688])
+__device__ __forceinline__ uint32_t deq_bf16x2(uint32_t h2, uint32_t s16) {
+    uint32_t d;
+    asm("{\n .reg .f16 a0, a1, s;\n .reg .f32 p0, p1;\n mov.b32 {a0, a1}, %1;\n"
+        " mov.b32 {s, _}, %2;\n fma.rn.f32.f16 p0, a0, s, 0f00000000;\n"
+        " fma.rn.f32.f16 p1, a1, s, 0f00000000;\n cvt.rn.bf16x2.f32 %0, p1, p0;\n}\n"
+        : "=r"(d) : "r"(h2), "r"(s16));
     return d;
 }
 
@@ -253,7 +265,6 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
     const uint32_t drain = bar0 + 8u * (3 * kStages + 4);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
-    float* lut = reinterpret_cast<float*>(base + kOffLut);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -272,7 +283,6 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (threadIdx.x < 128) lut[threadIdx.x] = e4m3_to_f32(threadIdx.x);
     if (warp == 1) tmem_alloc(base_s + kOffMisc, kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -467,20 +477,18 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                                 r * 32 + h * 16);
                 const uint32_t sb = *reinterpret_cast<const uint16_t*>(
                     base + kOffScale + s * kScaleBytes + (r & 31) * 16 + (r >> 5) * 4 + 2 * h);
-                const float s0 = lut[sb & 0x7Fu], s1 = lut[(sb >> 8) & 0x7Fu];
+                // the two block scales as f16 (e4m3 is exact in f16)
+                const uint32_t s01 = cvt_e4m3x2_f16x2(sb);
                 const uint32_t w[4] = {c.x, c.y, c.z, c.w};
                 uint8_t* arow = base + kOffA + s * kABytes + r * 128;
 #pragma unroll
                 for (int qd = 0; qd < 4; ++qd) {
                     uint32_t hh[4];
                     cvt8(w[qd], hh);
-                    const float sc = qd < 2 ? s0 : s1;
+                    const uint32_t sc = qd < 2 ? (s01 & 0xFFFFu) : (s01 >> 16);
                     uint32_t o[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh[i]));
-                        o[i] = pack_bf16x2(f.x * sc, f.y * sc);
-                    }
+                    for (int i = 0; i < 4; ++i) o[i] = deq_bf16x2(hh[i], sc);
                     const int chunk = (4 * h + qd) ^ (r & 7);
                     *reinterpret_cast<uint4*>(arow + chunk * 16) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
