@@ -1,0 +1,244 @@
+// gemm_w4a4.cu -- W4A4 NVFP4 GEMM for M > 16 on the 5th-generation tensor cores, block
+// scaled in hardware.  FlashRT docs/qwen36_usage.md (FLASHRT_QWEN36_FUSE_SILU_MUL_QUANT:
+// activations quantized to NVFP4 feed the NVFP4 GEMM).
+//
+//   y[m, n] = gx * gw * sum_b sx[m, b] * sw[n, b] * sum_{k in b} e2m1(qx[m, k]) * e2m1(qw[n, k])
+//
+// x has been quantized (codes [M, K/2], scale atoms, gx) by the quantizer into the
+// workspace.  tcgen05.mma kind::mxf4nvf4 with 16-element UE4M3 block scales
+// (scale_vec::4X) multiplies the packed E2M1 operands straight from shared memory; the
+// scales go shared -> TMEM with tcgen05.cp (one 512-byte atom of the tensor-core scale
+// layout per 128 rows x 64 K, which is how the repacked scales are stored).
+//
+// CTA tile: 128 rows of W (MMA M) x 128 rows of x (MMA N), K in steps of 256 (128 bytes of
+// codes per row: one 128-byte swizzle row).  Warp roles:
+//   warp 0      TMA producer: per K step the two 128 x 128-byte code boxes (128-byte
+//               swizzle) and the W and x scale atoms of those 256 K (bulk copies);
+//   warp 1      allocates TMEM (two 128-column fp32 accumulators + a scale area per
+//               stage) and, from one thread, copies the stage's scale atoms to TMEM and
+//               issues 4 x 128x128x64 block-scaled MMAs;
+//   warps 2-5   epilogue (shared with the W4A16 GEMM): x gx gw, y fp32 or bf16.
+// Work split, stream-K fixup, bounded waits and error reporting as in the W4A16 GEMM.
+#include <cuda.h>
+
+#include <atomic>
+
+#include "tcgen05.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kBN = 128;   // W rows per tile (MMA M)
+constexpr int kBM = 128;   // x rows per tile (MMA N)
+constexpr int kBK = 256;   // K per stage
+constexpr int kStages = 5;
+constexpr int kThreads = 6 * 32;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kTmemSf = 2 * kBM;             // first TMEM column of the scale area
+constexpr uint32_t kSfColsPerStage = 32;          // 4 W atoms + 4 x atoms, 4 columns each
+
+constexpr uint32_t kCodeBytes = kBN * kBK / 2;    // 16 KB per operand (kBN == kBM)
+constexpr uint32_t kAtomBytes = 512;
+constexpr uint32_t kSfBytes = 4 * kAtomBytes;     // 4 atoms (256 K) per operand
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kCodeBytes;
+constexpr uint32_t kOffSfa = kOffB + kStages * kCodeBytes;
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfBytes;
+constexpr uint32_t kOffBar = kOffSfb + kStages * kSfBytes;
+constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+
+static_assert(kTmemSf + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+
+// Instruction descriptor, block-scaled kind: E2M1 A and B, UE4M3 scales (scale type 0),
+// scale ids 0, dense K = 64 per instruction, both K-major, fp32 D, M x N.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 3) << 17) |
+                            ((uint32_t)(kBN >> 4) << 24);
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                 const __grid_constant__ CUtensorMap tmap_x, const uint8_t* __restrict__ wsz,
+                 const uint8_t* __restrict__ xsz, const float* __restrict__ gw,
+                 const float* __restrict__ gx, void* __restrict__ y, int y_bf16, int M, int N,
+                 int nkb, int natoms_row, int ntiles_m, int ntiles, int ntiles_sk, int p_sk,
+                 int64_t tsk, uint32_t* __restrict__ err, uint32_t* __restrict__ counters,
+                 float* __restrict__ slots) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_s - raw_s);
+    const uint32_t bar0 = base_s + kOffBar;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto accfull = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+    auto accempty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    const uint32_t drain = bar0 + 8u * (2 * kStages + 4);
+    auto bar_ptr = [&](uint32_t a) { return reinterpret_cast<uint64_t*>(base + (a - base_s)); };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_ptr(full(s)), 1);
+            mbar_init(bar_ptr(empty(s)), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_ptr(accfull(b)), 1);
+            mbar_init(bar_ptr(accempty(b)), 4);
+        }
+        mbar_init(bar_ptr(drain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::tmem_alloc(base_s + kOffMisc, kTmemCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // scale atoms of K step kb: 4, or fewer at the end of K
+    auto atoms_of = [&](int kb) { return min(4, natoms_row - 4 * kb); };
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int it = 0, issued = 0;
+            tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
+            int tile, kb0, kb1;
+            while (!*abort_flag && wi.next(tile, kb0, kb1)) {
+                const int nb = tile / ntiles_m, mb = tile % ntiles_m;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (it >= kStages &&
+                        !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err))
+                        break;
+                    const uint32_t sfb = (uint32_t)atoms_of(kb) * kAtomBytes;
+                    mbar_arrive_expect_tx(bar_ptr(full(s)), 2 * kCodeBytes + 2 * sfb);
+                    tc::tma_load_2d(base_s + kOffA + s * kCodeBytes, &tmap_w, kb * (kBK / 2),
+                                    nb * kBN, full(s));
+                    tc::tma_load_2d(base_s + kOffB + s * kCodeBytes, &tmap_x, kb * (kBK / 2),
+                                    mb * kBM, full(s));
+                    bulk_g2s(base + kOffSfa + s * kSfBytes,
+                             wsz + ((size_t)nb * natoms_row + 4 * kb) * kAtomBytes, sfb,
+                             bar_ptr(full(s)));
+                    bulk_g2s(base + kOffSfb + s * kSfBytes,
+                             xsz + ((size_t)mb * natoms_row + 4 * kb) * kAtomBytes, sfb,
+                             bar_ptr(full(s)));
+                    issued = it + 1;
+                }
+            }
+            // every copy issued has landed before the CTA moves on to exit
+            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+                mbar_wait_bounded(bar_ptr(full(i % kStages)), (i / kStages) & 1, kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- scale copies + MMA issue ----------------
+        if (lane == 0) {
+            int it = 0, lt = 0;
+            tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
+            int tile, kb0, kb1;
+            for (; !*abort_flag && wi.next(tile, kb0, kb1); ++lt) {
+                const int b = lt & 1;
+                if (lt >= 2 &&
+                    !tc::wait_or_abort(accempty(b), ((lt >> 1) - 1) & 1, abort_flag, err))
+                    break;
+                tc::fence_after();
+                const uint32_t d = tmem + (uint32_t)(b * kBM);
+                bool ok = true;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!tc::wait_or_abort(full(s), (it / kStages) & 1, abort_flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const int na = atoms_of(kb);
+                    const uint32_t sf = tmem + kTmemSf + (uint32_t)s * kSfColsPerStage;
+                    const uint32_t sfa_s = base_s + kOffSfa + s * kSfBytes;
+                    const uint32_t sfb_s = base_s + kOffSfb + s * kSfBytes;
+                    for (int j = 0; j < na; ++j) {
+                        tc::cp_scale_atom(sf + 4 * j, tc::atom_desc(sfa_s + j * kAtomBytes));
+                        tc::cp_scale_atom(sf + 16 + 4 * j, tc::atom_desc(sfb_s + j * kAtomBytes));
+                    }
+                    const uint32_t a_s = base_s + kOffA + s * kCodeBytes;
+                    const uint32_t b_s = base_s + kOffB + s * kCodeBytes;
+                    for (int j = 0; j < na; ++j)
+                        tc::mma_mxf4nvf4(d, tc::sw128_desc(a_s + j * 32),
+                                         tc::sw128_desc(b_s + j * 32), kIdesc, sf + 4 * j,
+                                         sf + 16 + 4 * j, (kb != kb0 || j != 0) ? 1u : 0u);
+                    tc::commit(empty(s));
+                }
+                if (!ok) break;
+                tc::commit(accfull(b));
+            }
+            // MMAs in flight complete before TMEM is freed
+            tc::commit(drain);
+            mbar_wait_bounded(bar_ptr(drain), 0, kWaitLimitNs);
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const float g = *gw * *gx;
+        int lt = 0;
+        tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
+        int tile, kb0, kb1;
+        for (; wi.next(tile, kb0, kb1); ++lt) {
+            const int b = lt & 1;
+            if (!__all_sync(0xffffffffu,
+                            tc::wait_or_abort(accfull(b), (lt >> 1) & 1, abort_flag, err)))
+                break;
+            tc::fence_after();
+            tc::epilogue_work<kBN, kBM>(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m,
+                                        kb0 == 0 && kb1 == nkb, nkb, p_sk, tsk, g, y, y_bf16, M,
+                                        N, slots, counters, accempty(b));
+        }
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t gemm_w4a4_stream_k_bytes(int64_t M, int64_t K, int64_t N) {
+    return tc::stream_k_bytes(M, K, N, kBN, kBM, kBK);
+}
+
+cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M,
+                             int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
+                             void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
+                             cudaStream_t stream, const DevInfo& dev) {
+    if (dev.smem_optin < kSmemBytes) return cudaErrorInvalidConfiguration;
+    const GemmPlan p = tc::make_plan(M, K, N, dev.sm_count, kBN, kBM, kBK);
+    CUtensorMap mw, mx;
+    cudaError_t e = tc::make_map_2d(&mw, wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2,
+                                    (uint64_t)N, kBK / 2, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    e = tc::make_map_2d(&mx, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)M,
+                        kBK / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    static std::atomic<uint64_t> configured{0};
+    const uint64_t bit = 1ull << (dev.device & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(gemm_w4a4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const int natoms_row = (K + 63) / 64;  // scale atoms per 128-row block
+    uint32_t* counters = reinterpret_cast<uint32_t*>(sk_state);
+    float* slots = reinterpret_cast<float*>(sk_state + tc::counters_bytes(p.ntiles));
+    gemm_w4a4_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(
+        mw, mx, wsz, xsz, gw, gx, y, y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, p.ntiles_m,
+        p.ntiles, p.ntiles_sk, p.p_sk, p.tsk, err, counters, slots);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

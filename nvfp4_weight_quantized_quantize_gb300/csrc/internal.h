@@ -59,6 +59,17 @@ cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
                               const uint8_t* wsz, const float* gw, int N, void* y, bool y_bf16,
                               uint8_t* workspace, cudaStream_t stream, const DevInfo& dev);
 
+// M > 16 W4A4 GEMM (block-scaled tcgen05.mma, kind::mxf4nvf4).  xq [M, K/2] and xsz (scale
+// atoms of x) and gx come from the quantizer; wsz: the atom part of W's repacked scales.
+// y = *gx * *gw * deq(x) . deq(W)^T.  err: the workspace error word; sk_state: stream-K
+// counters (zero before the first call) and partial-tile slots,
+// gemm_w4a4_stream_k_bytes() of them.
+size_t gemm_w4a4_stream_k_bytes(int64_t M, int64_t K, int64_t N);
+cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M,
+                             int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
+                             void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
+                             cudaStream_t stream, const DevInfo& dev);
+
 // The current device's cached properties; NVFP4_ERR_DEVICE unless it is sm_103
 // (the status is returned as an int holding an nvfp4_status).
 int query_device(DevInfo* out);

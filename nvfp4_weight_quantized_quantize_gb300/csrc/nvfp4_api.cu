@@ -82,18 +82,20 @@ int partial_count(int64_t n, const DevInfo& d) {
 }
 
 // W4A4 workspace: header | xq [M, K/2] | xs swizzled | gx (16 B) | partials | deq bf16
+// (M <= 16) | stream-K state of the tensor-core GEMM (M > 16)
 struct W4A4Layout {
-    size_t xq, xs, gx, partials, deq, total;
+    size_t xq, xs, gx, partials, deq, sk, total;
 };
 
-W4A4Layout w4a4_layout(int64_t M, int64_t K) {
+W4A4Layout w4a4_layout(int64_t M, int64_t K, int64_t N) {
     W4A4Layout L;
     L.xq = kHeaderBytes;
     L.xs = round_up(L.xq + (size_t)(M * K / 2), 256);
     L.gx = round_up(L.xs + repack_atom_bytes(M, K), 256);
     L.partials = L.gx + 256;
     L.deq = round_up(L.partials + (size_t)kMaxPartials * 4, 256);
-    L.total = L.deq + (M <= kGemvMaxM ? (size_t)(M * K * 2) : 0);
+    L.sk = round_up(L.deq + (M <= kGemvMaxM ? (size_t)(M * K * 2) : 0), 256);
+    L.total = L.sk + (M > kGemvMaxM ? gemm_w4a4_stream_k_bytes(M, K, N) : 0);
     return L;
 }
 
@@ -138,14 +140,14 @@ NVFP4_API size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
     if (op != 1 || M < 1 || K < 32 || K % 32 != 0 || N < 1) return (size_t)-1;
     if (mode == NVFP4_W4A16)
         return M <= kGemvMaxM ? kHeaderBytes : gemm_w4a16_workspace_bytes(M, K, N);
-    if (mode == NVFP4_W4A4) return w4a4_layout(M, K).total;
+    if (mode == NVFP4_W4A4) return w4a4_layout(M, K, N).total;
     return (size_t)-1;
 }
 
 NVFP4_API nvfp4_status nvfp4_w4a4_workspace_layout(int64_t M, int64_t K, size_t* xq_offset,
                                                    size_t* xs_offset, size_t* gx_offset) {
     if (M < 1 || K < 32 || K % 32 != 0) return NVFP4_ERR_SHAPE;
-    const W4A4Layout L = w4a4_layout(M, K);
+    const W4A4Layout L = w4a4_layout(M, K, 1);  // these offsets do not depend on N
     if (xq_offset) *xq_offset = L.xq;
     if (xs_offset) *xs_offset = L.xs;
     if (gx_offset) *gx_offset = L.gx;
@@ -238,7 +240,7 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
     }
     // W4A4: quantize x into the workspace (bit-exact with nvfp4_quantize + nvfp4_repack)
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const W4A4Layout L = w4a4_layout(M, K);
+    const W4A4Layout L = w4a4_layout(M, K, N);
     float* gx = reinterpret_cast<float*>(ws + L.gx);
     uint16_t* deq = M <= kGemvMaxM ? reinterpret_cast<uint16_t*>(ws + L.deq) : nullptr;
     cudaError_t e = launch_quantize(x, true, M, K, ws + L.xq, ws + L.xs, true, gx,
@@ -249,7 +251,9 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
         return from_cuda(launch_gemv_w4a16(deq, (int)M, (int)K, w_packed, w_scales_swizzled,
                                            w_global_scale, gx, (int)N, y, ybf,
                                            reinterpret_cast<uint32_t*>(ws), stream, d));
-    return NVFP4_ERR_UNSUPPORTED;
+    return from_cuda(launch_gemm_w4a4(ws + L.xq, ws + L.xs, gx, (int)M, (int)K, w_packed,
+                                      w_scales_swizzled, w_global_scale, (int)N, y, ybf,
+                                      reinterpret_cast<uint32_t*>(ws), ws + L.sk, stream, d));
 }
 
 NVFP4_API nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out,

@@ -1,0 +1,370 @@
+// tcgen05.cuh -- pieces shared by the tensor-core GEMMs (sm_100 family PTX): TMA tile loads,
+// TMEM allocation and loads, MMA issue and commit, shared-memory matrix descriptors, the
+// persistent work split (stream-K for the last partial wave of tiles, whole tiles for the
+// rest), the stream-K epilogue, and the host-side tensor-map encoding.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "nvfp4.h"
+
+namespace nvfp4 {
+namespace tc {
+
+// ---- TMA, TMEM, MMA wrappers -------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0,
+                                            int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] . B[smem desc]^T, bf16 inputs, fp32 accumulate
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= block-scaled A . B^T: E2M1 operands (two per byte), one UE4M3 scale per 16
+// elements of K for each row of A and of B, read from TMEM (sfa, sfb), fp32 accumulate
+__device__ __forceinline__ void mma_mxf4nvf4(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// shared -> TMEM copy of one 512-byte scale atom (32 rows of 16 bytes, each row broadcast to
+// the four 32-lane quarters): the layout the block-scaled MMA reads its scales in
+__device__ __forceinline__ void cp_scale_atom(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// arrive (once) on bar when every tcgen05 operation this thread issued so far completes
+__device__ __forceinline__ void commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
+        "%27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle layout: rows
+// of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), the tile based at a
+// 1024-byte boundary; the start address may move by 32-byte K steps inside the row.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;              // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+    d |= (uint64_t)1 << 46;              // descriptor version
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+
+// Descriptor of a 512-byte scale atom: no swizzle, 16-byte rows, 8-row core matrices 128
+// bytes apart.
+__device__ __forceinline__ uint64_t atom_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128 >> 4) << 16;     // leading byte offset
+    d |= (uint64_t)(128 >> 4) << 32;     // stride byte offset
+    d |= (uint64_t)1 << 46;              // descriptor version
+    return d;
+}
+
+// ---- bounded waits -----------------------------------------------------------------------
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, uint32_t* err) {
+    if (*abort_flag) return false;
+    if (mbar_wait_bounded(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bar)), parity,
+                          kWaitLimitNs))
+        return true;
+    if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+}
+
+__device__ __forceinline__ void arrive(uint32_t bar) {
+    mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bar)));
+}
+
+// ---- persistent work split ---------------------------------------------------------------
+
+// The CTA's work: first its stream-K range of (tile, K step) iterations over the first
+// ntiles_sk tiles, cut at tile boundaries, then whole tiles ntiles_sk + c, + grid, ...
+struct WorkIter {
+    int64_t i, i_end;
+    int dp, ntiles, nkb, stride;
+    __device__ bool next(int& tile, int& kb0, int& kb1) {
+        if (i < i_end) {
+            tile = (int)(i / nkb);
+            kb0 = (int)(i - (int64_t)tile * nkb);
+            const int64_t left = i_end - i;
+            kb1 = left < (int64_t)(nkb - kb0) ? kb0 + (int)left : nkb;
+            i += kb1 - kb0;
+            return true;
+        }
+        if (dp < ntiles) {
+            tile = dp;
+            kb0 = 0;
+            kb1 = nkb;
+            dp += stride;
+            return true;
+        }
+        return false;
+    }
+};
+
+__device__ __forceinline__ WorkIter make_iter(int ntiles, int nkb, int ntiles_sk, int p_sk,
+                                              int64_t tsk) {
+    WorkIter w;
+    const int c = blockIdx.x;
+    if (c < p_sk) {
+        w.i = (int64_t)c * tsk / p_sk;
+        w.i_end = (int64_t)(c + 1) * tsk / p_sk;
+    } else {
+        w.i = w.i_end = 0;
+    }
+    w.dp = ntiles_sk + c;
+    w.ntiles = ntiles;
+    w.nkb = nkb;
+    w.stride = gridDim.x;
+    return w;
+}
+
+// stream-K bookkeeping: the CTA whose range holds iteration i, and the slot CTA c uses for
+// its partial of the tile starting at iteration t0 (2c: its first segment, 2c + 1: its last)
+__device__ __forceinline__ int sk_cta_of(int64_t i, int p_sk, int64_t tsk) {
+    return (int)(((i + 1) * p_sk - 1) / tsk);
+}
+__device__ __forceinline__ int sk_slot(int c, int64_t t0, int p_sk, int64_t tsk) {
+    return 2 * c + ((int64_t)c * tsk / p_sk < t0 ? 1 : 0);
+}
+
+// ---- epilogue ----------------------------------------------------------------------------
+
+// y[m0 + j, n] = v[j] * scale for the rows inside M (fp32 or bf16 y)
+__device__ __forceinline__ void store_rows32(void* y, int y_bf16, int64_t M, int64_t N,
+                                             int64_t m0, int64_t n, const float (&v)[32],
+                                             float scale) {
+    if (n >= N) return;
+    if (y_bf16) {
+        uint16_t* yp = static_cast<uint16_t*>(y) + m0 * N + n;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (m0 + j < M) yp[(int64_t)j * N] = f32_to_bf16_rne(v[j] * scale);
+    } else {
+        float* yp = static_cast<float*>(y) + m0 * N + n;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (m0 + j < M) yp[(int64_t)j * N] = v[j] * scale;
+    }
+}
+
+// One work item's epilogue for one epilogue warp: TMEM lane quarter q holds W rows
+// q*32 .. q*32+31 of the tile, columns 0 .. BM-1 the tile's x rows.  A whole tile goes to y;
+// a stream-K segment goes to this CTA's fp32 slot, and the arrival that completes the
+// quarter's count (one counter per tile quarter, wrapping back to zero) adds the quarter's
+// partials in segment order and writes y.  The accumulator is released (accempty) as soon
+// as it has been read.
+template <int BN, int BM>
+__device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int tile,
+                                              int ntiles_m, bool whole, int nkb, int p_sk,
+                                              int64_t tsk, float scale, void* y, int y_bf16,
+                                              int M, int N, float* slots, uint32_t* counters,
+                                              uint32_t accempty) {
+    constexpr size_t kSlotFloats = (size_t)BN * BM;
+    const int nb = tile / ntiles_m, mb = tile % ntiles_m;
+    const int nl = q * 32 + lane;
+    const int64_t n = (int64_t)nb * BN + nl;
+    const uint32_t taddr = acc + ((uint32_t)(q * 32) << 16);
+    const int64_t t0 = (int64_t)tile * nkb;
+    float* mine = whole ? nullptr : slots + (size_t)sk_slot(blockIdx.x, t0, p_sk, tsk) * kSlotFloats;
+#pragma unroll 1
+    for (int c0 = 0; c0 < BM; c0 += 32) {
+        uint32_t u[32];
+        tmem_ld32(taddr + c0, u);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+        if (whole) {
+            store_rows32(y, y_bf16, M, N, (int64_t)mb * BM + c0, n, v, scale);
+        } else {
+            // partial tile: fp32 slot, [x row within tile][W row within tile]
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mine[(c0 + j) * BN + nl] = v[j];
+        }
+    }
+    fence_before();
+    __syncwarp();
+    if (lane == 0) arrive(accempty);
+    if (whole) return;
+    const int cf = sk_cta_of(t0, p_sk, tsk), cl = sk_cta_of(t0 + nkb - 1, p_sk, tsk);
+    const unsigned nseg = (unsigned)(cl - cf + 1);
+    __threadfence();
+    __syncwarp();
+    unsigned old = 0;
+    if (lane == 0) old = atomicInc(&counters[tile * 4 + q], nseg - 1);
+    if (__shfl_sync(0xffffffffu, old, 0) != nseg - 1) return;
+    __threadfence();
+    // 32 rows of the quarter at a time, every partial's 32 loads in flight together; the
+    // partials are added in segment order
+#pragma unroll 1
+    for (int c0 = 0; c0 < BM; c0 += 32) {
+        const int64_t m0 = (int64_t)mb * BM + c0;
+        if (m0 >= M) break;
+        float accv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) accv[j] = 0.0f;
+#pragma unroll 1
+        for (int cs = cf; cs <= cl; ++cs) {
+            const float* sp = slots + (size_t)sk_slot(cs, t0, p_sk, tsk) * kSlotFloats +
+                              (size_t)c0 * BN + nl;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __ldcg(sp + (size_t)j * BN);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) accv[j] += v[j];
+        }
+        store_rows32(y, y_bf16, M, N, m0, n, accv, scale);
+    }
+}
+
+// ---- host side ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D tiled map over a row-major [rows, inner] tensor, zero fill outside it
+inline cudaError_t make_map_2d(CUtensorMap* map, const void* ptr, CUtensorMapDataType type,
+                               int elem_bytes, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                               uint32_t box_rows, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, type, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+constexpr int kMaxSkCtas = 160;  // CTAs in the stream-K part, at most
+
+// Tiles of BN W rows x BM x rows, nkb K steps each.  The tiles of the last, partial wave
+// (all of them when there are fewer than the SMs) go stream-K over p_sk CTAs: at least 4 K
+// steps per CTA, at most 3 CTAs' worth per tile, at most kMaxSkCtas.
+inline GemmPlan make_plan(int64_t M, int64_t K, int64_t N, int sm_count, int bn, int bm,
+                          int bk) {
+    GemmPlan p;
+    p.nkb = (int)((K + bk - 1) / bk);
+    p.ntiles_m = (int)((M + bm - 1) / bm);
+    p.ntiles = (int)((N + bn - 1) / bn) * p.ntiles_m;
+    int sk = p.ntiles >= sm_count ? p.ntiles % sm_count : p.ntiles;
+    const int64_t tsk = (int64_t)sk * p.nkb;
+    int64_t psk = sm_count;
+    if (psk > 3 * (int64_t)sk) psk = 3 * (int64_t)sk;
+    if (psk > tsk / 4) psk = tsk / 4;
+    if (psk > kMaxSkCtas) psk = kMaxSkCtas;
+    if (psk < 2) {
+        sk = 0;
+        psk = 0;
+    }
+    p.ntiles_sk = sk;
+    p.p_sk = (int)psk;
+    p.tsk = (int64_t)sk * p.nkb;
+    const int dp = p.ntiles - sk;
+    int grid = dp < sm_count ? dp : sm_count;
+    if (grid < p.p_sk) grid = p.p_sk;
+    p.grid = grid;
+    return p;
+}
+
+// Stream-K state after a 256-byte header: counters (4 per tile, 256-byte padded), then two
+// fp32 partial-tile slots per stream-K CTA.  A bound over every SM count.
+inline size_t counters_bytes(int64_t ntiles) { return ((size_t)ntiles * 16 + 255) / 256 * 256; }
+inline size_t stream_k_bytes(int64_t M, int64_t K, int64_t N, int bn, int bm, int bk) {
+    const int64_t nkb = (K + bk - 1) / bk;
+    const int64_t ntiles = ((N + bn - 1) / bn) * ((M + bm - 1) / bm);
+    int64_t psk = kMaxSkCtas;
+    if (psk > 3 * ntiles) psk = 3 * ntiles;
+    if (psk > ntiles * nkb / 4) psk = ntiles * nkb / 4;
+    if (psk < 2) psk = 0;
+    return counters_bytes(ntiles) + (size_t)(2 * psk) * (size_t)bn * bm * 4;
+}
+
+}  // namespace tc
+}  // namespace nvfp4
