@@ -34,6 +34,9 @@ DECODE = ("decode_a", "decode_b")
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemv_w4a16_decode_traffic.txt")
 
 
+FP4_NOMINAL_TFLOPS = 13500.0  # dense FP4 tensor peak of a GB300 (nominal, not measured)
+
+
 def algo_bytes(M, K, N, y_bytes=2):
     return N * K // 2 + N * K // 16 + M * K * 2 + M * N * y_bytes + 4
 
@@ -394,6 +397,32 @@ def measure_rows(torch, nv, setup):
             "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
             "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4)}
         del cps, p, z
+    # a6 activation quantization (bf16 x 2048 x 5120) and a7 the W4A4 block-scaled GEMM
+    # (the call quantizes x itself, so its time includes a6)
+    wl = WORKLOADS["w4a4"]
+    x, w = workload_inputs("w4a4")
+    xd = x.cuda()
+    xq = torch.empty(wl.M, wl.K // 2, dtype=torch.uint8, device="cuda")
+    xs = torch.empty(wl.M, wl.K // 16, dtype=torch.uint8, device="cuda")
+    gxd = torch.empty(1, dtype=torch.float32, device="cuda")
+    wsq = torch.empty(nv.nvfp4_workspace_bytes(0, wl.M, wl.K), dtype=torch.uint8, device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_quantize(xd, xq, xs, gxd, wsq), 8, 5)
+    qb = wl.M * wl.K * 2 + wl.M * wl.K // 2 + wl.M * wl.K // 16 + 4
+    rows["a6_act_quant_bf16_%dx%d" % (wl.M, wl.K)] = {"GB/s": round(qb / ms / 1e6, 1),
+                                                      "us": round(ms * 1e3, 1)}
+    p, _, z, gg = nv.quantize_weight(w.cuda())
+    del w
+    cps = [(p, z), (p.clone(), z.clone())]
+    y = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+    wsv = torch.zeros(nv.nvfp4_workspace_bytes(1, wl.M, wl.K, wl.N, nv.NVFP4_W4A4),
+                      dtype=torch.uint8, device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_linear(xd, cps[i % 2][0], cps[i % 2][1], gg, y,
+                                                     mode="w4a4", workspace=wsv), 4, 5)
+    tf = 2.0 * wl.M * wl.N * wl.K / (ms * 1e-3) / 1e12
+    rows["a7_w4a4_M%d_K%d_N%d_incl_act_quant" % (wl.M, wl.K, wl.N)] = {
+        "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
+        "frac_fp4_nominal": round(tf / FP4_NOMINAL_TFLOPS, 4)}
+    del cps, p, z
     torch.cuda.synchronize()
     return rows
 
