@@ -7,17 +7,22 @@
 // x has been quantized (codes [M, K/2], scale atoms, gx) by the quantizer into the
 // workspace.  tcgen05.mma kind::mxf4nvf4 with 16-element UE4M3 block scales
 // (scale_vec::4X) multiplies the packed E2M1 operands straight from shared memory; the
-// scales go shared -> TMEM with tcgen05.cp (one 512-byte atom of the tensor-core scale
-// layout per 128 rows x 64 K, which is how the repacked scales are stored).
+// scales reach TMEM in the layout the block-scaled MMA reads: one 512-byte atom of the
+// tensor-core scale layout (128 rows x 64 K, which is how the repacked scales are stored)
+// is 32 rows of 16 bytes, and TMEM lane 32q + i, columns c .. c+3 hold row i of the atom
+// for every lane quarter q.
 //
 // CTA tile: 128 rows of W (MMA M) x 128 rows of x (MMA N), K in steps of 256 (128 bytes of
 // codes per row: one 128-byte swizzle row).  Warp roles:
 //   warp 0      TMA producer: per K step the two 128 x 128-byte code boxes (128-byte
 //               swizzle) and the W and x scale atoms of those 256 K (bulk copies);
 //   warp 1      allocates TMEM (two 128-column fp32 accumulators + a scale area per
-//               stage) and, from one thread, copies the stage's scale atoms to TMEM and
-//               issues 4 x 128x128x64 block-scaled MMAs;
-//   warps 2-5   epilogue (shared with the W4A16 GEMM): x gx gw, y fp32 or bf16.
+//               stage) and, from one thread, issues 4 x 128x128x64 block-scaled MMAs per
+//               stage once its codes and its scales are in place;
+//   warps 2-5   epilogue (shared with the W4A16 GEMM): x gx gw, y fp32 or bf16;
+//   warps 6-9   scale writers: each thread loads row (lane) of the stage's 8 atoms from
+//               shared memory and stores them to its TMEM lane with one tcgen05.st
+//               (keeping these copies off the MMA thread's in-order tcgen05 queue).
 // Work split, stream-K fixup, bounded waits and error reporting as in the W4A16 GEMM.
 #include <cuda.h>
 
@@ -32,7 +37,8 @@ constexpr int kBN = 128;   // W rows per tile (MMA M)
 constexpr int kBM = 128;   // x rows per tile (MMA N)
 constexpr int kBK = 256;   // K per stage
 constexpr int kStages = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kThreads = 10 * 32;
+constexpr int kSfWarp0 = 6;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kTmemSf = 2 * kBM;             // first TMEM column of the scale area
 constexpr uint32_t kSfColsPerStage = 32;          // 4 W atoms + 4 x atoms, 4 columns each
@@ -45,7 +51,7 @@ constexpr uint32_t kOffB = kOffA + kStages * kCodeBytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kCodeBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfBytes;
 constexpr uint32_t kOffBar = kOffSfb + kStages * kSfBytes;
-constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+constexpr uint32_t kNumBars = 3 * kStages + 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
@@ -75,6 +81,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
     auto accfull = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
     auto accempty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
     const uint32_t drain = bar0 + 8u * (2 * kStages + 4);
+    auto sfull = [&](int s) { return bar0 + 8u * (2 * kStages + 5 + s); };
     auto bar_ptr = [&](uint32_t a) { return reinterpret_cast<uint64_t*>(base + (a - base_s)); };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
@@ -90,6 +97,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             mbar_init(bar_ptr(accempty(b)), 4);
         }
         mbar_init(bar_ptr(drain), 1);
+        for (int s = 0; s < kStages; ++s) mbar_init(bar_ptr(sfull(s)), 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -135,7 +143,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 mbar_wait_bounded(bar_ptr(full(i % kStages)), (i / kStages) & 1, kWaitLimitNs);
         }
     } else if (warp == 1) {
-        // ---------------- scale copies + MMA issue ----------------
+        // ---------------- MMA issue ----------------
         if (lane == 0) {
             int it = 0, lt = 0;
             tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
@@ -150,19 +158,15 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
-                    if (!tc::wait_or_abort(full(s), (it / kStages) & 1, abort_flag, err)) {
+                    const uint32_t ph = (it / kStages) & 1;
+                    if (!tc::wait_or_abort(full(s), ph, abort_flag, err) ||
+                        !tc::wait_or_abort(sfull(s), ph, abort_flag, err)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
                     const int na = atoms_of(kb);
                     const uint32_t sf = tmem + kTmemSf + (uint32_t)s * kSfColsPerStage;
-                    const uint32_t sfa_s = base_s + kOffSfa + s * kSfBytes;
-                    const uint32_t sfb_s = base_s + kOffSfb + s * kSfBytes;
-                    for (int j = 0; j < na; ++j) {
-                        tc::cp_scale_atom(sf + 4 * j, tc::atom_desc(sfa_s + j * kAtomBytes));
-                        tc::cp_scale_atom(sf + 16 + 4 * j, tc::atom_desc(sfb_s + j * kAtomBytes));
-                    }
                     const uint32_t a_s = base_s + kOffA + s * kCodeBytes;
                     const uint32_t b_s = base_s + kOffB + s * kCodeBytes;
                     for (int j = 0; j < na; ++j)
@@ -177,6 +181,42 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             // MMAs in flight complete before TMEM is freed
             tc::commit(drain);
             mbar_wait_bounded(bar_ptr(drain), 0, kWaitLimitNs);
+        }
+    } else if (warp >= kSfWarp0) {
+        // ---------------- scale writers ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int it = 0;
+        tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
+        int tile, kb0, kb1;
+        while (wi.next(tile, kb0, kb1)) {
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int s = it % kStages;
+                if (!__all_sync(0xffffffffu,
+                                tc::wait_or_abort(full(s), (it / kStages) & 1, abort_flag, err))) {
+                    ok = false;
+                    break;
+                }
+                // columns 0..15: the 4 W atoms, 16..31: the 4 x atoms (atoms past the end
+                // of K hold stale bytes that no MMA reads)
+                uint32_t v[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(
+                        base + kOffSfa + s * kSfBytes + j * kAtomBytes + lane * 16);
+                    const uint4 c = *reinterpret_cast<const uint4*>(
+                        base + kOffSfb + s * kSfBytes + j * kAtomBytes + lane * 16);
+                    v[4 * j] = a.x; v[4 * j + 1] = a.y; v[4 * j + 2] = a.z; v[4 * j + 3] = a.w;
+                    v[16 + 4 * j] = c.x; v[17 + 4 * j] = c.y; v[18 + 4 * j] = c.z;
+                    v[19 + 4 * j] = c.w;
+                }
+                tc::tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + kTmemSf +
+                                  (uint32_t)s * kSfColsPerStage, v);
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::arrive(sfull(s));
+            }
+            if (!ok) break;
         }
     } else {
         // ---------------- epilogue ----------------

@@ -70,13 +70,6 @@ __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d, uint64_t adesc, uint64_
         : "memory");
 }
 
-// shared -> TMEM copy of one 512-byte scale atom (32 rows of 16 bytes, each row broadcast to
-// the four 32-lane quarters): the layout the block-scaled MMA reads its scales in
-__device__ __forceinline__ void cp_scale_atom(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
 // arrive (once) on bar when every tcgen05 operation this thread issued so far completes
 __device__ __forceinline__ void commit(uint32_t bar) {
     asm volatile(
@@ -100,6 +93,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32 consecutive TMEM columns of this warp's 32 lanes <- v (each thread its own lane)
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -113,16 +121,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
     d |= (uint64_t)1 << 46;              // descriptor version
     d |= (uint64_t)2 << 61;              // 128-byte swizzle
-    return d;
-}
-
-// Descriptor of a 512-byte scale atom: no swizzle, 16-byte rows, 8-row core matrices 128
-// bytes apart.
-__device__ __forceinline__ uint64_t atom_desc(uint32_t saddr) {
-    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(128 >> 4) << 16;     // leading byte offset
-    d |= (uint64_t)(128 >> 4) << 32;     // stride byte offset
-    d |= (uint64_t)1 << 46;              // descriptor version
     return d;
 }
 
