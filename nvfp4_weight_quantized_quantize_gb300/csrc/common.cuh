@@ -14,14 +14,23 @@ namespace nvfp4 {
 // ---- element rounding (the quantizer's steps 2 and 3) ----------------------------
 
 // E2M1 code of v: nearest magnitude, ties to the even code, |v| >= 6 -> 6, and the
-// sign bit of v.  The seven decision points are the midpoints between neighbouring
-// magnitudes; at a midpoint the comparison is strict when the lower neighbour has the
-// even code (0.25, 1.25, 2.5, 5) and inclusive when the upper one has (0.75, 1.75, 3.5).
+// sign bit of v.  The magnitude comes from the hardware converter (round to nearest even
+// on the E2M1 grid, saturating); the sign bit is copied from v, so a value that rounds to
+// zero keeps its sign (-0.1 -> 0x8).
 __device__ __forceinline__ uint32_t e2m1_encode(float v) {
-    const float a = fabsf(v);
-    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-                 (a >= 3.5f) + (a > 5.0f);
-    return c | ((__float_as_uint(v) >> 28) & 8u);
+    uint32_t r;
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}\n"
+        : "=r"(r) : "f"(0.0f), "f"(fabsf(v)));
+    return (r & 7u) | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// Two codes in one byte: element a in the low nibble, b in the high one (same rounding
+// and sign rule as e2m1_encode).
+__device__ __forceinline__ uint32_t e2m1_encode2(float a, float b) {
+    uint32_t r;
+    asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}\n"
+        : "=r"(r) : "f"(fabsf(b)), "f"(fabsf(a)));
+    return (r & 0x77u) | ((__float_as_uint(a) >> 28) & 8u) | ((__float_as_uint(b) >> 24) & 0x80u);
 }
 
 // E4M3 byte of a non-negative float: hardware round-to-nearest-even with saturation
@@ -56,10 +65,25 @@ __device__ __forceinline__ float global_scale_from_amax(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
 }
 
+// t / d rounded to nearest even, by P. Markstein's correction step ("IA-64 and Elementary
+// Functions", 2000): with r = RN(1/d) and q0 = RN(t r), the residual e = t - d q0 is exact
+// (one FMA) and RN(q0 + e r) is the correctly rounded quotient, provided nothing
+// under- or overflows.  Only the E2M1 code of the quotient is used, so: the caller keeps
+// d in [2^-100, 2^100]; a quotient that may reach 8 in magnitude is returned as +-8 (its
+// code is the saturated one, 6, either way); a tiny one may lose its last bits (its code
+// is zero either way); and the sign is the dividend's (d > 0), so -0 stays -0.
+__device__ __forceinline__ float div_rn_by_recip(float t, float d, float r) {
+    const float q0 = __fmul_rn(t, r);
+    const float e = __fmaf_rn(-q0, d, t);
+    const float q = fabsf(q0) < 8.0f ? fabsf(__fmaf_rn(e, r, q0)) : 8.0f;
+    return copysignf(q, t);
+}
+
 // Quantize one block of 16 fp32 values with global scale g.  Returns the E4M3 scale
 // byte; `lo`/`hi` get the 8 packed bytes (element 2j in the low nibble of byte j).
 // Every step is one correctly rounded fp32 operation, in the reference's order:
-// s_raw = bmax / (6 g), d = e4m3(s) * g, v = t / d.
+// s_raw = bmax / (6 g), d = e4m3(s) * g, v = t / d (the quotient correctly rounded, by
+// a division or by the reciprocal correction above).
 __device__ __forceinline__ uint32_t quantize_block16(const float (&t)[16], float g,
                                                      uint32_t& lo, uint32_t& hi) {
     float bmax = 0.0f;
@@ -70,12 +94,31 @@ __device__ __forceinline__ uint32_t quantize_block16(const float (&t)[16], float
     const float d = __fmul_rn(e4m3_to_f32(s8), g);
     lo = 0u;
     hi = 0u;
+    if (d == 0.0f) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const uint32_t code = (d == 0.0f) ? ((__float_as_uint(t[i]) >> 28) & 8u)
-                                          : e2m1_encode(__fdiv_rn(t[i], d));
-        if (i < 8) lo |= code << (4 * i);
-        else hi |= code << (4 * (i - 8));
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t code = (__float_as_uint(t[i]) >> 28) & 8u;
+            if (i < 8) lo |= code << (4 * i);
+            else hi |= code << (4 * (i - 8));
+        }
+    } else if (d >= 0x1p-100f && d <= 0x1p100f) {
+        const float r = __frcp_rn(d);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            const uint32_t byte = e2m1_encode2(div_rn_by_recip(t[i], d, r),
+                                               div_rn_by_recip(t[i + 1], d, r));
+            if (i < 8) lo |= byte << (4 * i);
+            else hi |= byte << (4 * (i - 8));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+            // an infinite quotient (huge t, tiny d) saturates like any value >= 6
+            const uint32_t byte = e2m1_encode2(copysignf(fminf(fabsf(__fdiv_rn(t[i], d)), 8.0f), t[i]),
+                                               copysignf(fminf(fabsf(__fdiv_rn(t[i + 1], d)), 8.0f), t[i + 1]));
+            if (i < 8) lo |= byte << (4 * i);
+            else hi |= byte << (4 * (i - 8));
+        }
     }
     return s8;
 }

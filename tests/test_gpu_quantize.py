@@ -78,6 +78,45 @@ def test_zero_and_tiny_blocks():
     assert_same_quantization(t)
 
 
+@pytest.mark.parametrize("amax", [1.0, 0.0123456, 3.3e-20, 7.7e25, 1e-36, 1e38])
+def test_quotients_next_to_every_midpoint(amax):
+    """Elements within +-3 ulps of every E2M1 decision point m * d, for every block scale:
+    the element codes hang on the last bit of the fp32 quotient t / d."""
+    f32 = np.float32
+    amax = f32(amax)
+    g = f32(amax / f32(2688.0))
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    rows = []
+    for s in range(1, 127):
+        sval = f32(oracle.e4m3_value(s))
+        bmax = f32(sval * f32(6.0) * g)
+        if not (0 < bmax < amax):
+            continue
+        s8 = int(oracle.e4m3_encode(np.array([bmax / (f32(6.0) * g)], dtype=np.float32))[0])
+        d = f32(f32(oracle.e4m3_value(s8)) * g)
+        if d == 0:
+            continue
+        vals = []
+        for m in mids:
+            c = f32(f32(m) * d)
+            for k in (-3, -2, -1, 0, 1, 2, 3):
+                v = c
+                for _ in range(abs(k)):
+                    v = np.nextafter(v, f32(np.inf) if k > 0 else f32(0))
+                vals.append(v)
+        vals = vals[:45]
+        # 3 blocks: bmax first in each, then the 45 probe values (both signs)
+        row = []
+        for b in range(3):
+            blk = vals[15 * b:15 * b + 15]
+            blk = [(-x if (i + b) % 2 else x) for i, x in enumerate(blk)]
+            row += [bmax] + blk
+        rows.append(row)
+    t = np.array(rows, dtype=np.float32)
+    t[0, 0] = amax  # the tensor's amax
+    assert_same_quantization(torch.from_numpy(t))
+
+
 def test_outliers_and_extreme_ranges():
     for scale in (1e-30, 1e-3, 1.0, 1e30):
         assert_same_quantization(random_w(64, 256, 12, std=scale))
