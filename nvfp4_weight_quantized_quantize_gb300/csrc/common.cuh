@@ -42,6 +42,14 @@ __device__ __forceinline__ uint32_t e4m3_encode_nonneg(float s) {
     return (uint32_t)r & 0xFFu;
 }
 
+// two e4m3 bytes (low 16 bits) -> f16x2, exact
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t b2) {
+    uint32_t d;
+    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
+        : "=r"(d) : "r"(b2));
+    return d;
+}
+
 // Value of a non-negative finite E4M3 byte (0x00..0x7E), exact.
 __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
     const uint32_t e = (b >> 3) & 15u, m = b & 7u;

@@ -75,14 +75,6 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignm
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             ((uint32_t)(kBM >> 3) << 17) | ((uint32_t)(kBN >> 4) << 24);
 
-// two e4m3 bytes (low 16 bits) -> f16x2, exact
-__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t b2) {
-    uint32_t d;
-    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
-        : "=r"(d) : "r"(b2));
-    return d;
-}
-
 // f16x2 codes times an f16 scale -> bf16x2: the products (mixed f16 x f16 -> f32 FMA with a
 // zero addend) are exact in f32, and in bf16 (at most 5 significant bits, in [2^-10, 2688])
 __device__ __forceinline__ uint32_t deq_bf16x2(uint32_t h2, uint32_t s16) {

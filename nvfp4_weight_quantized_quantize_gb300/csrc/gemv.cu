@@ -290,6 +290,8 @@ __host__ __device__ __forceinline__ size_t pipe_slot_bytes(int rows_max, int ngr
     return ((size_t)rows_max * ngroups * 4 + 15) & ~(size_t)15;
 }
 
+// Each CTA releases the next launch on the stream (programmatic dependent launch) once its
+// producer has issued its last copy, so the next kernel's prologue overlaps this one's tail.
 template <int G>
 __global__ void __launch_bounds__(kPipeMaxThreads, 1)
 gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict__ wq,
@@ -320,7 +322,6 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     const int nst = (nrows + rps - 1) / rps;
     const int64_t rowb = K >> 1, rows_sb = K >> 4;  // code and scale bytes per row
 
-    pdl_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
@@ -364,6 +365,9 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                 bulk_g2s(st + (size_t)rps * rowb, wrm + s_lo, (uint32_t)(s_hi - s_lo), &full[s]);
                 issued = it + 1;
             }
+            // every copy of this CTA is in flight: the next kernel on the stream may now
+            // be scheduled (its CTAs overlap only this kernel's tail)
+            pdl_launch_dependents();
             // every copy this thread issued has landed before the CTA can exit
             for (int it = max(0, issued - stages); it < issued; ++it)
                 mbar_wait_bounded(&full[it % stages], (it / stages) & 1, kWaitLimitNs);
@@ -415,6 +419,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     if (inexact) any_inexact_sh = 1;
     named_bar_sync(1, nthreads_c);
     const bool any_inexact = any_inexact_sh != 0;
+    const bool lean = !any_inexact && ngroups * G == rowchunks;
 
     for (int it = 0; it < nst; ++it) {
         const int s = it % stages;
@@ -431,6 +436,43 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
         const int nr = min(rps, nrows - it * rps);
         const int64_t rbeg = r0 + (int64_t)it * rps;
         const uint8_t* sst = st + (size_t)rps * rowb + ((rbeg * rows_sb) & 15);
+        if (lean && nr == rps) {
+            // a full stage, every lane on a real chunk, no residual pass: no predicates
+            const uint8_t* wp = st + ((size_t)rsub * rowchunks + c) * 16;
+            const uint8_t* sp = sst + (size_t)rsub * rows_sb + 2 * c;
+            float* sl = slots + (size_t)(it * rps + rsub) * ngroups + warp;
+            const int wstep = L * rowchunks * 16, sstep = L * rows_sb, slstep = L * ngroups;
+            const int nsteps = rps / L;
+#pragma unroll 2
+            for (int t = 0; t < nsteps; ++t) {
+                const uint4 wv = *reinterpret_cast<const uint4*>(wp);
+                const uint32_t s01 = *reinterpret_cast<const uint16_t*>(sp);
+                const uint32_t s16 = cvt_e4m3x2_f16x2(s01);  // both block scales, exact
+                const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&s16));
+                const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+                float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t hh[4];
+                    cvt8(w[j], hh);
+                    const int b = (j >> 1) * 2;
+                    mfma2(a[b], a[b + 1], hh[0], xh[4 * j + 0]);
+                    mfma2(a[b], a[b + 1], hh[1], xh[4 * j + 1]);
+                    mfma2(a[b], a[b + 1], hh[2], xh[4 * j + 2]);
+                    mfma2(a[b], a[b + 1], hh[3], xh[4 * j + 3]);
+                }
+                float pv = fmaf(sc.x, a[0] + a[1], sc.y * (a[2] + a[3]));
+#pragma unroll
+                for (int o = G / 2; o > 0; o >>= 1) pv += __shfl_xor_sync(0xffffffffu, pv, o);
+                if ((lane % G) == 0) *sl = pv;
+                wp += wstep;
+                sp += sstep;
+                sl += slstep;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            continue;
+        }
         for (int t = 0; t < nr; t += L) {
             const int rl = t + rsub;       // row within the stage
             float pv = 0.0f;
@@ -472,7 +514,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
 #pragma unroll
             for (int o = G / 2; o > 0; o >>= 1) pv += __shfl_xor_sync(0xffffffffu, pv, o);
             if ((lane % G) == 0 && rl < nr)
-                slots[(it * rps + rl) * ngroups + warp] += pv;
+                slots[(it * rps + rl) * ngroups + warp] = pv;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -793,10 +835,13 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     int rps = (int)(kPipeStageTarget / (K / 2));
     if (rps < 1) rps = 1;
     if (rps > rows_max) rps = rows_max;
+    // whole steps of 32/G rows per full stage (the kernel's predicate-free path)
+    constexpr int L = 32 / G;
+    if (rps >= L) rps = rps / L * L;
     // the deepest ring (2..8 stages) that fits one CTA per SM
+    const size_t budget = dev.smem_optin - 2048;
     int stages = 8;
-    while (stages > 2 && pipe_smem(K, rows_max, rps, stages, ngroups) + 2048 > dev.smem_optin)
-        --stages;
+    while (stages > 2 && pipe_smem(K, rows_max, rps, stages, ngroups) > budget) --stages;
     const size_t smem = pipe_smem(K, rows_max, rps, stages, ngroups);
     if (smem + 2048 > dev.smem_optin) return cudaSuccess;
     static std::atomic<uint64_t> configured{0};
@@ -814,8 +859,8 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G>, x, K, wq, wrm, gw, gx, N, y,
-                           y_bf16 ? 1 : 0, rows_max, rps, stages, err);
+    e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G>, x, K, wq, wrm, gw, gx, N,
+                           y, y_bf16 ? 1 : 0, rows_max, rps, stages, err);
     *launched = true;
     return e != cudaSuccess ? e : cudaGetLastError();
 }
