@@ -1,0 +1,79 @@
+// gemv_helpers.cuh -- element helpers of the small-M kernels (M <= 16): E2M1 code pairs
+// to f16, mixed f16 x f16 -> f32 FMAs, the per-row power-of-two rescale that carries bf16
+// x as fp16 (exact for every value within 2^31 of the row maximum, with an exact fp32
+// residual for the rest), and the y store.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+// two codes (one byte, element 2i in the low nibble) -> f16x2
+__device__ __forceinline__ uint32_t cvt2(uint32_t byte_in_low_bits) {
+    uint32_t h;
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n"
+        : "=r"(h)
+        : "r"(byte_in_low_bits));
+    return h;
+}
+
+// p0 += lo(v) * lo(x); p1 += hi(v) * hi(x), fp16 products accumulated in fp32.
+__device__ __forceinline__ void mfma2(float& p0, float& p1, uint32_t v, uint32_t x) {
+    asm("{\n .reg .f16 a0, a1, b0, b1;\n mov.b32 {a0, a1}, %2;\n mov.b32 {b0, b1}, %3;\n"
+        " fma.rn.f32.f16 %0, a0, b0, %0;\n fma.rn.f32.f16 %1, a1, b1, %1;\n}\n"
+        : "+f"(p0), "+f"(p1)
+        : "r"(v), "r"(x));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// E4M3 byte -> f16x2 with the value in both halves (exact: E4M3 is a subset of f16).
+__device__ __forceinline__ uint32_t e4m3_to_h2(uint32_t b) {
+    const __half h = __float2half_rn(e4m3_to_f32(b));
+    const uint32_t u = __half_as_ushort(h);
+    return u | (u << 16);
+}
+
+__device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
+    const uint32_t m = code & 7u;
+    const float v = m < 4u ? 0.5f * (float)m : (m == 7u ? 6.0f : (float)m - 2.0f);
+    return (code & 8u) ? -v : v;
+}
+
+// exponent e with amax * 2^e in [2^14, 2^15) (0 for amax == 0)
+__device__ __forceinline__ int chunk_exponent(float amax) {
+    if (!(amax > 0.0f)) return 0;
+    int E;
+    frexpf(amax, &E);
+    return 15 - E;
+}
+
+__device__ __forceinline__ uint32_t to_h2_scaled(uint32_t bf16x2, int e, bool& inexact) {
+    const float a = ldexpf(bf16_to_f32(bf16x2 & 0xFFFFu), e);
+    const float b = ldexpf(bf16_to_f32(bf16x2 >> 16), e);
+    const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
+    inexact |= (__half2float(ha) != a) | (__half2float(hb) != b);
+    return (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
+}
+
+// residual x' - fp16(x') of one bf16 element, exact in fp32
+__device__ __forceinline__ float residual(uint32_t bf16bits, int e) {
+    const float a = ldexpf(bf16_to_f32(bf16bits), e);
+    return a - __half2float(__float2half_rn(a));
+}
+
+__device__ __forceinline__ void store_y(void* y, int64_t o, float v, int y_bf16) {
+    if (y_bf16) static_cast<uint16_t*>(y)[o] = f32_to_bf16_rne(v);
+    else static_cast<float*>(y)[o] = v;
+}
+
+}  // namespace nvfp4

@@ -44,6 +44,14 @@ cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
 
 constexpr int kGemvMaxM = 16;
 
+// 2 <= M <= 8 W4A16 skinny GEMM streaming W through a shared-memory ring, tensor cores
+// for the arithmetic.  wrm: the row-major part of the repacked scales.  Sets *launched
+// when it took the call (K small enough for its ring); otherwise the caller falls back.
+cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
+                                const uint8_t* wrm, const float* gw, const float* gx, int N,
+                                void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
+                                const DevInfo& dev, bool* launched);
+
 // M > 16 W4A16 GEMM on the tensor cores (tcgen05, TMA).  wsz: the atom part of the
 // repacked scales (offset 0 of the repacked buffer).  y = *gw * x . W^T.
 // Workspace: the 256-byte header (error word) | stream-K counters, 4 per tile (zero before

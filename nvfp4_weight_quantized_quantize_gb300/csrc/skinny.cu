@@ -1,0 +1,381 @@
+// skinny.cu -- W4A16 NVFP4 skinny GEMM for 2 <= M <= 8 (MTP verify: drafts + 1 rows of x
+// against the same weights).  FlashRT docs/qwen36_usage.md
+// (generate_own_speculative_KN_nvfp4 argument table: verify runs K + 1 tokens at once).
+//
+//   y[m, n] = gw * sum_b s[n, b] * sum_{k in b} x[m, k] * e2m1(q[n, k])
+//
+// Bound by HBM (each weight is read once for all M rows of x), so the kernel streams W the
+// way the M = 1 kernel does, and does the arithmetic on the tensor cores:
+//   - one CTA per SM owns a contiguous run of 16-row groups; a producer warp fills a ring
+//     of stages (one 16-row group each: its codes and its row-major scale bytes, two bulk
+//     copies, mbarrier-gated, bounded waits);
+//   - consumer warp w owns the K columns [w CG, (w+1) CG) (CG = 4 U chunks of 32) for the
+//     whole kernel, so its slice of x -- the B fragments of mma.sync m16n8k16, fp16 after a
+//     per-token power-of-two rescale -- is built once and stays in registers;
+//   - per stage and 128-element unit, a lane of quad t takes 16-byte chunk 4u + t of rows g
+//     and g + 8; MMA j (0..7) takes elements 4j .. 4j+3 of those chunks for its k-slots
+//     {2t, 2t+1, 2t+8, 2t+9} (any bijection works when A and B use the same one), with the
+//     block scale folded into A (e2m1 * e4m3 is exact in fp16);
+//   - each warp leaves its 16 x 8 partial tile in a per-stage slot; the warp whose arrival
+//     completes the stage's count adds the slots in warp order (deterministic) and writes
+//     the 16 rows of y.  No warp waits for another.
+// x values that fp16 cannot hold exactly after the rescale (more than about 2^31 below
+// the token's maximum) make every warp add the exact fp32 residual of its slice.
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "nvfp4.h"
+#include "common.cuh"
+#include "gemv_helpers.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kSkMaxGroups = 23;  // consumer warps, at most (plus the producer: 768 threads)
+constexpr int kSkMaxThreads = (kSkMaxGroups + 1) * 32;
+constexpr int kSkRows = 16;  // rows of W per stage (one mma row group)
+
+__host__ __device__ __forceinline__ size_t sk_stage_bytes(int K) {
+    return (((size_t)kSkRows * (K / 2) + (size_t)kSkRows * (K / 16) + 32) + 127) & ~(size_t)127;
+}
+
+// slot area of one stage: ngroups partial tiles of 16 rows x 8 tokens (fp32)
+__host__ __device__ __forceinline__ size_t sk_slot_bytes(int ngroups) {
+    return (size_t)ngroups * kSkRows * 8 * 4;
+}
+
+__host__ __device__ __forceinline__ size_t sk_smem(int K, int ngroups, int stages) {
+    return (size_t)stages * (sk_stage_bytes(K) + sk_slot_bytes(ngroups)) +
+           (size_t)stages * (8 + 8 + 16);  // full, empty barriers; stage counters
+}
+
+template <int U>
+__global__ void __launch_bounds__(kSkMaxThreads, 1)
+skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* __restrict__ wq,
+                   const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
+                   const float* __restrict__ gx, int N, void* __restrict__ y, int y_bf16,
+                   int stages, uint32_t* __restrict__ err) {
+    constexpr int CG = 4 * U;  // 16-byte chunks (32 elements) of K per consumer warp
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int rowchunks = K >> 5;
+    const int ngroups = (rowchunks + CG - 1) / CG;
+    const int nthreads_c = ngroups * 32;
+    const size_t st_bytes = sk_stage_bytes(K);
+    const size_t sl_bytes = sk_slot_bytes(ngroups);
+    uint8_t* ring = smem;
+    float* slots = reinterpret_cast<float*>(smem + (size_t)stages * st_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * (st_bytes + sl_bytes));
+    uint64_t* empty = full + stages;
+    int* cnt = reinterpret_cast<int*>(empty + stages);
+    __shared__ uint32_t amax_bits[8];
+    __shared__ int e_sh[8];
+    __shared__ float pw_sh[8];  // 2^-e of each token (exact)
+    __shared__ int any_inexact_sh;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int nrg_all = (N + kSkRows - 1) / kSkRows;
+    const int rg0 = (int)((int64_t)nrg_all * blockIdx.x / gridDim.x);
+    const int rg1 = (int)((int64_t)nrg_all * (blockIdx.x + 1) / gridDim.x);
+    const int nst = rg1 - rg0;
+    const int64_t rowb = K >> 1, rows_sb = K >> 4;  // code and scale bytes per row
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], ngroups);
+            cnt[s] = 0;
+        }
+        for (int m = 0; m < 8; ++m) amax_bits[m] = 0u;
+        abort_flag = 0;
+        any_inexact_sh = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == ngroups) {
+        // ---- producer ----
+        if (lane == 0) {
+            // the first ring's worth of codes heads for L2 while the previous kernel on the
+            // stream may still run; every read that lands in shared memory comes after the
+            // wait for it
+            for (int it = 0; it < min(nst, stages); ++it) {
+                const int64_t rbeg = (int64_t)(rg0 + it) * kSkRows;
+                prefetch_l2(wq + rbeg * rowb,
+                            (uint32_t)(min((int64_t)kSkRows, (int64_t)N - rbeg) * rowb));
+            }
+            pdl_wait_prior_grid();
+            int issued = 0;
+            for (int it = 0; it < nst; ++it) {
+                const int s = it % stages;
+                if (it >= stages &&
+                    !mbar_wait_bounded(&empty[s], ((it / stages) - 1) & 1, kWaitLimitNs)) {
+                    if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+                    abort_flag = 1;
+                    break;
+                }
+                if (abort_flag) break;
+                const int64_t rbeg = (int64_t)(rg0 + it) * kSkRows;
+                const int nr = (int)min((int64_t)kSkRows, (int64_t)N - rbeg);
+                const uint32_t wbytes = (uint32_t)(nr * rowb);
+                // scale bytes of these rows, copied from a 16-byte boundary
+                const int64_t s_lo = (rbeg * rows_sb) & ~(int64_t)15;
+                const int64_t s_hi = ((rbeg + nr) * rows_sb + 15) & ~(int64_t)15;
+                mbar_arrive_expect_tx(&full[s], wbytes + (uint32_t)(s_hi - s_lo));
+                uint8_t* st = ring + (size_t)s * st_bytes;
+                bulk_g2s(st, wq + rbeg * rowb, wbytes, &full[s]);
+                bulk_g2s(st + (size_t)kSkRows * rowb, wrm + s_lo, (uint32_t)(s_hi - s_lo),
+                         &full[s]);
+                issued = it + 1;
+            }
+            // every copy of this CTA is in flight: the next kernel on the stream may now be
+            // scheduled
+            pdl_launch_dependents();
+            // every copy this thread issued has landed before the CTA can exit
+            for (int it = max(0, issued - stages); it < issued; ++it)
+                mbar_wait_bounded(&full[it % stages], (it / stages) & 1, kWaitLimitNs);
+        }
+        return;
+    }
+
+    // ---- consumers: this warp's slice of x in registers, per-token exponent ----
+    // Every (token, chunk) pair belongs to exactly one consumer thread (token g, chunk
+    // w CG + 4u + t), so one pass of loads gives both the B fragments and, reduced over
+    // the threads of each token, the token's maximum magnitude.
+    pdl_wait_prior_grid();
+    uint2 raw[U][8];
+    float am = 0.0f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int c = warp * CG + 4 * u + t;
+        const bool ok = g < M && c < rowchunks;
+        const uint16_t* xp = x + (int64_t)g * K + 32 * c;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            raw[u][j] = ok ? *reinterpret_cast<const uint2*>(xp + 4 * j) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t w2[2] = {raw[u][j].x, raw[u][j].y};
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                am = fmaxf(am, fmaxf(fabsf(bf16_to_f32(w2[h] & 0xFFFFu)),
+                                     fabsf(bf16_to_f32(w2[h] >> 16))));
+        }
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    // non-negative floats order like their bit patterns
+    if (t == 0 && g < M) atomicMax(&amax_bits[g], __float_as_uint(am));
+    named_bar_sync(1, nthreads_c);
+    if (threadIdx.x < 8) {
+        const int e = chunk_exponent(__uint_as_float(amax_bits[threadIdx.x]));
+        e_sh[threadIdx.x] = e;
+        pw_sh[threadIdx.x] = ldexpf(1.0f, -e);
+    }
+    named_bar_sync(1, nthreads_c);
+
+    // B fragment (unit u, mma j): b0 = token g, elements 4j, 4j+1 of chunk c; b1 = elements
+    // 4j+2, 4j+3 (k-slots 2t, 2t+1 and 2t+8, 2t+9)
+    uint32_t bf[U][8][2];
+    bool inexact = false;
+    const int eg = e_sh[g];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            bf[u][j][0] = to_h2_scaled(raw[u][j].x, eg, inexact);
+            bf[u][j][1] = to_h2_scaled(raw[u][j].y, eg, inexact);
+        }
+    if (inexact) any_inexact_sh = 1;
+    named_bar_sync(1, nthreads_c);
+    const bool any_inexact = any_inexact_sh != 0;
+    const float gscale = *gw * (gx ? *gx : 1.0f);
+
+    for (int it = 0; it < nst; ++it) {
+        const int s = it % stages;
+        // the wait's outcome and the abort flag are made warp-uniform before they steer
+        // control flow: mma.sync and the shuffles below are warp-collective
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (it / stages) & 1,
+                                                                  kWaitLimitNs));
+        if (!ok) {
+            if (err && lane == 0) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+            abort_flag = 1;
+        }
+        if (__any_sync(0xffffffffu, abort_flag != 0)) break;
+        const uint8_t* st = ring + (size_t)s * st_bytes;
+        const int64_t rbeg = (int64_t)(rg0 + it) * kSkRows;
+        const int nr = (int)min((int64_t)kSkRows, (int64_t)N - rbeg);
+        const uint8_t* sst = st + (size_t)kSkRows * rowb + ((rbeg * rows_sb) & 15);
+        const bool rga = g < nr, rgb = g + 8 < nr;  // rows past N hold stale bytes
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = warp * CG + 4 * u + t;
+            const bool cv = c < rowchunks;
+            const uint4 wa = (cv && rga) ? *reinterpret_cast<const uint4*>(st + (size_t)g * rowb + 16 * c)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 wb = (cv && rgb) ? *reinterpret_cast<const uint4*>(st + (size_t)(g + 8) * rowb + 16 * c)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t sa = (cv && rga) ? *reinterpret_cast<const uint16_t*>(sst + (size_t)g * rows_sb + 2 * c) : 0u;
+            const uint32_t sb = (cv && rgb) ? *reinterpret_cast<const uint16_t*>(sst + (size_t)(g + 8) * rows_sb + 2 * c) : 0u;
+            // block scales of the chunk (blocks 2c, 2c+1) as f16, each in both halves
+            const uint32_t ha = cvt_e4m3x2_f16x2(sa), hb = cvt_e4m3x2_f16x2(sb);
+            const uint32_t sa0 = __byte_perm(ha, 0, 0x1010), sa1 = __byte_perm(ha, 0, 0x3232);
+            const uint32_t sb0 = __byte_perm(hb, 0, 0x1010), sb1 = __byte_perm(hb, 0, 0x3232);
+            const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
+            const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                // word q of each chunk: bytes 4q .. 4q+3 = elements 8q .. 8q+7 (block q / 2),
+                // the A registers of MMAs 2q and 2q+1
+                uint32_t ha[4], hb[4];
+                cvt8(wa4[q], ha);
+                cvt8(wb4[q], hb);
+                const uint32_t sca = q < 2 ? sa0 : sa1, scb = q < 2 ? sb0 : sb1;
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int j = 2 * q + jj;
+                    const uint32_t a0 = hmul2(ha[2 * jj], sca), a2 = hmul2(ha[2 * jj + 1], sca);
+                    const uint32_t a1 = hmul2(hb[2 * jj], scb), a3 = hmul2(hb[2 * jj + 1], scb);
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+                        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(bf[u][j][0]), "r"(bf[u][j][1]));
+                }
+            }
+        }
+        // this warp's partial tile: slot[row][token], row g / g + 8, tokens 2t, 2t+1
+        float* mine = slots + ((size_t)s * ngroups + warp) * (kSkRows * 8);
+        mine[g * 8 + 2 * t] = d[0];
+        mine[g * 8 + 2 * t + 1] = d[1];
+        mine[(g + 8) * 8 + 2 * t] = d[2];
+        mine[(g + 8) * 8 + 2 * t + 1] = d[3];
+        if (any_inexact) {
+            // exact residual x' - fp16(x') of this warp's K slice (slow path, rare): lane l
+            // takes row l % 16 and tokens l / 16, l / 16 + 2, ...
+            __syncwarp();
+            const int r = lane & 15;
+            if (r < nr) {
+                for (int m = lane >> 4; m < M; m += 2) {
+                    float q = 0.0f;
+                    for (int c = warp * CG; c < min(rowchunks, (warp + 1) * CG); ++c) {
+                        const uint32_t s2 = *reinterpret_cast<const uint16_t*>(sst + (size_t)r * rows_sb + 2 * c);
+                        for (int k = 0; k < 32; ++k) {
+                            const uint32_t byte = st[(size_t)r * rowb + 16 * c + (k >> 1)];
+                            const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);
+                            const float sc = e4m3_to_f32(k < 16 ? (s2 & 0xFFu) : (s2 >> 8));
+                            q = fmaf(residual(x[(int64_t)m * K + 32 * c + k], e_sh[m]),
+                                     e2m1_to_f32(code) * sc, q);
+                        }
+                    }
+                    mine[r * 8 + m] += q;
+                }
+            }
+        }
+        // count this warp in; the arrival that completes the stage adds the partial tiles
+        // in warp order (every slot's loads in flight together), releases the stage, then
+        // writes the 16 rows of y
+        __threadfence_block();
+        __syncwarp();
+        int old = 0;
+        if (lane == 0) old = atomicAdd(&cnt[s], 1);
+        const bool last = __shfl_sync(0xffffffffu, old, 0) == ngroups - 1;
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (last) {
+            __threadfence_block();
+            const float* base = slots + (size_t)s * ngroups * (kSkRows * 8) + lane;
+#pragma unroll
+            for (int w = 0; w < kSkMaxGroups; ++w)
+                if (w < ngroups) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] += base[(size_t)w * (kSkRows * 8) + 32 * i];
+                }
+            __syncwarp();
+            if (lane == 0) cnt[s] = 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (last) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = lane + 32 * i, r = e >> 3, m = e & 7;
+                if (r < nr && m < M)
+                    store_y(y, (int64_t)m * N + rbeg + r, v[i] * pw_sh[m] * gscale, y_bf16);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+namespace {
+
+template <int U>
+cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
+                            const uint8_t* wrm, const float* gw, const float* gx, int N, void* y,
+                            bool y_bf16, uint32_t* err, cudaStream_t stream, const DevInfo& dev,
+                            bool* launched) {
+    *launched = false;
+    const int rowchunks = K / 32;
+    const int ngroups = (rowchunks + 4 * U - 1) / (4 * U);
+    int grid = dev.sm_count;
+    const int nrg = (N + kSkRows - 1) / kSkRows;
+    if (grid > nrg) grid = nrg;
+    // the deepest ring (2..6 stages) that fits one CTA per SM
+    int stages = 6;
+    while (stages > 2 && sk_smem(K, ngroups, stages) + 2048 > dev.smem_optin) --stages;
+    const size_t smem = sk_smem(K, ngroups, stages);
+    if (smem + 2048 > dev.smem_optin) return cudaSuccess;
+    static std::atomic<uint64_t> configured{0};
+    const uint64_t bit = 1ull << (dev.device & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, skinny_pipe_kernel<U>);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(skinny_pipe_kernel<U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(dev.smem_optin - fa.sharedSizeBytes));
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3((ngroups + 1) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_pipe_kernel<U>, x, M, K, wq, wrm, gw, gx, N,
+                                       y, y_bf16 ? 1 : 0, stages, err);
+    *launched = true;
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
+                                const uint8_t* wrm, const float* gw, const float* gx, int N,
+                                void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
+                                const DevInfo& dev, bool* launched) {
+    *launched = false;
+    if (M < 2 || M > 8) return cudaSuccess;
+    // at most kSkMaxGroups consumer warps: 4 or 8 chunks of K per warp
+    const int rowchunks = K / 32;
+    if ((rowchunks + 3) / 4 <= kSkMaxGroups)
+        return launch_skinny_u<1>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, stream, dev,
+                                  launched);
+    if ((rowchunks + 7) / 8 <= kSkMaxGroups)
+        return launch_skinny_u<2>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, stream, dev,
+                                  launched);
+    return cudaSuccess;
+}
+
+}  // namespace nvfp4
