@@ -12,16 +12,18 @@
 // is 32 rows of 16 bytes, and TMEM lane 32q + i, columns c .. c+3 hold row i of the atom
 // for every lane quarter q.
 //
-// CTA tile: 128 rows of W (MMA M) x 128 rows of x (MMA N), K in steps of 256 (128 bytes of
-// codes per row: one 128-byte swizzle row).  Warp roles:
+// CTA tile: 128 rows of W (MMA M) x 256 rows of x (MMA N), K in steps of 256 (128 bytes of
+// codes per row: one 128-byte swizzle row).  One 256-column fp32 accumulator (the rest of
+// TMEM holds the scales of the stages in flight), so the MMAs of a tile start once the
+// epilogue has read the previous one.  Warp roles:
 //   warp 0      TMA producer: per K step the two 128 x 128-byte code boxes (128-byte
 //               swizzle) and the W and x scale atoms of those 256 K (bulk copies);
-//   warp 1      allocates TMEM (two 128-column fp32 accumulators + a scale area per
-//               stage) and, from one thread, issues 4 x 128x128x64 block-scaled MMAs per
-//               stage once its codes and its scales are in place;
+//   warp 1      allocates TMEM (the accumulator + a scale area per stage) and, from one
+//               thread, issues 4 x 128x256x64 block-scaled MMAs per stage once its codes
+//               and its scales are in place;
 //   warps 2-5   epilogue (shared with the W4A16 GEMM): x gx gw, y fp32 or bf16;
-//   warps 6-9   scale writers: each thread loads row (lane) of the stage's 8 atoms from
-//               shared memory and stores them to its TMEM lane with one tcgen05.st
+//   warps 6-9   scale writers: each thread loads row (lane) of the stage's 12 atoms (4 of
+//               W, 2 x 4 of x) from shared memory and stores them to its TMEM lane
 //               (keeping these copies off the MMA thread's in-order tcgen05 queue).
 // Work split, stream-K fixup, bounded waits and error reporting as in the W4A16 GEMM.
 #include <cuda.h>
@@ -34,23 +36,27 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kBN = 128;   // W rows per tile (MMA M)
-constexpr int kBM = 128;   // x rows per tile (MMA N)
+constexpr int kBM = 256;   // x rows per tile (MMA N)
 constexpr int kBK = 256;   // K per stage
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kThreads = 10 * 32;
 constexpr int kSfWarp0 = 6;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kTmemSf = 2 * kBM;             // first TMEM column of the scale area
-constexpr uint32_t kSfColsPerStage = 32;          // 4 W atoms + 4 x atoms, 4 columns each
+constexpr uint32_t kTmemSf = kBM;                 // first TMEM column of the scale area
+// per stage: 4 W atoms (columns 0..15), then per MMA k-step j the x atoms of rows 0..127
+// and 128..255 (columns 16 + 8j .. 16 + 8j + 7), 4 columns each
+constexpr uint32_t kSfColsPerStage = 48;
 
-constexpr uint32_t kCodeBytes = kBN * kBK / 2;    // 16 KB per operand (kBN == kBM)
+constexpr uint32_t kABytes = kBN * kBK / 2;       // 16 KB of W codes
+constexpr uint32_t kBBytes = kBM * kBK / 2;       // 32 KB of x codes
 constexpr uint32_t kAtomBytes = 512;
-constexpr uint32_t kSfBytes = 4 * kAtomBytes;     // 4 atoms (256 K) per operand
+constexpr uint32_t kSfaBytes = 4 * kAtomBytes;    // 4 atoms (256 K) of W
+constexpr uint32_t kSfbBytes = 8 * kAtomBytes;    // 2 row blocks x 4 atoms of x
 constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffB = kOffA + kStages * kCodeBytes;
-constexpr uint32_t kOffSfa = kOffB + kStages * kCodeBytes;
-constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfBytes;
-constexpr uint32_t kOffBar = kOffSfb + kStages * kSfBytes;
+constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
+constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
 constexpr uint32_t kNumBars = 3 * kStages + 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
@@ -68,7 +74,8 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_x, const uint8_t* __restrict__ wsz,
                  const uint8_t* __restrict__ xsz, const float* __restrict__ gw,
                  const float* __restrict__ gx, void* __restrict__ y, int y_bf16, int M, int N,
-                 int nkb, int natoms_row, int ntiles_m, int ntiles, int ntiles_sk, int p_sk,
+                 int nkb, int natoms_row, int x_row_blocks, int ntiles_m, int ntiles,
+                 int ntiles_sk, int p_sk,
                  int64_t tsk, uint32_t* __restrict__ err, uint32_t* __restrict__ counters,
                  float* __restrict__ slots) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -124,17 +131,25 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err))
                         break;
                     const uint32_t sfb = (uint32_t)atoms_of(kb) * kAtomBytes;
-                    mbar_arrive_expect_tx(bar_ptr(full(s)), 2 * kCodeBytes + 2 * sfb);
-                    tc::tma_load_2d(base_s + kOffA + s * kCodeBytes, &tmap_w, kb * (kBK / 2),
+                    // x rows of the tile: scale row blocks 2 mb and 2 mb + 1 (the second one
+                    // only when it exists; rows past M are masked in the epilogue)
+                    const bool two = 2 * mb + 1 < x_row_blocks;
+                    mbar_arrive_expect_tx(bar_ptr(full(s)),
+                                          kABytes + kBBytes + sfb * (two ? 3u : 2u));
+                    tc::tma_load_2d(base_s + kOffA + s * kABytes, &tmap_w, kb * (kBK / 2),
                                     nb * kBN, full(s));
-                    tc::tma_load_2d(base_s + kOffB + s * kCodeBytes, &tmap_x, kb * (kBK / 2),
+                    tc::tma_load_2d(base_s + kOffB + s * kBBytes, &tmap_x, kb * (kBK / 2),
                                     mb * kBM, full(s));
-                    bulk_g2s(base + kOffSfa + s * kSfBytes,
+                    bulk_g2s(base + kOffSfa + s * kSfaBytes,
                              wsz + ((size_t)nb * natoms_row + 4 * kb) * kAtomBytes, sfb,
                              bar_ptr(full(s)));
-                    bulk_g2s(base + kOffSfb + s * kSfBytes,
-                             xsz + ((size_t)mb * natoms_row + 4 * kb) * kAtomBytes, sfb,
+                    bulk_g2s(base + kOffSfb + s * kSfbBytes,
+                             xsz + ((size_t)(2 * mb) * natoms_row + 4 * kb) * kAtomBytes, sfb,
                              bar_ptr(full(s)));
+                    if (two)
+                        bulk_g2s(base + kOffSfb + s * kSfbBytes + 4 * kAtomBytes,
+                                 xsz + ((size_t)(2 * mb + 1) * natoms_row + 4 * kb) * kAtomBytes,
+                                 sfb, bar_ptr(full(s)));
                     issued = it + 1;
                 }
             }
@@ -149,12 +164,10 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
             int tile, kb0, kb1;
             for (; !*abort_flag && wi.next(tile, kb0, kb1); ++lt) {
-                const int b = lt & 1;
-                if (lt >= 2 &&
-                    !tc::wait_or_abort(accempty(b), ((lt >> 1) - 1) & 1, abort_flag, err))
+                if (lt >= 1 && !tc::wait_or_abort(accempty(0), (lt - 1) & 1, abort_flag, err))
                     break;
                 tc::fence_after();
-                const uint32_t d = tmem + (uint32_t)(b * kBM);
+                const uint32_t d = tmem;
                 bool ok = true;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
@@ -167,16 +180,16 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     tc::fence_after();
                     const int na = atoms_of(kb);
                     const uint32_t sf = tmem + kTmemSf + (uint32_t)s * kSfColsPerStage;
-                    const uint32_t a_s = base_s + kOffA + s * kCodeBytes;
-                    const uint32_t b_s = base_s + kOffB + s * kCodeBytes;
+                    const uint32_t a_s = base_s + kOffA + s * kABytes;
+                    const uint32_t b_s = base_s + kOffB + s * kBBytes;
                     for (int j = 0; j < na; ++j)
                         tc::mma_mxf4nvf4(d, tc::sw128_desc(a_s + j * 32),
                                          tc::sw128_desc(b_s + j * 32), kIdesc, sf + 4 * j,
-                                         sf + 16 + 4 * j, (kb != kb0 || j != 0) ? 1u : 0u);
+                                         sf + 16 + 8 * j, (kb != kb0 || j != 0) ? 1u : 0u);
                     tc::commit(empty(s));
                 }
                 if (!ok) break;
-                tc::commit(accfull(b));
+                tc::commit(accfull(0));
             }
             // MMAs in flight complete before TMEM is freed
             tc::commit(drain);
@@ -197,21 +210,29 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     ok = false;
                     break;
                 }
-                // columns 0..15: the 4 W atoms, 16..31: the 4 x atoms (atoms past the end
-                // of K hold stale bytes that no MMA reads)
-                uint32_t v[32];
+                // columns 0..15: the 4 W atoms; 16 + 8j .. 16 + 8j + 7: x atom j of row blocks
+                // 2 mb and 2 mb + 1 (atoms past the end of K or of M hold stale bytes that no
+                // MMA reads or whose rows the epilogue masks)
+                const uint8_t* sa_s = base + kOffSfa + s * kSfaBytes + lane * 16;
+                const uint8_t* sb_s = base + kOffSfb + s * kSfbBytes + lane * 16;
+                uint32_t v[32], u16[16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint4 a = *reinterpret_cast<const uint4*>(
-                        base + kOffSfa + s * kSfBytes + j * kAtomBytes + lane * 16);
-                    const uint4 c = *reinterpret_cast<const uint4*>(
-                        base + kOffSfb + s * kSfBytes + j * kAtomBytes + lane * 16);
+                    const uint4 a = *reinterpret_cast<const uint4*>(sa_s + j * kAtomBytes);
                     v[4 * j] = a.x; v[4 * j + 1] = a.y; v[4 * j + 2] = a.z; v[4 * j + 3] = a.w;
-                    v[16 + 4 * j] = c.x; v[17 + 4 * j] = c.y; v[18 + 4 * j] = c.z;
-                    v[19 + 4 * j] = c.w;
                 }
-                tc::tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + kTmemSf +
-                                  (uint32_t)s * kSfColsPerStage, v);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 b0 = *reinterpret_cast<const uint4*>(sb_s + j * kAtomBytes);
+                    const uint4 b1 = *reinterpret_cast<const uint4*>(sb_s + (4 + j) * kAtomBytes);
+                    uint32_t* dst = j < 2 ? &v[16 + 8 * j] : &u16[8 * (j - 2)];
+                    dst[0] = b0.x; dst[1] = b0.y; dst[2] = b0.z; dst[3] = b0.w;
+                    dst[4] = b1.x; dst[5] = b1.y; dst[6] = b1.z; dst[7] = b1.w;
+                }
+                const uint32_t col = tmem + ((uint32_t)(q * 32) << 16) + kTmemSf +
+                                     (uint32_t)s * kSfColsPerStage;
+                tc::tmem_st32(col, v);
+                tc::tmem_st16(col + 32, u16);
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) tc::arrive(sfull(s));
@@ -226,14 +247,13 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
         tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
         int tile, kb0, kb1;
         for (; wi.next(tile, kb0, kb1); ++lt) {
-            const int b = lt & 1;
             if (!__all_sync(0xffffffffu,
-                            tc::wait_or_abort(accfull(b), (lt >> 1) & 1, abort_flag, err)))
+                            tc::wait_or_abort(accfull(0), lt & 1, abort_flag, err)))
                 break;
             tc::fence_after();
-            tc::epilogue_work<kBN, kBM>(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m,
-                                        kb0 == 0 && kb1 == nkb, nkb, p_sk, tsk, g, y, y_bf16, M,
-                                        N, slots, counters, accempty(b));
+            tc::epilogue_work<kBN, kBM>(tmem, q, lane, tile, ntiles_m, kb0 == 0 && kb1 == nkb,
+                                        nkb, p_sk, tsk, g, y, y_bf16, M, N, slots, counters,
+                                        accempty(0));
         }
     }
 
@@ -276,7 +296,8 @@ cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float*
     uint32_t* counters = reinterpret_cast<uint32_t*>(sk_state);
     float* slots = reinterpret_cast<float*>(sk_state + tc::counters_bytes(p.ntiles));
     gemm_w4a4_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(
-        mw, mx, wsz, xsz, gw, gx, y, y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, p.ntiles_m,
+        mw, mx, wsz, xsz, gw, gx, y, y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, (M + 127) / 128,
+        p.ntiles_m,
         p.ntiles, p.ntiles_sk, p.p_sk, p.tsk, err, counters, slots);
     return cudaGetLastError();
 }
