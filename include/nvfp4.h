@@ -167,7 +167,14 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *   workspace          >= nvfp4_workspace_bytes(1, M, K, N, mode) bytes (at least the
  *                      256-byte header holding the sticky error word), zero-filled once
  *                      at allocation.  Calls that share a workspace must be ordered (one
- *                      stream), since W4A4 keeps the quantized x there.
+ *                      stream), since W4A4 keeps the quantized x there.  For M > 16 it
+ *                      also holds the tensor-core GEMM's stream-K counters (they must be
+ *                      zero before the first call; every call that completes without a
+ *                      device error leaves them zero) and fp32 partial tiles.  After a
+ *                      device error (nvfp4_workspace_error != 0), zero-fill it again.
+ * Kernels: M = 1 pipelined GEMV; 2 <= M <= 8 streamed skinny GEMM (mma.sync); M <= 16
+ * otherwise the mma.sync skinny GEMM; M > 16 the tcgen05 GEMMs (W4A16: W dequantized to
+ * bf16 per tile; W4A4: block-scaled kind::mxf4nvf4).  Results are deterministic.
  */
 nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K, const uint8_t* w_packed,
                           const uint8_t* w_scales_swizzled, const float* w_global_scale,
