@@ -213,7 +213,7 @@ gemv_m1_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict_
 // is bounded; on time-out the kernel sets NVFP4_DEVERR_TIMEOUT in the error word, stops,
 // and lets the copies it issued land before it exits.
 constexpr int kPipeMaxThreads = 1024;
-constexpr int kPipeStageTarget = 32 * 1024;  // bytes of codes per stage (whole rows)
+constexpr int kPipeStageTarget = 80 * 1024;  // bytes of codes per stage (whole rows)
 
 // exact x * 2^e for a bf16 value (two multiplies keep 2^e representable for any e)
 __device__ __forceinline__ float pow2_scale(float v, float f1, float f2) { return v * f1 * f2; }
