@@ -23,6 +23,7 @@
 // the token's maximum) make every warp add the exact fp32 residual of its slice.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "nvfp4.h"
@@ -35,20 +36,24 @@ namespace {
 
 constexpr int kSkMaxGroups = 23;  // consumer warps, at most (plus the producer: 768 threads)
 constexpr int kSkMaxThreads = (kSkMaxGroups + 1) * 32;
-constexpr int kSkRows = 16;  // rows of W per stage (one mma row group)
+constexpr int kSkRows = 16;           // rows of an mma row group
+constexpr int kSkMaxRgs = 4;          // row groups per stage, at most
+constexpr int kSkStageTarget = 80 * 1024;  // bytes of codes per stage
 
-__host__ __device__ __forceinline__ size_t sk_stage_bytes(int K) {
-    return (((size_t)kSkRows * (K / 2) + (size_t)kSkRows * (K / 16) + 32) + 127) & ~(size_t)127;
+// a stage: rgs row groups of codes, then their row-major scale bytes
+__host__ __device__ __forceinline__ size_t sk_stage_bytes(int K, int rgs) {
+    const size_t rows = (size_t)kSkRows * rgs;
+    return ((rows * (K / 2) + rows * (K / 16) + 32) + 127) & ~(size_t)127;
 }
 
-// slot area of one stage: ngroups partial tiles of 16 rows x 8 tokens (fp32)
-__host__ __device__ __forceinline__ size_t sk_slot_bytes(int ngroups) {
-    return (size_t)ngroups * kSkRows * 8 * 4;
+// slot area of one stage: per row group, ngroups partial tiles of 16 rows x 8 tokens (fp32)
+__host__ __device__ __forceinline__ size_t sk_slot_bytes(int ngroups, int rgs) {
+    return (size_t)rgs * ngroups * kSkRows * 8 * 4;
 }
 
-__host__ __device__ __forceinline__ size_t sk_smem(int K, int ngroups, int stages) {
-    return (size_t)stages * (sk_stage_bytes(K) + sk_slot_bytes(ngroups)) +
-           (size_t)stages * (8 + 8 + 16);  // full, empty barriers; stage counters
+__host__ __device__ __forceinline__ size_t sk_smem(int K, int ngroups, int stages, int rgs) {
+    return (size_t)stages * (sk_stage_bytes(K, rgs) + sk_slot_bytes(ngroups, rgs)) +
+           (size_t)stages * (8 + 8 + 4 * kSkMaxRgs);  // full, empty barriers; row-group counters
 }
 
 template <int U>
@@ -56,14 +61,15 @@ __global__ void __launch_bounds__(kSkMaxThreads, 1)
 skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* __restrict__ wq,
                    const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
                    const float* __restrict__ gx, int N, void* __restrict__ y, int y_bf16,
-                   int stages, uint32_t* __restrict__ err) {
+                   int stages, int rgs, uint32_t* __restrict__ err) {
     constexpr int CG = 4 * U;  // 16-byte chunks (32 elements) of K per consumer warp
     extern __shared__ __align__(128) uint8_t smem[];
     const int rowchunks = K >> 5;
     const int ngroups = (rowchunks + CG - 1) / CG;
     const int nthreads_c = ngroups * 32;
-    const size_t st_bytes = sk_stage_bytes(K);
-    const size_t sl_bytes = sk_slot_bytes(ngroups);
+    const size_t st_bytes = sk_stage_bytes(K, rgs);
+    const size_t sl_bytes = sk_slot_bytes(ngroups, rgs);
+    const int srows = kSkRows * rgs;  // rows of a full stage
     uint8_t* ring = smem;
     float* slots = reinterpret_cast<float*>(smem + (size_t)stages * st_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * (st_bytes + sl_bytes));
@@ -80,14 +86,15 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
     const int nrg_all = (N + kSkRows - 1) / kSkRows;
     const int rg0 = (int)((int64_t)nrg_all * blockIdx.x / gridDim.x);
     const int rg1 = (int)((int64_t)nrg_all * (blockIdx.x + 1) / gridDim.x);
-    const int nst = rg1 - rg0;
+    const int nst = (rg1 - rg0 + rgs - 1) / rgs;
+    const int64_t r_end = min((int64_t)N, (int64_t)rg1 * kSkRows);  // this CTA's rows end
     const int64_t rowb = K >> 1, rows_sb = K >> 4;  // code and scale bytes per row
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], ngroups);
-            cnt[s] = 0;
+            for (int r = 0; r < kSkMaxRgs; ++r) cnt[s * kSkMaxRgs + r] = 0;
         }
         for (int m = 0; m < 8; ++m) amax_bits[m] = 0u;
         abort_flag = 0;
@@ -103,9 +110,9 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
             // stream may still run; every read that lands in shared memory comes after the
             // wait for it
             for (int it = 0; it < min(nst, stages); ++it) {
-                const int64_t rbeg = (int64_t)(rg0 + it) * kSkRows;
+                const int64_t rbeg = (int64_t)rg0 * kSkRows + (int64_t)it * srows;
                 prefetch_l2(wq + rbeg * rowb,
-                            (uint32_t)(min((int64_t)kSkRows, (int64_t)N - rbeg) * rowb));
+                            (uint32_t)(min((int64_t)srows, r_end - rbeg) * rowb));
             }
             pdl_wait_prior_grid();
             int issued = 0;
@@ -118,8 +125,8 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                     break;
                 }
                 if (abort_flag) break;
-                const int64_t rbeg = (int64_t)(rg0 + it) * kSkRows;
-                const int nr = (int)min((int64_t)kSkRows, (int64_t)N - rbeg);
+                const int64_t rbeg = (int64_t)rg0 * kSkRows + (int64_t)it * srows;
+                const int nr = (int)min((int64_t)srows, r_end - rbeg);
                 const uint32_t wbytes = (uint32_t)(nr * rowb);
                 // scale bytes of these rows, copied from a 16-byte boundary
                 const int64_t s_lo = (rbeg * rows_sb) & ~(int64_t)15;
@@ -127,7 +134,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                 mbar_arrive_expect_tx(&full[s], wbytes + (uint32_t)(s_hi - s_lo));
                 uint8_t* st = ring + (size_t)s * st_bytes;
                 bulk_g2s(st, wq + rbeg * rowb, wbytes, &full[s]);
-                bulk_g2s(st + (size_t)kSkRows * rowb, wrm + s_lo, (uint32_t)(s_hi - s_lo),
+                bulk_g2s(st + (size_t)srows * rowb, wrm + s_lo, (uint32_t)(s_hi - s_lo),
                          &full[s]);
                 issued = it + 1;
             }
@@ -208,107 +215,115 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
         }
         if (__any_sync(0xffffffffu, abort_flag != 0)) break;
         const uint8_t* st = ring + (size_t)s * st_bytes;
-        const int64_t rbeg = (int64_t)(rg0 + it) * kSkRows;
-        const int nr = (int)min((int64_t)kSkRows, (int64_t)N - rbeg);
-        const uint8_t* sst = st + (size_t)kSkRows * rowb + ((rbeg * rows_sb) & 15);
-        const bool rga = g < nr, rgb = g + 8 < nr;  // rows past N hold stale bytes
-        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const int64_t sbeg = (int64_t)rg0 * kSkRows + (int64_t)it * srows;
+        const int snr = (int)min((int64_t)srows, r_end - sbeg);  // rows in this stage
+        const uint8_t* sst = st + (size_t)srows * rowb + ((sbeg * rows_sb) & 15);
+        const int nrgi = (snr + kSkRows - 1) / kSkRows;
+        for (int rgi = 0; rgi < nrgi; ++rgi) {
+            const int nr = min(kSkRows, snr - kSkRows * rgi);
+            const uint8_t* sw = st + (size_t)(kSkRows * rgi) * rowb;
+            const uint8_t* ss = sst + (size_t)(kSkRows * rgi) * rows_sb;
+            const bool rga = g < nr, rgb = g + 8 < nr;  // rows past N hold stale bytes
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int c = warp * CG + 4 * u + t;
-            const bool cv = c < rowchunks;
-            const uint4 wa = (cv && rga) ? *reinterpret_cast<const uint4*>(st + (size_t)g * rowb + 16 * c)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-            const uint4 wb = (cv && rgb) ? *reinterpret_cast<const uint4*>(st + (size_t)(g + 8) * rowb + 16 * c)
-                                         : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t sa = (cv && rga) ? *reinterpret_cast<const uint16_t*>(sst + (size_t)g * rows_sb + 2 * c) : 0u;
-            const uint32_t sb = (cv && rgb) ? *reinterpret_cast<const uint16_t*>(sst + (size_t)(g + 8) * rows_sb + 2 * c) : 0u;
-            // block scales of the chunk (blocks 2c, 2c+1) as f16, each in both halves
-            const uint32_t ha = cvt_e4m3x2_f16x2(sa), hb = cvt_e4m3x2_f16x2(sb);
-            const uint32_t sa0 = __byte_perm(ha, 0, 0x1010), sa1 = __byte_perm(ha, 0, 0x3232);
-            const uint32_t sb0 = __byte_perm(hb, 0, 0x1010), sb1 = __byte_perm(hb, 0, 0x3232);
-            const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
-            const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
+            for (int u = 0; u < U; ++u) {
+                const int c = warp * CG + 4 * u + t;
+                const bool cv = c < rowchunks;
+                const uint4 wa = (cv && rga) ? *reinterpret_cast<const uint4*>(sw + (size_t)g * rowb + 16 * c)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 wb = (cv && rgb) ? *reinterpret_cast<const uint4*>(sw + (size_t)(g + 8) * rowb + 16 * c)
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t sa = (cv && rga) ? *reinterpret_cast<const uint16_t*>(ss + (size_t)g * rows_sb + 2 * c) : 0u;
+                const uint32_t sb = (cv && rgb) ? *reinterpret_cast<const uint16_t*>(ss + (size_t)(g + 8) * rows_sb + 2 * c) : 0u;
+                // block scales of the chunk (blocks 2c, 2c+1) as f16, each in both halves
+                const uint32_t ha = cvt_e4m3x2_f16x2(sa), hb = cvt_e4m3x2_f16x2(sb);
+                const uint32_t sa0 = __byte_perm(ha, 0, 0x1010), sa1 = __byte_perm(ha, 0, 0x3232);
+                const uint32_t sb0 = __byte_perm(hb, 0, 0x1010), sb1 = __byte_perm(hb, 0, 0x3232);
+                const uint32_t wa4[4] = {wa.x, wa.y, wa.z, wa.w};
+                const uint32_t wb4[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                // word q of each chunk: bytes 4q .. 4q+3 = elements 8q .. 8q+7 (block q / 2),
-                // the A registers of MMAs 2q and 2q+1
-                uint32_t ha[4], hb[4];
-                cvt8(wa4[q], ha);
-                cvt8(wb4[q], hb);
-                const uint32_t sca = q < 2 ? sa0 : sa1, scb = q < 2 ? sb0 : sb1;
+                for (int q = 0; q < 4; ++q) {
+                    // word q of each chunk: bytes 4q .. 4q+3 = elements 8q .. 8q+7 (block q / 2),
+                    // the A registers of MMAs 2q and 2q+1
+                    uint32_t ha[4], hb[4];
+                    cvt8(wa4[q], ha);
+                    cvt8(wb4[q], hb);
+                    const uint32_t sca = q < 2 ? sa0 : sa1, scb = q < 2 ? sb0 : sb1;
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int j = 2 * q + jj;
-                    const uint32_t a0 = hmul2(ha[2 * jj], sca), a2 = hmul2(ha[2 * jj + 1], sca);
-                    const uint32_t a1 = hmul2(hb[2 * jj], scb), a3 = hmul2(hb[2 * jj + 1], scb);
-                    asm volatile(
-                        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-                        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(bf[u][j][0]), "r"(bf[u][j][1]));
-                }
-            }
-        }
-        // this warp's partial tile: slot[row][token], row g / g + 8, tokens 2t, 2t+1
-        float* mine = slots + ((size_t)s * ngroups + warp) * (kSkRows * 8);
-        mine[g * 8 + 2 * t] = d[0];
-        mine[g * 8 + 2 * t + 1] = d[1];
-        mine[(g + 8) * 8 + 2 * t] = d[2];
-        mine[(g + 8) * 8 + 2 * t + 1] = d[3];
-        if (any_inexact) {
-            // exact residual x' - fp16(x') of this warp's K slice (slow path, rare): lane l
-            // takes row l % 16 and tokens l / 16, l / 16 + 2, ...
-            __syncwarp();
-            const int r = lane & 15;
-            if (r < nr) {
-                for (int m = lane >> 4; m < M; m += 2) {
-                    float q = 0.0f;
-                    for (int c = warp * CG; c < min(rowchunks, (warp + 1) * CG); ++c) {
-                        const uint32_t s2 = *reinterpret_cast<const uint16_t*>(sst + (size_t)r * rows_sb + 2 * c);
-                        for (int k = 0; k < 32; ++k) {
-                            const uint32_t byte = st[(size_t)r * rowb + 16 * c + (k >> 1)];
-                            const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);
-                            const float sc = e4m3_to_f32(k < 16 ? (s2 & 0xFFu) : (s2 >> 8));
-                            q = fmaf(residual(x[(int64_t)m * K + 32 * c + k], e_sh[m]),
-                                     e2m1_to_f32(code) * sc, q);
-                        }
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * q + jj;
+                        const uint32_t a0 = hmul2(ha[2 * jj], sca), a2 = hmul2(ha[2 * jj + 1], sca);
+                        const uint32_t a1 = hmul2(hb[2 * jj], scb), a3 = hmul2(hb[2 * jj + 1], scb);
+                        asm volatile(
+                            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+                            "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(bf[u][j][0]), "r"(bf[u][j][1]));
                     }
-                    mine[r * 8 + m] += q;
+                }
+            }
+            // this warp's partial tile of the row group: slot[row][token], row g / g + 8,
+            // tokens 2t, 2t+1
+            float* tiles = slots + ((size_t)s * rgs + rgi) * ngroups * (kSkRows * 8);
+            float* mine = tiles + (size_t)warp * (kSkRows * 8);
+            mine[g * 8 + 2 * t] = d[0];
+            mine[g * 8 + 2 * t + 1] = d[1];
+            mine[(g + 8) * 8 + 2 * t] = d[2];
+            mine[(g + 8) * 8 + 2 * t + 1] = d[3];
+            if (any_inexact) {
+                // exact residual x' - fp16(x') of this warp's K slice (slow path, rare): lane l
+                // takes row l % 16 and tokens l / 16, l / 16 + 2, ...
+                __syncwarp();
+                const int r = lane & 15;
+                if (r < nr) {
+                    for (int m = lane >> 4; m < M; m += 2) {
+                        float q = 0.0f;
+                        for (int c = warp * CG; c < min(rowchunks, (warp + 1) * CG); ++c) {
+                            const uint32_t s2 = *reinterpret_cast<const uint16_t*>(ss + (size_t)r * rows_sb + 2 * c);
+                            for (int k = 0; k < 32; ++k) {
+                                const uint32_t byte = sw[(size_t)r * rowb + 16 * c + (k >> 1)];
+                                const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);
+                                const float sc = e4m3_to_f32(k < 16 ? (s2 & 0xFFu) : (s2 >> 8));
+                                q = fmaf(residual(x[(int64_t)m * K + 32 * c + k], e_sh[m]),
+                                         e2m1_to_f32(code) * sc, q);
+                            }
+                        }
+                        mine[r * 8 + m] += q;
+                    }
+                }
+            }
+            // count this warp in; the arrival that completes the row group adds its partial
+            // tiles in warp order (every slot's loads in flight together) and writes its 16
+            // rows of y
+            __threadfence_block();
+            __syncwarp();
+            int* c_rg = &cnt[s * kSkMaxRgs + rgi];
+            int old = 0;
+            if (lane == 0) old = atomicAdd(c_rg, 1);
+            if (__shfl_sync(0xffffffffu, old, 0) == ngroups - 1) {
+                __threadfence_block();
+                float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                const float* base = tiles + lane;
+#pragma unroll
+                for (int w = 0; w < kSkMaxGroups; ++w)
+                    if (w < ngroups) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) v[i] += base[(size_t)w * (kSkRows * 8) + 32 * i];
+                    }
+                __syncwarp();
+                if (lane == 0) *c_rg = 0;
+                const int64_t rbeg = sbeg + kSkRows * rgi;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = lane + 32 * i, r = e >> 3, m = e & 7;
+                    if (r < nr && m < M)
+                        store_y(y, (int64_t)m * N + rbeg + r, v[i] * pw_sh[m] * gscale, y_bf16);
                 }
             }
         }
-        // count this warp in; the arrival that completes the stage adds the partial tiles
-        // in warp order (every slot's loads in flight together), releases the stage, then
-        // writes the 16 rows of y
-        __threadfence_block();
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) old = atomicAdd(&cnt[s], 1);
-        const bool last = __shfl_sync(0xffffffffu, old, 0) == ngroups - 1;
-        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (last) {
-            __threadfence_block();
-            const float* base = slots + (size_t)s * ngroups * (kSkRows * 8) + lane;
-#pragma unroll
-            for (int w = 0; w < kSkMaxGroups; ++w)
-                if (w < ngroups) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) v[i] += base[(size_t)w * (kSkRows * 8) + 32 * i];
-                }
-            __syncwarp();
-            if (lane == 0) cnt[s] = 0;
-        }
+        // the stage (codes and partial tiles) is free once every warp has passed here
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (last) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int e = lane + 32 * i, r = e >> 3, m = e & 7;
-                if (r < nr && m < M)
-                    store_y(y, (int64_t)m * N + rbeg + r, v[i] * pw_sh[m] * gscale, y_bf16);
-            }
-        }
     }
 }
 
@@ -327,10 +342,22 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
     int grid = dev.sm_count;
     const int nrg = (N + kSkRows - 1) / kSkRows;
     if (grid > nrg) grid = nrg;
-    // the deepest ring (2..6 stages) that fits one CTA per SM
+    // row groups per stage: about kSkStageTarget bytes of codes, but no fewer than four
+    // stages per CTA where the CTA's rows allow, so that short slices still pipeline
+    const size_t rg_bytes = (size_t)kSkRows * (K / 2);
+    int rgs = (int)std::max<size_t>(1, kSkStageTarget / rg_bytes);
+    rgs = std::min(rgs, std::max(1, (nrg / grid) / 4));
+    rgs = std::min(rgs, kSkMaxRgs);
+    // the deepest ring (2..6 stages) that fits one CTA per SM; fewer row groups per
+    // stage where two stages of rgs do not fit
     int stages = 6;
-    while (stages > 2 && sk_smem(K, ngroups, stages) + 2048 > dev.smem_optin) --stages;
-    const size_t smem = sk_smem(K, ngroups, stages);
+    for (;;) {
+        stages = 6;
+        while (stages > 2 && sk_smem(K, ngroups, stages, rgs) + 2048 > dev.smem_optin) --stages;
+        if (sk_smem(K, ngroups, stages, rgs) + 2048 <= dev.smem_optin || rgs == 1) break;
+        --rgs;
+    }
+    const size_t smem = sk_smem(K, ngroups, stages, rgs);
     if (smem + 2048 > dev.smem_optin) return cudaSuccess;
     static std::atomic<uint64_t> configured{0};
     const uint64_t bit = 1ull << (dev.device & 63);
@@ -354,7 +381,7 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_pipe_kernel<U>, x, M, K, wq, wrm, gw, gx, N,
-                                       y, y_bf16 ? 1 : 0, stages, err);
+                                       y, y_bf16 ? 1 : 0, stages, rgs, err);
     *launched = true;
     return e != cudaSuccess ? e : cudaGetLastError();
 }

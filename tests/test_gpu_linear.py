@@ -157,3 +157,20 @@ def test_multiple_k_chunks(M, K, N):
     y, _ = run_linear(x, wq, ws, gw, K, torch.float32)
     y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
     check_tolerance(y_to_f64(y), y_ref, ab, "chunks M%d K%d" % (M, K))
+
+
+@pytest.mark.parametrize("M,K,N,wide", [(5, 256, 39001, False), (7, 512, 31623, False),
+                                        (2, 1024, 24000, False), (7, 256, 39001, True)])
+def test_skinny_stages_of_several_row_groups(M, K, N, wide):
+    # enough rows per CTA that a pipeline stage of the 2..8-token kernel holds two to four
+    # 16-row groups, the last one ragged; the wide-range case takes the exact residual path
+    x, w = make_inputs(M, K, N, seed=500 + M + K)
+    if wide:
+        xf = x.float()
+        xf[:, ::5] *= 1e-12
+        xf[:, 3] = 2.0e4
+        x = xf.to(torch.bfloat16)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, _ = run_linear(x, wq, ws, gw, K, torch.bfloat16)
+    y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+    check_tolerance(y_to_f64(y), y_ref, ab, "row groups M%d K%d N%d" % (M, K, N))
