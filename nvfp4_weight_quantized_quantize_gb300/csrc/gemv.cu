@@ -214,9 +214,6 @@ gemv_m1_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict_
 // and lets the copies it issued land before it exits.
 constexpr int kPipeMaxThreads = 1024;
 constexpr int kPipeStageTarget = 80 * 1024;  // bytes of codes per stage (whole rows)
-// codes a CTA sends to L2 before it waits for the previous kernel on the stream, at least
-// one ring's worth
-constexpr int64_t kPrefetchBytes = 160 * 1024;
 
 // exact x * 2^e for a bf16 value (two multiplies keep 2^e representable for any e)
 __device__ __forceinline__ float pow2_scale(float v, float f1, float f2) { return v * f1 * f2; }
@@ -278,8 +275,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
             // the first ring's worth of codes heads for L2 while the previous kernel on the
             // stream may still run (a prefetch cannot observe stale data: L2 is the point of
             // coherence); every read that lands in shared memory comes after the wait
-            for (int it = 0; it < nst && (it < stages || (int64_t)it * rps * rowb < kPrefetchBytes);
-                 ++it)
+            for (int it = 0; it < min(nst, stages); ++it)
                 prefetch_l2(wq + (r0 + (int64_t)it * rps) * rowb,
                             (uint32_t)(min(rps, nrows - it * rps) * rowb));
             pdl_wait_prior_grid();
@@ -838,19 +834,9 @@ cudaError_t launch_m1(const uint16_t* x, int K, const uint8_t* wq, const uint8_t
 
 cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz_all, const float* gw, const float* gx, int N,
-                              void* y, bool y_bf16, uint32_t* err, uint8_t* tc_state,
-                              cudaStream_t stream, const DevInfo& dev) {
-    // The tensor-core GEMV is parity-clean but not yet faster than the CUDA-core kernel on
-    // the decode shapes (its x-plane prologue and stream-K fixup cost more than the
-    // dequantization they replace), so M = 1 stays on the CUDA cores for now.
-    constexpr bool kTensorCoreM1 = false;
-    if (kTensorCoreM1 && M == 1 && tc_state) {
-        bool launched = false;
-        const cudaError_t e = launch_gemv_tc(x, K, wq, wsz_all, gw, gx, N, y, y_bf16, tc_state,
-                                             false, stream, dev, &launched);
-        if (e != cudaSuccess || launched) return e;
-    }
-    // the CUDA-core kernels read the row-major part of the repacked scales
+                              void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
+                              const DevInfo& dev) {
+    // the small-M kernels read the row-major part of the repacked scales
     const int64_t atom = (int64_t)((N + 127) / 128 * 128) * ((K / 16 + 3) / 4 * 4);
     const uint8_t* wsz = wsz_all + atom;
     if (M == 1) return launch_m1(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, stream, dev);

@@ -37,21 +37,10 @@ cudaError_t launch_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out
 
 // Small-M (M <= 16) W4A16 GEMV / skinny GEMM.  y = (gx ? *gx : 1) * *gw * x . W^T.
 // err: the workspace's sticky error word (bounded waits OR bits into it).
-// tc_state: a workspace of at least gemv_tc_workspace_bytes(K, N) bytes (error word first,
-// stream-K counters zeroed) lets M = 1 run on the tensor cores; nullptr keeps every M on
-// the CUDA-core kernels.
 cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz, const float* gw, const float* gx, int N,
-                              void* y, bool y_bf16, uint32_t* err, uint8_t* tc_state,
-                              cudaStream_t stream, const DevInfo& dev);
-
-// M = 1 on the block-scaled tensor cores (x as 16 exact E2M1 digit planes); *launched stays
-// false when the shape does not fit the kernel (the caller then takes the CUDA-core GEMV).
-size_t gemv_tc_workspace_bytes(int64_t K, int64_t N);
-cudaError_t launch_gemv_tc(const uint16_t* x, int K, const uint8_t* wq, const uint8_t* wsz_all,
-                           const float* gw, const float* gx, int N, void* y, bool y_bf16,
-                           uint8_t* workspace, bool w_static, cudaStream_t stream,
-                           const DevInfo& dev, bool* launched);
+                              void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
+                              const DevInfo& dev);
 
 constexpr int kGemvMaxM = 16;
 

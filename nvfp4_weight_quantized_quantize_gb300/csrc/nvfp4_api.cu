@@ -139,8 +139,7 @@ NVFP4_API size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
     }
     if (op != 1 || M < 1 || K < 32 || K % 32 != 0 || N < 1) return (size_t)-1;
     if (mode == NVFP4_W4A16)
-        return M == 1 ? gemv_tc_workspace_bytes(K, N)
-                      : M <= kGemvMaxM ? kHeaderBytes : gemm_w4a16_workspace_bytes(M, K, N);
+        return M <= kGemvMaxM ? kHeaderBytes : gemm_w4a16_workspace_bytes(M, K, N);
     if (mode == NVFP4_W4A4) return w4a4_layout(M, K, N).total;
     return (size_t)-1;
 }
@@ -234,8 +233,7 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
         if (M <= kGemvMaxM)
             return from_cuda(launch_gemv_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
                                                w_global_scale, nullptr, (int)N, y, ybf,
-                                               static_cast<uint32_t*>(workspace),
-                                               static_cast<uint8_t*>(workspace), stream, d));
+                                               static_cast<uint32_t*>(workspace), stream, d));
         return from_cuda(launch_gemm_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
                                            w_global_scale, (int)N, y, ybf,
                                            static_cast<uint8_t*>(workspace), stream, d));
@@ -252,7 +250,7 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
     if (M <= kGemvMaxM)
         return from_cuda(launch_gemv_w4a16(deq, (int)M, (int)K, w_packed, w_scales_swizzled,
                                            w_global_scale, gx, (int)N, y, ybf,
-                                           reinterpret_cast<uint32_t*>(ws), nullptr, stream, d));
+                                           reinterpret_cast<uint32_t*>(ws), stream, d));
     return from_cuda(launch_gemm_w4a4(ws + L.xq, ws + L.xs, gx, (int)M, (int)K, w_packed,
                                       w_scales_swizzled, w_global_scale, (int)N, y, ybf,
                                       reinterpret_cast<uint32_t*>(ws), ws + L.sk, stream, d));
