@@ -37,6 +37,10 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "gemv_w4a16_decode_traffic.txt"
 FP4_NOMINAL_TFLOPS = 13500.0  # dense FP4 tensor peak of a GB300 (nominal, not measured)
 
 
+
+# set from --static-weights: the decode/verify calls pass NVFP4_STATIC_WEIGHTS
+STATIC_W = False
+
 def algo_bytes(M, K, N, y_bytes=2):
     return N * K // 2 + N * K // 16 + M * K * 2 + M * N * y_bytes + 4
 
@@ -178,7 +182,7 @@ def run_ours(args, rank, world, dist):
             if events is not None:
                 events[2 * j].record()
             nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c],
-                            workspace=s["ws"])
+                            workspace=s["ws"], static_weights=STATIC_W)
             if events is not None:
                 events[2 * j + 1].record()
 
@@ -256,6 +260,7 @@ def run_ours(args, rank, world, dist):
                                    "(K=17408,N=5120), y bf16",
                        "operands": "e2m1 weights + e4m3 per-16 scales + fp32 global, bf16 x, "
                                    "fp32 accumulate",
+                       "static_weights": STATIC_W,
                        "bytes_per_step": setup.bytes_per_step,
                        "l2": "inputs larger than L2: %d rotating weight copies (%.0f MB)"
                              % (setup.copies, setup.bytes_per_step * setup.copies / 1e6),
@@ -292,7 +297,7 @@ def run_e2e(torch, nv, setup, args):
         for j, s in enumerate(S):
             s["x"].copy_(xh[j], non_blocking=True)
             nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c],
-                            workspace=s["ws"])
+                            workspace=s["ws"], static_weights=STATIC_W)
             yh[j].copy_(s["ys"][c], non_blocking=True)
 
     n = min(args.steps, 2048)
@@ -356,7 +361,8 @@ def measure_rows(torch, nv, setup):
     for sh in setup.shapes:
         ms = time_graph(torch, lambda i, sh=sh: nv.nvfp4_linear(
             sh["x"], sh["copies"][i % setup.copies][0], sh["copies"][i % setup.copies][1],
-            sh["g"], sh["ys"][i % setup.copies], workspace=sh["ws"]), 4 * setup.copies, 50)
+            sh["g"], sh["ys"][i % setup.copies], workspace=sh["ws"], static_weights=STATIC_W),
+            4 * setup.copies, 50)
         b = algo_bytes(1, sh["K"], sh["N"])
         rows["a3_decode_%s_K%d_N%d" % (sh["name"], sh["K"], sh["N"])] = {
             "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
@@ -373,7 +379,8 @@ def measure_rows(torch, nv, setup):
         wsv = torch.zeros(nv.nvfp4_workspace_bytes(1, wl.M, wl.K, wl.N), dtype=torch.uint8,
                           device="cuda")
         ms = time_graph(torch, lambda i: nv.nvfp4_linear(xd, cps[i % ncp][0], cps[i % ncp][1],
-                                                         gg, y, workspace=wsv), 2 * ncp, 20)
+                                                         gg, y, workspace=wsv,
+                                                         static_weights=STATIC_W), 2 * ncp, 20)
         b = algo_bytes(wl.M, wl.K, wl.N)
         rows["a4_verify_%s_M7_K%d_N%d" % (name, wl.K, wl.N)] = {
             "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
@@ -549,12 +556,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=256)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--copies", type=int, default=4)
+    ap.add_argument("--static-weights", type=int, default=1,
+                    help="1 (default): the decode and verify calls declare their weights "
+                         "static (NVFP4_STATIC_WEIGHTS: nothing in flight writes them), so "
+                         "each launch streams them before the previous launch has ended")
     ap.add_argument("--rows", type=int, default=1, help="also measure the other rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only-workload", default=None,
                     help="run a few calls of one workload and exit (for ncu captures)")
     args = ap.parse_args()
+    global STATIC_W
+    STATIC_W = bool(args.static_weights)
     if args.only_workload:
         run_one_workload(args.only_workload)
         return

@@ -60,7 +60,15 @@ typedef enum {
 } nvfp4_status;
 
 typedef enum { NVFP4_F32 = 0, NVFP4_BF16 = 1 } nvfp4_dtype;
-typedef enum { NVFP4_W4A16 = 0, NVFP4_W4A4 = 1 } nvfp4_mode;
+typedef enum {
+    NVFP4_W4A16 = 0,
+    NVFP4_W4A4 = 1,
+    /* Flag, OR-ed into the mode of nvfp4_linear: the caller promises that no kernel
+     * enqueued earlier on the stream, and possibly still running, writes w_packed or
+     * w_scales_swizzled (true of inference weights).  The decode kernels then start
+     * streaming the weights before the previous kernel on the stream has finished. */
+    NVFP4_STATIC_WEIGHTS = 0x10
+} nvfp4_mode;
 
 /* error-word bits (see nvfp4_workspace_error) */
 #define NVFP4_DEVERR_TIMEOUT 0x1u
@@ -161,7 +169,8 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *   w_scales_swizzled  nvfp4_repack_bytes(N, K) bytes (nvfp4_repack output).
  *   w_global_scale     one float (device).
  *   y                  out [M, N], dtype y_dtype (NVFP4_F32 or NVFP4_BF16).
- *   mode               NVFP4_W4A16 or NVFP4_W4A4.
+ *   mode               NVFP4_W4A16 or NVFP4_W4A4, optionally | NVFP4_STATIC_WEIGHTS
+ *                      (used by the M <= 8 kernels; the others ignore it).
  *   x_global_scale     W4A4 only: NULL = dynamic (amax of x), else one float
  *                      (device, finite, > 0).  Must be NULL for W4A16.
  *   workspace          >= nvfp4_workspace_bytes(1, M, K, N, mode) bytes (at least the

@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libnvfp4.so")
 
 NVFP4_F32, NVFP4_BF16 = 0, 1
 NVFP4_W4A16, NVFP4_W4A4 = 0, 1
+NVFP4_STATIC_WEIGHTS = 0x10  # flag OR-ed into the mode (see nvfp4_linear)
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ERR_ALIGN",
           4: "NVFP4_ERR_DTYPE", 5: "NVFP4_ERR_WORKSPACE", 6: "NVFP4_ERR_DEVICE",
           7: "NVFP4_ERR_CUDA", 8: "NVFP4_ERR_TIMEOUT", 9: "NVFP4_ERR_UNSUPPORTED"}
@@ -160,10 +161,15 @@ def nvfp4_repack(scales: torch.Tensor, cols: int, out: torch.Tensor, stream=None
 def nvfp4_linear(x: torch.Tensor, w_packed: torch.Tensor, w_scales_swizzled: torch.Tensor,
                  w_global_scale: torch.Tensor, y: torch.Tensor, mode: str = "w4a16",
                  x_global_scale: torch.Tensor | None = None,
-                 workspace: torch.Tensor | None = None, stream=None) -> None:
+                 workspace: torch.Tensor | None = None, stream=None,
+                 static_weights: bool = False) -> None:
+    """static_weights: no kernel still in flight on the stream writes the weights
+    (NVFP4_STATIC_WEIGHTS), so the decode kernels may stream them early."""
     M, K = x.shape
     N = w_packed.shape[0]
     m = {"w4a16": NVFP4_W4A16, "w4a4": NVFP4_W4A4}[mode]
+    if static_weights:
+        m |= NVFP4_STATIC_WEIGHTS
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().nvfp4_linear(_p(x), M, K, _p(w_packed), _p(w_scales_swizzled),
                              _p(w_global_scale), N, _p(y), _dtype_code(y.dtype), m,

@@ -233,7 +233,8 @@ __global__ void __launch_bounds__(kPipeMaxThreads, 1)
 gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict__ wq,
                     const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
                     const float* __restrict__ gx, int N, void* __restrict__ y, int y_bf16,
-                    int rows_max, int rps, int stages, uint32_t* __restrict__ err) {
+                    int rows_max, int rps, int stages, int w_static,
+                    uint32_t* __restrict__ err) {
     constexpr int L = 32 / G;              // rows per step
     extern __shared__ __align__(128) uint8_t smem[];
     const int rowchunks = K >> 5;          // 16-byte chunks per row
@@ -272,13 +273,16 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     if (warp == ngroups) {
         // ---- producer ----
         if (lane == 0) {
-            // the first ring's worth of codes heads for L2 while the previous kernel on the
+            // Unless the weights are static (no kernel still in flight writes them), the
+            // first ring's worth of codes only heads for L2 while the previous kernel on the
             // stream may still run (a prefetch cannot observe stale data: L2 is the point of
-            // coherence); every read that lands in shared memory comes after the wait
-            for (int it = 0; it < min(nst, stages); ++it)
-                prefetch_l2(wq + (r0 + (int64_t)it * rps) * rowb,
-                            (uint32_t)(min(rps, nrows - it * rps) * rowb));
-            pdl_wait_prior_grid();
+            // coherence), and every read that lands in shared memory comes after the wait.
+            if (!w_static) {
+                for (int it = 0; it < min(nst, stages); ++it)
+                    prefetch_l2(wq + (r0 + (int64_t)it * rps) * rowb,
+                                (uint32_t)(min(rps, nrows - it * rps) * rowb));
+                pdl_wait_prior_grid();
+            }
             int issued = 0;
             for (int it = 0; it < nst; ++it) {
                 const int s = it % stages;
@@ -761,7 +765,8 @@ size_t pipe_smem(int K, int rows_max, int rps, int stages, int ngroups) {
 template <int G>
 cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8_t* wrm,
                         const float* gw, const float* gx, int N, void* y, bool y_bf16,
-                        uint32_t* err, cudaStream_t stream, const DevInfo& dev, bool* launched) {
+                        uint32_t* err, bool w_static, cudaStream_t stream, const DevInfo& dev,
+                        bool* launched) {
     *launched = false;
     const int rowchunks = K / 32;
     const int ngroups = (rowchunks + G - 1) / G;
@@ -796,25 +801,28 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G>, x, K, wq, wrm, gw, gx, N,
-                           y, y_bf16 ? 1 : 0, rows_max, rps, stages, err);
+                           y, y_bf16 ? 1 : 0, rows_max, rps, stages, w_static ? 1 : 0, err);
     *launched = true;
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_m1(const uint16_t* x, int K, const uint8_t* wq, const uint8_t* wsz,
                       const float* gw, const float* gx, int N, void* y, bool y_bf16,
-                      uint32_t* err, cudaStream_t stream, const DevInfo& dev) {
+                      uint32_t* err, bool w_static, cudaStream_t stream, const DevInfo& dev) {
     // x-stationary pipelined kernel: column groups of G chunks, one consumer warp each,
     // at most 31 of them (plus the producer warp); G is the smallest of 8, 16, 32 that fits
     const int rowchunks = K / 32;
     bool launched = false;
     cudaError_t e = cudaSuccess;
     if (rowchunks >= 8 * 8 && (rowchunks + 7) / 8 <= 31)
-        e = launch_pipe<8>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, stream, dev, &launched);
+        e = launch_pipe<8>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
+                           &launched);
     else if (rowchunks >= 8 * 16 && (rowchunks + 15) / 16 <= 31)
-        e = launch_pipe<16>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, stream, dev, &launched);
+        e = launch_pipe<16>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
+                            &launched);
     else if (rowchunks >= 8 * 32 && (rowchunks + 31) / 32 <= 31)
-        e = launch_pipe<32>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, stream, dev, &launched);
+        e = launch_pipe<32>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
+                            &launched);
     if (e != cudaSuccess || launched) return e;
     static std::atomic<uint64_t> configured{0};
     e = opt_in_smem(gemv_m1_kernel, dev, configured);
@@ -834,16 +842,16 @@ cudaError_t launch_m1(const uint16_t* x, int K, const uint8_t* wq, const uint8_t
 
 cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz_all, const float* gw, const float* gx, int N,
-                              void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
-                              const DevInfo& dev) {
+                              void* y, bool y_bf16, uint32_t* err, bool w_static,
+                              cudaStream_t stream, const DevInfo& dev) {
     // the small-M kernels read the row-major part of the repacked scales
     const int64_t atom = (int64_t)((N + 127) / 128 * 128) * ((K / 16 + 3) / 4 * 4);
     const uint8_t* wsz = wsz_all + atom;
-    if (M == 1) return launch_m1(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, stream, dev);
+    if (M == 1) return launch_m1(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev);
     if (M <= 8) {
         bool launched = false;
         const cudaError_t e = launch_skinny_w4a16(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, err,
-                                                  stream, dev, &launched);
+                                                  w_static, stream, dev, &launched);
         if (e != cudaSuccess || launched) return e;
         return launch_mma<1>(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, stream, dev);
     }

@@ -37,10 +37,12 @@ cudaError_t launch_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out
 
 // Small-M (M <= 16) W4A16 GEMV / skinny GEMM.  y = (gx ? *gx : 1) * *gw * x . W^T.
 // err: the workspace's sticky error word (bounded waits OR bits into it).
+// w_static: no kernel still in flight before this one writes the weights, so the M = 1
+// and skinny kernels may stream them before waiting for the previous kernel on the stream
 cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz, const float* gw, const float* gx, int N,
-                              void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
-                              const DevInfo& dev);
+                              void* y, bool y_bf16, uint32_t* err, bool w_static,
+                              cudaStream_t stream, const DevInfo& dev);
 
 constexpr int kGemvMaxM = 16;
 
@@ -49,8 +51,8 @@ constexpr int kGemvMaxM = 16;
 // when it took the call (K small enough for its ring); otherwise the caller falls back.
 cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                                 const uint8_t* wrm, const float* gw, const float* gx, int N,
-                                void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
-                                const DevInfo& dev, bool* launched);
+                                void* y, bool y_bf16, uint32_t* err, bool w_static,
+                                cudaStream_t stream, const DevInfo& dev, bool* launched);
 
 // M > 16 W4A16 GEMM on the tensor cores (tcgen05, TMA).  wsz: the atom part of the
 // repacked scales (offset 0 of the repacked buffer).  y = *gw * x . W^T.

@@ -133,6 +133,7 @@ NVFP4_API size_t nvfp4_repack_bytes(int64_t rows, int64_t cols) {
 
 NVFP4_API size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
                                        nvfp4_mode mode) {
+    mode = (nvfp4_mode)(mode & ~NVFP4_STATIC_WEIGHTS);
     if (op == 0) {
         if (M < 1 || K < 16 || K % 16 != 0) return (size_t)-1;
         return kHeaderBytes + (size_t)kMaxPartials * 4;
@@ -212,6 +213,8 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
                                     const float* x_global_scale, void* workspace,
                                     size_t workspace_bytes, nvfp4_stream_t stream) {
     if (!x || !w_packed || !w_scales_swizzled || !w_global_scale || !y) return NVFP4_ERR_NULL;
+    const bool w_static = (mode & NVFP4_STATIC_WEIGHTS) != 0;
+    mode = (nvfp4_mode)(mode & ~NVFP4_STATIC_WEIGHTS);
     if (y_dtype != NVFP4_F32 && y_dtype != NVFP4_BF16) return NVFP4_ERR_DTYPE;
     if (mode != NVFP4_W4A16 && mode != NVFP4_W4A4) return NVFP4_ERR_DTYPE;
     if (mode == NVFP4_W4A16 && x_global_scale) return NVFP4_ERR_DTYPE;
@@ -233,7 +236,8 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
         if (M <= kGemvMaxM)
             return from_cuda(launch_gemv_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
                                                w_global_scale, nullptr, (int)N, y, ybf,
-                                               static_cast<uint32_t*>(workspace), stream, d));
+                                               static_cast<uint32_t*>(workspace), w_static,
+                                               stream, d));
         return from_cuda(launch_gemm_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
                                            w_global_scale, (int)N, y, ybf,
                                            static_cast<uint8_t*>(workspace), stream, d));
@@ -250,7 +254,8 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
     if (M <= kGemvMaxM)
         return from_cuda(launch_gemv_w4a16(deq, (int)M, (int)K, w_packed, w_scales_swizzled,
                                            w_global_scale, gx, (int)N, y, ybf,
-                                           reinterpret_cast<uint32_t*>(ws), stream, d));
+                                           reinterpret_cast<uint32_t*>(ws), w_static, stream,
+                                           d));
     return from_cuda(launch_gemm_w4a4(ws + L.xq, ws + L.xs, gx, (int)M, (int)K, w_packed,
                                       w_scales_swizzled, w_global_scale, (int)N, y, ybf,
                                       reinterpret_cast<uint32_t*>(ws), ws + L.sk, stream, d));

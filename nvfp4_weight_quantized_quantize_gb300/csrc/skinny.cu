@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kSkMaxThreads, 1)
 skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* __restrict__ wq,
                    const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
                    const float* __restrict__ gx, int N, void* __restrict__ y, int y_bf16,
-                   int stages, int rgs, uint32_t* __restrict__ err) {
+                   int stages, int rgs, int w_static, uint32_t* __restrict__ err) {
     constexpr int CG = 4 * U;  // 16-byte chunks (32 elements) of K per consumer warp
     extern __shared__ __align__(128) uint8_t smem[];
     const int rowchunks = K >> 5;
@@ -109,12 +109,14 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
             // the first ring's worth of codes heads for L2 while the previous kernel on the
             // stream may still run; every read that lands in shared memory comes after the
             // wait for it
-            for (int it = 0; it < min(nst, stages); ++it) {
-                const int64_t rbeg = (int64_t)rg0 * kSkRows + (int64_t)it * srows;
-                prefetch_l2(wq + rbeg * rowb,
-                            (uint32_t)(min((int64_t)srows, r_end - rbeg) * rowb));
+            if (!w_static) {  // static weights stream before the wait
+                for (int it = 0; it < min(nst, stages); ++it) {
+                    const int64_t rbeg = (int64_t)rg0 * kSkRows + (int64_t)it * srows;
+                    prefetch_l2(wq + rbeg * rowb,
+                                (uint32_t)(min((int64_t)srows, r_end - rbeg) * rowb));
+                }
+                pdl_wait_prior_grid();
             }
-            pdl_wait_prior_grid();
             int issued = 0;
             for (int it = 0; it < nst; ++it) {
                 const int s = it % stages;
@@ -334,8 +336,8 @@ namespace {
 template <int U>
 cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
                             const uint8_t* wrm, const float* gw, const float* gx, int N, void* y,
-                            bool y_bf16, uint32_t* err, cudaStream_t stream, const DevInfo& dev,
-                            bool* launched) {
+                            bool y_bf16, uint32_t* err, bool w_static, cudaStream_t stream,
+                            const DevInfo& dev, bool* launched) {
     *launched = false;
     const int rowchunks = K / 32;
     const int ngroups = (rowchunks + 4 * U - 1) / (4 * U);
@@ -381,7 +383,8 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_pipe_kernel<U>, x, M, K, wq, wrm, gw, gx, N,
-                                       y, y_bf16 ? 1 : 0, stages, rgs, err);
+                                       y, y_bf16 ? 1 : 0, stages, rgs, w_static ? 1 : 0,
+                                       err);
     *launched = true;
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -390,18 +393,18 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
 
 cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                                 const uint8_t* wrm, const float* gw, const float* gx, int N,
-                                void* y, bool y_bf16, uint32_t* err, cudaStream_t stream,
-                                const DevInfo& dev, bool* launched) {
+                                void* y, bool y_bf16, uint32_t* err, bool w_static,
+                                cudaStream_t stream, const DevInfo& dev, bool* launched) {
     *launched = false;
     if (M < 2 || M > 8) return cudaSuccess;
     // at most kSkMaxGroups consumer warps: 4 or 8 chunks of K per warp
     const int rowchunks = K / 32;
     if ((rowchunks + 3) / 4 <= kSkMaxGroups)
-        return launch_skinny_u<1>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, stream, dev,
-                                  launched);
+        return launch_skinny_u<1>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, w_static, stream,
+                                  dev, launched);
     if ((rowchunks + 7) / 8 <= kSkMaxGroups)
-        return launch_skinny_u<2>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, stream, dev,
-                                  launched);
+        return launch_skinny_u<2>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, w_static, stream,
+                                  dev, launched);
     return cudaSuccess;
 }
 

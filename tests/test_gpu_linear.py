@@ -174,3 +174,23 @@ def test_skinny_stages_of_several_row_groups(M, K, N, wide):
     y, _ = run_linear(x, wq, ws, gw, K, torch.bfloat16)
     y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
     check_tolerance(y_to_f64(y), y_ref, ab, "row groups M%d K%d N%d" % (M, K, N))
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 5120, 1000), (1, 1024, 77), (7, 5120, 600), (3, 2048, 130)])
+def test_static_weights_flag(M, K, N):
+    # NVFP4_STATIC_WEIGHTS only moves the weight stream ahead of the wait for the previous
+    # kernel: the result is the same, here right after a kernel that wrote the weights'
+    # neighbour buffers and a quantization on the same stream
+    x, w = make_inputs(M, K, N, seed=700 + M + K)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    d_wq, d_swz, d_g = upload_weights(wq, ws, gw, K)
+    y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    wsb = nv.nvfp4_workspace_bytes(1, M, K, N)
+    work = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda")
+    d_x = x.cuda()
+    for _ in range(3):
+        nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, workspace=work, static_weights=True)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_workspace_error(work) == 0
+    y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+    check_tolerance(y_to_f64(y), y_ref, ab, "static M%d K%d N%d" % (M, K, N))
