@@ -247,9 +247,8 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                                                  pipe_slot_bytes(rows_max, ngroups));
     uint64_t* full = bars;
     uint64_t* empty = bars + stages;
-    __shared__ float red[32];
+    __shared__ float red[32], red_min[32];
     __shared__ float lut[128];
-    __shared__ int any_inexact_sh;
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -265,7 +264,6 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
             mbar_init(&empty[s], ngroups);
         }
         abort_flag = 0;
-        any_inexact_sh = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -315,50 +313,67 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
         return;
     }
 
-    // ---- consumers: the amax of x, then this lane's 32 values of x in registers ----
+    // ---- consumers: this lane's 32 values of x in registers, then x's largest and smallest
+    // nonzero magnitudes ----
+    // Every chunk of x belongs to at least one lane (chunk w G + l % G of warp w), so one
+    // round of loads gives both the lane's values and, reduced over the CTA, the magnitudes
+    // that fix the exponent e and whether every value is exact in fp16 after it.
     pdl_wait_prior_grid();
-    float am = 0.0f;
-    const uint32_t* xw = reinterpret_cast<const uint32_t*>(x);
-    for (int i = threadIdx.x; i < (K >> 1); i += nthreads_c) {
-        const uint32_t v = xw[i];
-        am = fmaxf(am, fmaxf(fabsf(bf16_to_f32(v & 0xFFFFu)), fabsf(bf16_to_f32(v >> 16))));
-    }
-    if (threadIdx.x < 128) lut[threadIdx.x] = e4m3_to_f32(threadIdx.x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    if (lane == 0) red[warp] = am;
-    named_bar_sync(1, nthreads_c);
-    float amax = 0.0f;
-    for (int i = 0; i < ngroups; ++i) amax = fmaxf(amax, red[i]);
-    const int e = chunk_exponent(amax);
-    const int e1 = e / 2, e2 = e - e / 2;
-    const float f1 = __int_as_float((e1 + 127) << 23), f2 = __int_as_float((e2 + 127) << 23);
-
     const int c = warp * G + (lane % G);   // this lane's chunk (column), fixed
     const int rsub = lane / G;             // its row within a step
     const bool cvalid = c < rowchunks;
-    uint32_t xh[16];                       // x'[32c .. 32c+32) as 16 fp16 pairs
-    bool inexact = false;
+    uint4 xv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        xv[q] = cvalid ? *reinterpret_cast<const uint4*>(x + 32 * c + 8 * q)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x < 128) lut[threadIdx.x] = e4m3_to_f32(threadIdx.x);
+    for (int i = threadIdx.x; i < nrows * ngroups; i += nthreads_c) slots[i] = 0.0f;
+    float am = 0.0f, mn = __int_as_float(0x7f800000);  // max, smallest nonzero
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const uint4 v = cvalid ? *reinterpret_cast<const uint4*>(x + 32 * c + 8 * q)
-                               : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w4[4] = {xv[q].x, xv[q].y, xv[q].z, xv[q].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = fabsf(bf16_to_f32(w4[j] & 0xFFFFu)), b = fabsf(bf16_to_f32(w4[j] >> 16));
+            am = fmaxf(am, fmaxf(a, b));
+            if (a > 0.0f) mn = fminf(mn, a);
+            if (b > 0.0f) mn = fminf(mn, b);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) {
+        red[warp] = am;
+        red_min[warp] = mn;
+    }
+    named_bar_sync(1, nthreads_c);
+    float amax = 0.0f, amin = __int_as_float(0x7f800000);
+    for (int i = 0; i < ngroups; ++i) {
+        amax = fmaxf(amax, red[i]);
+        amin = fminf(amin, red_min[i]);
+    }
+    const int e = chunk_exponent(amax);
+    const int e1 = e / 2, e2 = e - e / 2;
+    const float f1 = __int_as_float((e1 + 127) << 23), f2 = __int_as_float((e2 + 127) << 23);
+    // a bf16 value (8 significant bits) is exact in fp16 from 2^-17 upward: every value is
+    // when the smallest nonzero one is
+    const bool any_inexact = pow2_scale(amin, f1, f2) < 7.62939453125e-06f;
+    uint32_t xh[16];                       // x'[32c .. 32c+32) as 16 fp16 pairs
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t w4[4] = {xv[q].x, xv[q].y, xv[q].z, xv[q].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float a = pow2_scale(bf16_to_f32(w4[j] & 0xFFFFu), f1, f2);
             const float b = pow2_scale(bf16_to_f32(w4[j] >> 16), f1, f2);
-            // a bf16 value (8 significant bits) is exact in fp16 from 2^-17 upward
-            inexact |= (a != 0.0f && fabsf(a) < 7.62939453125e-06f) |
-                       (b != 0.0f && fabsf(b) < 7.62939453125e-06f);
             const __half2 hh = __floats2half2_rn(a, b);
             xh[q * 4 + j] = *reinterpret_cast<const uint32_t*>(&hh);
         }
     }
-    for (int i = threadIdx.x; i < nrows * ngroups; i += nthreads_c) slots[i] = 0.0f;
-    if (inexact) any_inexact_sh = 1;
-    named_bar_sync(1, nthreads_c);
-    const bool any_inexact = any_inexact_sh != 0;
     const bool lean = !any_inexact && ngroups * G == rowchunks;
 
     for (int it = 0; it < nst; ++it) {
