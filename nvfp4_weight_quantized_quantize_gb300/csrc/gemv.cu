@@ -247,8 +247,6 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                                                  pipe_slot_bytes(rows_max, ngroups));
     uint64_t* full = bars;
     uint64_t* empty = bars + stages;
-    __shared__ float red[32], red_min[32];
-    __shared__ float lut[128];
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -313,11 +311,13 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
         return;
     }
 
-    // ---- consumers: this lane's 32 values of x in registers, then x's largest and smallest
-    // nonzero magnitudes ----
-    // Every chunk of x belongs to at least one lane (chunk w G + l % G of warp w), so one
-    // round of loads gives both the lane's values and, reduced over the CTA, the magnitudes
-    // that fix the exponent e and whether every value is exact in fp16 after it.
+    // ---- consumers: this lane's 32 values of x in registers, fp16 after the lane's own
+    // power-of-two rescale ----
+    // A lane keeps one 32-element chunk of x for the whole kernel, so it scales the chunk
+    // by its own 2^e (largest magnitude in [2^14, 2^15)) and each partial dot product back
+    // by 2^-e before the row's lanes are added: no reduction over the CTA, no barrier.  A
+    // bf16 value is exact in fp16 after the rescale from 2^-17 upward; a warp with any lane
+    // whose smallest nonzero value falls below that takes the exact residual path.
     pdl_wait_prior_grid();
     const int c = warp * G + (lane % G);   // this lane's chunk (column), fixed
     const int rsub = lane / G;             // its row within a step
@@ -327,8 +327,6 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     for (int q = 0; q < 4; ++q)
         xv[q] = cvalid ? *reinterpret_cast<const uint4*>(x + 32 * c + 8 * q)
                        : make_uint4(0u, 0u, 0u, 0u);
-    if (threadIdx.x < 128) lut[threadIdx.x] = e4m3_to_f32(threadIdx.x);
-    for (int i = threadIdx.x; i < nrows * ngroups; i += nthreads_c) slots[i] = 0.0f;
     float am = 0.0f, mn = __int_as_float(0x7f800000);  // max, smallest nonzero
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -341,27 +339,12 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
             if (b > 0.0f) mn = fminf(mn, b);
         }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    }
-    if (lane == 0) {
-        red[warp] = am;
-        red_min[warp] = mn;
-    }
-    named_bar_sync(1, nthreads_c);
-    float amax = 0.0f, amin = __int_as_float(0x7f800000);
-    for (int i = 0; i < ngroups; ++i) {
-        amax = fmaxf(amax, red[i]);
-        amin = fminf(amin, red_min[i]);
-    }
-    const int e = chunk_exponent(amax);
+    const int e = chunk_exponent(am);
     const int e1 = e / 2, e2 = e - e / 2;
     const float f1 = __int_as_float((e1 + 127) << 23), f2 = __int_as_float((e2 + 127) << 23);
-    // a bf16 value (8 significant bits) is exact in fp16 from 2^-17 upward: every value is
-    // when the smallest nonzero one is
-    const bool any_inexact = pow2_scale(amin, f1, f2) < 7.62939453125e-06f;
+    const float u1 = __int_as_float((127 - e1) << 23), u2 = __int_as_float((127 - e2) << 23);
+    const bool inexact = pow2_scale(mn, f1, f2) < 7.62939453125e-06f;
+    const bool any_inexact = __any_sync(0xffffffffu, inexact);  // this warp's lanes
     uint32_t xh[16];                       // x'[32c .. 32c+32) as 16 fp16 pairs
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -416,7 +399,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                     mfma2(a[b], a[b + 1], hh[2], xh[4 * j + 2]);
                     mfma2(a[b], a[b + 1], hh[3], xh[4 * j + 3]);
                 }
-                float pv = fmaf(sc.x, a[0] + a[1], sc.y * (a[2] + a[3]));
+                float pv = fmaf(sc.x, a[0] + a[1], sc.y * (a[2] + a[3])) * u1 * u2;
 #pragma unroll
                 for (int o = G / 2; o > 0; o >>= 1) pv += __shfl_xor_sync(0xffffffffu, pv, o);
                 if ((lane % G) == 0) *sl = pv;
@@ -434,7 +417,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
             if (cvalid && rl < nr) {
                 const uint4 wv = *reinterpret_cast<const uint4*>(st + ((size_t)rl * rowchunks + c) * 16);
                 const uint32_t s01 = *reinterpret_cast<const uint16_t*>(sst + (size_t)rl * rows_sb + 2 * c);
-                const float s0 = lut[s01 & 0x7Fu], s1 = lut[(s01 >> 8) & 0x7Fu];
+                const float s0 = e4m3_to_f32(s01 & 0x7Fu), s1 = e4m3_to_f32((s01 >> 8) & 0x7Fu);
                 const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
                 float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -448,7 +431,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                     mfma2(a[b], a[b + 1], hh[3], xh[4 * j + 3]);
                 }
                 pv = fmaf(s0, a[0] + a[1], s1 * (a[2] + a[3]));
-                if (any_inexact) {
+                if (inexact) {
                     // exact residual of x' - fp16(x') (slow path, rare), fp16(x') formed
                     // exactly as above
                     float q0 = 0.0f, q1 = 0.0f;
@@ -464,6 +447,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                     }
                     pv += fmaf(s0, q0, s1 * q1);
                 }
+                pv = pv * u1 * u2;
             }
             // sum over the G lanes of each row of this step
 #pragma unroll
@@ -480,7 +464,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     for (int i = threadIdx.x; i < nrows; i += nthreads_c) {
         float v = 0.0f;
         for (int w = 0; w < ngroups; ++w) v += slots[i * ngroups + w];
-        store_y(y, r0 + i, ldexpf(v, -e) * scale, y_bf16);
+        store_y(y, r0 + i, v * scale, y_bf16);
     }
 }
 

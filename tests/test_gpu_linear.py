@@ -194,3 +194,20 @@ def test_static_weights_flag(M, K, N):
     assert nv.nvfp4_workspace_error(work) == 0
     y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
     check_tolerance(y_to_f64(y), y_ref, ab, "static M%d K%d N%d" % (M, K, N))
+
+
+@pytest.mark.parametrize("K,N", [(5120, 700), (17408, 300)])
+def test_m1_chunks_of_very_different_magnitude(K, N):
+    # every 32-element chunk of x at its own scale (2^-60 .. 2^60): the M=1 kernel rescales
+    # each lane's chunk by its own power of two and must still match the oracle
+    x, w = make_inputs(1, K, N, seed=800 + K)
+    xf = x.float()
+    scales = 2.0 ** torch.arange(-60, 61, 7, dtype=torch.float64).float()
+    for c in range(K // 32):
+        xf[:, 32 * c:32 * c + 32] *= scales[c % len(scales)]
+    x = xf.to(torch.bfloat16)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    for ydt in (torch.float32, torch.bfloat16):
+        y, _ = run_linear(x, wq, ws, gw, K, ydt)
+        y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+        check_tolerance(y_to_f64(y), y_ref, ab, "chunk scales K%d" % K)
