@@ -214,6 +214,7 @@ gemv_m1_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict_
 // and lets the copies it issued land before it exits.
 constexpr int kPipeMaxThreads = 1024;
 constexpr int kPipeStageTarget = 80 * 1024;  // bytes of codes per stage (whole rows)
+constexpr int kLeanUnroll = 2;  // unroll of the predicate-free step loop
 
 // exact x * 2^e for a bf16 value (two multiplies keep 2^e representable for any e)
 __device__ __forceinline__ float pow2_scale(float v, float f1, float f2) { return v * f1 * f2; }
@@ -374,14 +375,16 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
         const int nr = min(rps, nrows - it * rps);
         const int64_t rbeg = r0 + (int64_t)it * rps;
         const uint8_t* sst = st + (size_t)rps * rowb + ((rbeg * rows_sb) & 15);
-        if (lean && nr == rps) {
-            // a full stage, every lane on a real chunk, no residual pass: no predicates
+        // whole steps of L rows with every lane on a real chunk and no residual pass run
+        // without predicates; the rest of a short last stage takes the predicated loop
+        const int lean_rows = lean ? nr / L * L : 0;
+        if (lean_rows > 0) {
             const uint8_t* wp = st + ((size_t)rsub * rowchunks + c) * 16;
             const uint8_t* sp = sst + (size_t)rsub * rows_sb + 2 * c;
             float* sl = slots + (size_t)(it * rps + rsub) * ngroups + warp;
             const int wstep = L * rowchunks * 16, sstep = L * rows_sb, slstep = L * ngroups;
-            const int nsteps = rps / L;
-#pragma unroll 2
+            const int nsteps = lean_rows / L;
+#pragma unroll kLeanUnroll
             for (int t = 0; t < nsteps; ++t) {
                 const uint4 wv = *reinterpret_cast<const uint4*>(wp);
                 const uint32_t s01 = *reinterpret_cast<const uint16_t*>(sp);
@@ -407,11 +410,13 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                 sp += sstep;
                 sl += slstep;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            continue;
+            if (lean_rows == nr) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                continue;
+            }
         }
-        for (int t = 0; t < nr; t += L) {
+        for (int t = lean_rows; t < nr; t += L) {
             const int rl = t + rsub;       // row within the stage
             float pv = 0.0f;
             if (cvalid && rl < nr) {
