@@ -57,9 +57,17 @@ __device__ __forceinline__ int chunk_exponent(float amax) {
     return 15 - E;
 }
 
+// exact v * 2^e for |e| <= 252, as two power-of-two factors of the same sign (the
+// intermediate never leaves the range the final value is in); a chunk exponent lies in
+// [-114, 148]
+__device__ __forceinline__ float times_pow2(float v, int e) {
+    const int e1 = e / 2, e2 = e - e / 2;
+    return v * __int_as_float((e1 + 127) << 23) * __int_as_float((e2 + 127) << 23);
+}
+
 __device__ __forceinline__ uint32_t to_h2_scaled(uint32_t bf16x2, int e, bool& inexact) {
-    const float a = ldexpf(bf16_to_f32(bf16x2 & 0xFFFFu), e);
-    const float b = ldexpf(bf16_to_f32(bf16x2 >> 16), e);
+    const float a = times_pow2(bf16_to_f32(bf16x2 & 0xFFFFu), e);
+    const float b = times_pow2(bf16_to_f32(bf16x2 >> 16), e);
     const __half ha = __float2half_rn(a), hb = __float2half_rn(b);
     inexact |= (__half2float(ha) != a) | (__half2float(hb) != b);
     return (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
@@ -67,7 +75,7 @@ __device__ __forceinline__ uint32_t to_h2_scaled(uint32_t bf16x2, int e, bool& i
 
 // residual x' - fp16(x') of one bf16 element, exact in fp32
 __device__ __forceinline__ float residual(uint32_t bf16bits, int e) {
-    const float a = ldexpf(bf16_to_f32(bf16bits), e);
+    const float a = times_pow2(bf16_to_f32(bf16bits), e);
     return a - __half2float(__float2half_rn(a));
 }
 

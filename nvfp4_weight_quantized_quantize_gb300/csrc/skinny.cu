@@ -66,7 +66,6 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
     extern __shared__ __align__(128) uint8_t smem[];
     const int rowchunks = K >> 5;
     const int ngroups = (rowchunks + CG - 1) / CG;
-    const int nthreads_c = ngroups * 32;
     const size_t st_bytes = sk_stage_bytes(K, rgs);
     const size_t sl_bytes = sk_slot_bytes(ngroups, rgs);
     const int srows = kSkRows * rgs;  // rows of a full stage
@@ -75,11 +74,9 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * (st_bytes + sl_bytes));
     uint64_t* empty = full + stages;
     int* cnt = reinterpret_cast<int*>(empty + stages);
-    __shared__ uint32_t amax_bits[8];
-    __shared__ int e_sh[8];
-    __shared__ float pw_sh[8];  // 2^-e of each token (exact)
-    __shared__ int any_inexact_sh;
     __shared__ volatile int abort_flag;
+    __shared__ int e_w[kSkMaxGroups][8];    // per consumer warp and token: the exponent
+    __shared__ float u_w[kSkMaxGroups][8];  // and 2^-e
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -96,9 +93,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
             mbar_init(&empty[s], ngroups);
             for (int r = 0; r < kSkMaxRgs; ++r) cnt[s * kSkMaxRgs + r] = 0;
         }
-        for (int m = 0; m < 8; ++m) amax_bits[m] = 0u;
         abort_flag = 0;
-        any_inexact_sh = 0;
         fence_mbar_init();
     }
     __syncthreads();
@@ -150,13 +145,17 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
         return;
     }
 
-    // ---- consumers: this warp's slice of x in registers, per-token exponent ----
+    // ---- consumers: this warp's slice of x in registers, an exponent per token ----
     // Every (token, chunk) pair belongs to exactly one consumer thread (token g, chunk
-    // w CG + 4u + t), so one pass of loads gives both the B fragments and, reduced over
-    // the threads of each token, the token's maximum magnitude.
+    // w CG + 4u + t), so one pass of loads gives the B fragments and, reduced over the four
+    // threads of each token, the token's largest and smallest nonzero magnitude in this
+    // warp's K slice.  The warp scales each token's slice by its own 2^e (largest magnitude
+    // in [2^14, 2^15)) and each partial tile column back by 2^-e before it leaves the warp:
+    // no reduction over the CTA, no barrier.  A bf16 value is exact in fp16 after the
+    // rescale from 2^-17 upward; a warp with a value below that takes the residual path.
     pdl_wait_prior_grid();
     uint2 raw[U][8];
-    float am = 0.0f;
+    float am = 0.0f, mn = __int_as_float(0x7f800000);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int c = warp * CG + 4 * u + t;
@@ -172,27 +171,38 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
         for (int j = 0; j < 8; ++j) {
             const uint32_t w2[2] = {raw[u][j].x, raw[u][j].y};
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                am = fmaxf(am, fmaxf(fabsf(bf16_to_f32(w2[h] & 0xFFFFu)),
-                                     fabsf(bf16_to_f32(w2[h] >> 16))));
+            for (int h = 0; h < 2; ++h) {
+                const float a = fabsf(bf16_to_f32(w2[h] & 0xFFFFu));
+                const float b = fabsf(bf16_to_f32(w2[h] >> 16));
+                am = fmaxf(am, fmaxf(a, b));
+                if (a > 0.0f) mn = fminf(mn, a);
+                if (b > 0.0f) mn = fminf(mn, b);
+            }
         }
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-    // non-negative floats order like their bit patterns
-    if (t == 0 && g < M) atomicMax(&amax_bits[g], __float_as_uint(am));
-    named_bar_sync(1, nthreads_c);
-    if (threadIdx.x < 8) {
-        const int e = chunk_exponent(__uint_as_float(amax_bits[threadIdx.x]));
-        e_sh[threadIdx.x] = e;
-        pw_sh[threadIdx.x] = ldexpf(1.0f, -e);
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
+    const int eg = chunk_exponent(am);  // token g's exponent in this warp
+    const bool any_inexact =
+        __any_sync(0xffffffffu, times_pow2(mn, eg) < 7.62939453125e-06f);
+    // every token's exponent and 2^-e in this warp (token m's lanes are 4m .. 4m + 3), in
+    // the warp's own shared-memory row
+    {
+        const int em = __shfl_sync(0xffffffffu, eg, 4 * (lane & 7));
+        if (lane < 8) {
+            e_w[warp][lane] = em;
+            u_w[warp][lane] = times_pow2(1.0f, -em);
+        }
+        __syncwarp();
     }
-    named_bar_sync(1, nthreads_c);
+    // the columns this lane holds in the accumulator: tokens 2t and 2t + 1
+    const float ua = u_w[warp][2 * t], ub = u_w[warp][2 * t + 1];
 
     // B fragment (unit u, mma j): b0 = token g, elements 4j, 4j+1 of chunk c; b1 = elements
     // 4j+2, 4j+3 (k-slots 2t, 2t+1 and 2t+8, 2t+9)
     uint32_t bf[U][8][2];
-    bool inexact = false;
-    const int eg = e_sh[g];
+    bool inexact = false;  // (decided for the warp above)
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -200,9 +210,6 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
             bf[u][j][0] = to_h2_scaled(raw[u][j].x, eg, inexact);
             bf[u][j][1] = to_h2_scaled(raw[u][j].y, eg, inexact);
         }
-    if (inexact) any_inexact_sh = 1;
-    named_bar_sync(1, nthreads_c);
-    const bool any_inexact = any_inexact_sh != 0;
     const float gscale = *gw * (gx ? *gx : 1.0f);
 
     for (int it = 0; it < nst; ++it) {
@@ -268,10 +275,10 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
             // tokens 2t, 2t+1
             float* tiles = slots + ((size_t)s * rgs + rgi) * ngroups * (kSkRows * 8);
             float* mine = tiles + (size_t)warp * (kSkRows * 8);
-            mine[g * 8 + 2 * t] = d[0];
-            mine[g * 8 + 2 * t + 1] = d[1];
-            mine[(g + 8) * 8 + 2 * t] = d[2];
-            mine[(g + 8) * 8 + 2 * t + 1] = d[3];
+            mine[g * 8 + 2 * t] = d[0] * ua;
+            mine[g * 8 + 2 * t + 1] = d[1] * ub;
+            mine[(g + 8) * 8 + 2 * t] = d[2] * ua;
+            mine[(g + 8) * 8 + 2 * t + 1] = d[3] * ub;
             if (any_inexact) {
                 // exact residual x' - fp16(x') of this warp's K slice (slow path, rare): lane l
                 // takes row l % 16 and tokens l / 16, l / 16 + 2, ...
@@ -286,11 +293,11 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                                 const uint32_t byte = sw[(size_t)r * rowb + 16 * c + (k >> 1)];
                                 const uint32_t code = (k & 1) ? (byte >> 4) : (byte & 15u);
                                 const float sc = e4m3_to_f32(k < 16 ? (s2 & 0xFFu) : (s2 >> 8));
-                                q = fmaf(residual(x[(int64_t)m * K + 32 * c + k], e_sh[m]),
+                                q = fmaf(residual(x[(int64_t)m * K + 32 * c + k], e_w[warp][m]),
                                          e2m1_to_f32(code) * sc, q);
                             }
                         }
-                        mine[r * 8 + m] += q;
+                        mine[r * 8 + m] += q * u_w[warp][m];
                     }
                 }
             }
@@ -319,7 +326,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                 for (int i = 0; i < 4; ++i) {
                     const int e = lane + 32 * i, r = e >> 3, m = e & 7;
                     if (r < nr && m < M)
-                        store_y(y, (int64_t)m * N + rbeg + r, v[i] * pw_sh[m] * gscale, y_bf16);
+                        store_y(y, (int64_t)m * N + rbeg + r, v[i] * gscale, y_bf16);
                 }
             }
         }
