@@ -154,11 +154,15 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
     // no reduction over the CTA, no barrier.  A bf16 value is exact in fp16 after the
     // rescale from 2^-17 upward; a warp with a value below that takes the residual path.
     pdl_wait_prior_grid();
+    // the warp's K slice, rotated by the CTA index so that the CTAs, which all read the
+    // whole of x at the same moment, start on different parts of it
+    const int wk = (warp + (int)(blockIdx.x % (unsigned)ngroups)) % ngroups;
+    const int cbase = wk * CG + t;  // this lane's first chunk
     uint2 raw[U][8];
     float am = 0.0f, mn = __int_as_float(0x7f800000);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int c = warp * CG + 4 * u + t;
+        const int c = cbase + 4 * u;
         const bool ok = g < M && c < rowchunks;
         const uint16_t* xp = x + (int64_t)g * K + 32 * c;
 #pragma unroll
@@ -236,7 +240,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
             float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int c = warp * CG + 4 * u + t;
+                const int c = cbase + 4 * u;
                 const bool cv = c < rowchunks;
                 const uint4 wa = (cv && rga) ? *reinterpret_cast<const uint4*>(sw + (size_t)g * rowb + 16 * c)
                                              : make_uint4(0u, 0u, 0u, 0u);
@@ -287,7 +291,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                 if (r < nr) {
                     for (int m = lane >> 4; m < M; m += 2) {
                         float q = 0.0f;
-                        for (int c = warp * CG; c < min(rowchunks, (warp + 1) * CG); ++c) {
+                        for (int c = cbase - t; c < min(rowchunks, cbase - t + CG); ++c) {
                             const uint32_t s2 = *reinterpret_cast<const uint16_t*>(ss + (size_t)r * rows_sb + 2 * c);
                             for (int k = 0; k < 32; ++k) {
                                 const uint32_t byte = sw[(size_t)r * rowb + 16 * c + (k >> 1)];
