@@ -211,3 +211,23 @@ def test_m1_chunks_of_very_different_magnitude(K, N):
         y, _ = run_linear(x, wq, ws, gw, K, ydt)
         y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
         check_tolerance(y_to_f64(y), y_ref, ab, "chunk scales K%d" % K)
+
+
+def test_static_weights_flag_w4a4_small_m():
+    # the flag passes through the W4A4 path for M <= 16 (in-call x quantization, then the
+    # GEMV on the dequantized x): same result as without it
+    M, K, N = 1, 2048, 300
+    x, w = make_inputs(M, K, N, seed=901)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    d_wq, d_swz, d_g = upload_weights(wq, ws, gw, K)
+    outs = []
+    for flag in (False, True):
+        y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        wsb = nv.nvfp4_workspace_bytes(1, M, K, N, nv.NVFP4_W4A4)
+        work = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        nv.nvfp4_linear(x.cuda(), d_wq, d_swz, d_g, y, mode="w4a4", workspace=work,
+                        static_weights=flag)
+        torch.cuda.synchronize()
+        assert nv.nvfp4_workspace_error(work) == 0
+        outs.append(y.cpu())
+    assert torch.equal(outs[0], outs[1])
