@@ -289,16 +289,24 @@ def run_ours(args, rank, world, dist):
 
 def run_e2e(torch, nv, setup, args):
     S = setup.shapes
-    xh = [s["x_host"].pin_memory() for s in S]
-    yh = [torch.empty(1, s["N"], dtype=torch.bfloat16).pin_memory() for s in S]
+    # the step's inputs (both projections' x) sit in one pinned host buffer and go over in
+    # one copy; both outputs come back in one copy
+    ks = [s["K"] for s in S]
+    ns = [s["N"] for s in S]
+    xh = torch.cat([s["x_host"].reshape(-1) for s in S]).pin_memory()
+    yh = torch.empty(sum(ns), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty(sum(ks), dtype=torch.bfloat16, device="cuda")
+    yd = torch.empty(sum(ns), dtype=torch.bfloat16, device="cuda")
+    xv = [xd[sum(ks[:j]):sum(ks[:j + 1])].view(1, -1) for j in range(len(S))]
+    yv = [yd[sum(ns[:j]):sum(ns[:j + 1])].view(1, -1) for j in range(len(S))]
 
     def step(i):
         c = i % setup.copies
+        xd.copy_(xh, non_blocking=True)
         for j, s in enumerate(S):
-            s["x"].copy_(xh[j], non_blocking=True)
-            nv.nvfp4_linear(s["x"], s["copies"][c][0], s["copies"][c][1], s["g"], s["ys"][c],
+            nv.nvfp4_linear(xv[j], s["copies"][c][0], s["copies"][c][1], s["g"], yv[j],
                             workspace=s["ws"], static_weights=STATIC_W)
-            yh[j].copy_(s["ys"][c], non_blocking=True)
+        yh.copy_(yd, non_blocking=True)
 
     n = min(args.steps, 2048)
     G = min(n, 32)
@@ -316,8 +324,8 @@ def run_e2e(torch, nv, setup, args):
     t1.record()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    h2d = sum(s["x"].numel() * 2 for s in S)
-    d2h = sum(s["N"] * 2 for s in S)
+    h2d = xh.numel() * 2
+    d2h = yh.numel() * 2
     return {"value": round(setup.bytes_per_step * n / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
 
@@ -338,7 +346,7 @@ def time_graph(torch, fn, nsteps, reps):
 
 def measure_rows(torch, nv, setup):
     """Per-row throughput of the other hot-path steps (outside the timed region)."""
-    from synth import WORKLOADS, workload_inputs
+    from synth import WORKLOADS, random_x, workload_inputs
     rows = {}
     # a1 quantize (fp32 weights) and a2 repack, decode_a shape
     s = setup.shapes[0]
@@ -358,6 +366,18 @@ def measure_rows(torch, nv, setup):
     rows["a2_repack_17408x5120"] = {"GB/s": round(2 * N * K / 16 / ms / 1e6, 1),
                                     "us": round(ms * 1e3, 1)}
     del wd
+    # FP8 (E4M3, block-128) checkpoint -> BF16 -> NVFP4 on the same shape; 3 rotating
+    # copies of the FP8 input (267 MB > L2)
+    from synth import random_fp8_block128
+    q8, s8 = random_fp8_block128(N, K, 1)
+    q8d = [torch.from_numpy(q8).cuda() for _ in range(3)]
+    s8d = torch.from_numpy(s8).cuda()
+    ms = time_graph(torch, lambda i: nv.nvfp4_quantize_fp8_block128(q8d[i % 3], s8d, packed,
+                                                                    scales, g, ws), 6, 5)
+    fb = N * K + s8.size * 4 + N * K // 2 + N * K // 16 + 4
+    rows["f3_fp8_block128_to_nvfp4_17408x5120"] = {"GB/s": round(fb / ms / 1e6, 1),
+                                                   "us": round(ms * 1e3, 1)}
+    del q8d
     for sh in setup.shapes:
         ms = time_graph(torch, lambda i, sh=sh: nv.nvfp4_linear(
             sh["x"], sh["copies"][i % setup.copies][0], sh["copies"][i % setup.copies][1],
@@ -385,6 +405,40 @@ def measure_rows(torch, nv, setup):
         rows["a4_verify_%s_M7_K%d_N%d" % (name, wl.K, wl.N)] = {
             "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
         del cps, p, z
+    # the small-M curve: M = 1 .. 16 on the verify_a weights (K 5120, N 34816; 3 copies)
+    wl = WORKLOADS["verify_a"]
+    _, w = workload_inputs("verify_a")
+    p, _, z, gg = nv.quantize_weight(w.cuda())
+    del w
+    cps = [(p, z)] + [(p.clone(), z.clone()) for _ in range(2)]
+    curve = {}
+    for m in range(1, 17):
+        xd = random_x(m, wl.K, 40 + m).cuda()
+        y = torch.empty(m, wl.N, dtype=torch.bfloat16, device="cuda")
+        wsv = torch.zeros(nv.nvfp4_workspace_bytes(1, m, wl.K, wl.N), dtype=torch.uint8,
+                          device="cuda")
+        ms = time_graph(torch, lambda i: nv.nvfp4_linear(xd, cps[i % 3][0], cps[i % 3][1], gg,
+                                                         y, workspace=wsv,
+                                                         static_weights=STATIC_W), 6, 10)
+        curve["M%d" % m] = round(algo_bytes(m, wl.K, wl.N) / ms / 1e6, 1)
+    rows["f4_small_m_curve_K%d_N%d_GBps" % (wl.K, wl.N)] = curve
+    del cps, p, z
+    # a wide output (an lm-head-sized N = 151936, K 5120) at M = 1: one 438 MB copy > L2;
+    # weights drawn on the device (same N(0, 0.02) recipe, device generator)
+    Nw, Kw = 151936, 5120
+    gen = torch.Generator(device="cuda").manual_seed(9)
+    w = torch.randn(Nw, Kw, generator=gen, device="cuda", dtype=torch.float32) * 0.02
+    p, _, z, gg = nv.quantize_weight(w)
+    del w
+    xd = random_x(1, Kw, 9).cuda()
+    y = torch.empty(1, Nw, dtype=torch.bfloat16, device="cuda")
+    wsv = torch.zeros(nv.nvfp4_workspace_bytes(1, 1, Kw, Nw), dtype=torch.uint8, device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_linear(xd, p, z, gg, y, workspace=wsv,
+                                                     static_weights=STATIC_W), 4, 10)
+    b = algo_bytes(1, Kw, Nw)
+    rows["f4_wide_n_M1_K%d_N%d" % (Kw, Nw)] = {"GB/s": round(b / ms / 1e6, 1),
+                                               "us": round(ms * 1e3, 2)}
+    del p, z
     # a5 prefill M=512 W4A16 on the tensor cores (2 weight copies, inputs > L2)
     pk, _ = peaks()
     for name in ("prefill_a", "prefill_b"):

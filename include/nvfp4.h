@@ -129,6 +129,39 @@ nvfp4_status nvfp4_quantize_noalloc(const void* src, nvfp4_dtype src_dtype, int6
                                     float* global_scale, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_fp8_block128 -- FP8 (E4M3, block-128 scaled) weights to NVFP4.
+ *
+ * Defines: the load-time conversion of an FP8 "e4m3 block-128" checkpoint (the MTP
+ * head) through BF16 to NVFP4 (FlashRT docs/qwen36_usage.md, env-var table,
+ * FLASHRT_QWEN36_MTP_CKPT_DIR).  The pages name the chain without its arithmetic;
+ * the reading taken here is the common checkpoint convention:
+ *   1. w[r][c] = e4m3(src[r][c]) * block_scales[r / 128][c / 128], one fp32
+ *      round-to-nearest-even product (the scale multiplies: it is the inverse of the
+ *      scale the checkpoint's quantizer divided by);
+ *   2. w is rounded to bf16 (round to nearest even);
+ *   3. the bf16 tensor is quantized exactly as nvfp4_quantize quantizes a
+ *      NVFP4_BF16 source.
+ * Arguments:
+ *   src           [rows, cols] E4M3 (OCP "E4M3FN") bytes, row-major; NaN bytes (0x7F,
+ *                 0xFF), non-finite scales or a product that overflows give
+ *                 unspecified codes.
+ *   block_scales  [ceil(rows / 128), ceil(cols / 128)] fp32, row-major (device).
+ *   rows, cols    rows >= 1, cols >= 16, cols % 16 == 0 (a 16-element block never
+ *                 straddles two 128-column tiles).
+ *   packed, scales, global_scale, workspace: as for nvfp4_quantize (the same
+ *                 workspace size, nvfp4_workspace_bytes(0, rows, cols, 0, 0)).
+ *   src, packed, scales and workspace are 16-byte aligned; block_scales and
+ *   global_scale 4-byte aligned.
+ * Two kernels are enqueued (amax, then quantize); src is read twice and no bf16
+ * copy is written.  The result is bit-exact with the CPU reference of steps 1-3.
+ */
+nvfp4_status nvfp4_quantize_fp8_block128(const uint8_t* src, const float* block_scales,
+                                         int64_t rows, int64_t cols, uint8_t* packed,
+                                         uint8_t* scales, float* global_scale,
+                                         void* workspace, size_t workspace_bytes,
+                                         nvfp4_stream_t stream);
+
+/*
  * nvfp4_repack -- row-major E4M3 scales to the kernels' swizzled layout.
  *
  * Defines: the load-time "NVFP4 swizzle" (FlashRT docs/qwen36_usage.md, constructor

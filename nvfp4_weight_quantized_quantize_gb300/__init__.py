@@ -29,7 +29,7 @@ STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ER
 EXPORTS = ("nvfp4_quantize", "nvfp4_repack", "nvfp4_linear", "nvfp4_repack_bytes",
            "nvfp4_workspace_bytes", "nvfp4_w4a4_workspace_layout", "nvfp4_workspace_error",
            "nvfp4_status_str", "nvfp4_encode_elements", "nvfp4_quantize_noalloc",
-           "nvfp4_last_cuda_error")
+           "nvfp4_last_cuda_error", "nvfp4_quantize_fp8_block128")
 
 
 class Nvfp4Error(RuntimeError):
@@ -64,6 +64,7 @@ def load(path: str = LIB_PATH):
         "nvfp4_encode_elements": (I, [P, I64, P, P, P]),
         "nvfp4_quantize_noalloc": (I, [P, I, I64, I64, P, P, P, P]),
         "nvfp4_last_cuda_error": (ctypes.c_char_p, []),
+        "nvfp4_quantize_fp8_block128": (I, [P, P, I64, I64, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -149,6 +150,24 @@ def nvfp4_quantize_noalloc(src: torch.Tensor, packed: torch.Tensor, scales: torc
     st = load().nvfp4_quantize_noalloc(_p(src), _dtype_code(src.dtype), rows, cols, _p(packed),
                                        _p(scales), _p(global_scale), _stream(stream))
     _check(st, "nvfp4_quantize_noalloc")
+
+
+def nvfp4_quantize_fp8_block128(src: torch.Tensor, block_scales: torch.Tensor,
+                                packed: torch.Tensor, scales: torch.Tensor,
+                                global_scale: torch.Tensor, workspace: torch.Tensor,
+                                stream=None) -> None:
+    """FP8 E4M3 weights (uint8 bytes [rows, cols]) with fp32 scales per 128 x 128 tile
+    ([ceil(rows/128), ceil(cols/128)]) to NVFP4 through bf16."""
+    rows, cols = src.shape
+    if src.dtype != torch.uint8 or block_scales.dtype != torch.float32:
+        raise ValueError("src must be uint8 E4M3 bytes and block_scales float32")
+    if tuple(block_scales.shape) != ((rows + 127) // 128, (cols + 127) // 128):
+        raise ValueError("block_scales must be [ceil(rows/128), ceil(cols/128)]")
+    st = load().nvfp4_quantize_fp8_block128(_p(src), _p(block_scales), rows, cols, _p(packed),
+                                            _p(scales), _p(global_scale), _p(workspace),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream(stream))
+    _check(st, "nvfp4_quantize_fp8_block128")
 
 
 def nvfp4_repack(scales: torch.Tensor, cols: int, out: torch.Tensor, stream=None) -> None:

@@ -28,6 +28,13 @@ cudaError_t launch_quantize(const void* src, bool src_bf16, int64_t rows, int64_
                             int npartials, uint16_t* deq_bf16, cudaStream_t stream,
                             const DevInfo& dev);
 
+// FP8 (E4M3) source with one fp32 scale per 128 x 128 tile: each value is
+// bf16(e4m3 * scale), then quantized as launch_quantize does (scales row-major).
+cudaError_t launch_quantize_fp8_b128(const uint8_t* src, const float* block_scales,
+                                     int64_t rows, int64_t cols, uint8_t* packed,
+                                     uint8_t* scales, float* g_out, float* partials,
+                                     int npartials, cudaStream_t stream, const DevInfo& dev);
+
 cudaError_t launch_repack(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out,
                           cudaStream_t stream, const DevInfo& dev);
 

@@ -192,6 +192,30 @@ NVFP4_API nvfp4_status nvfp4_quantize(const void* src, nvfp4_dtype src_dtype, in
                                      partial_count(rows * cols, d), nullptr, stream, d));
 }
 
+NVFP4_API nvfp4_status nvfp4_quantize_fp8_block128(const uint8_t* src,
+                                                   const float* block_scales, int64_t rows,
+                                                   int64_t cols, uint8_t* packed,
+                                                   uint8_t* scales, float* global_scale,
+                                                   void* workspace, size_t workspace_bytes,
+                                                   nvfp4_stream_t stream) {
+    if (!src || !block_scales || !packed || !scales || !global_scale || !workspace)
+        return NVFP4_ERR_NULL;
+    if (rows < 1 || cols < 16 || cols % 16 != 0 || rows > kMaxDim || cols > kMaxDim)
+        return NVFP4_ERR_SHAPE;
+    if (!aligned(src, 16) || !aligned(packed, 16) || !aligned(scales, 16) ||
+        !aligned(workspace, 16) || !aligned(block_scales, 4) || !aligned(global_scale, 4))
+        return NVFP4_ERR_ALIGN;
+    if (workspace_bytes < nvfp4_workspace_bytes(0, rows, cols, 0, NVFP4_W4A16))
+        return NVFP4_ERR_WORKSPACE;
+    DevInfo d;
+    nvfp4_status st = current_device(&d);
+    if (st != NVFP4_OK) return st;
+    float* partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kHeaderBytes);
+    return from_cuda(launch_quantize_fp8_b128(src, block_scales, rows, cols, packed, scales,
+                                              global_scale, partials,
+                                              partial_count(rows * cols, d), stream, d));
+}
+
 NVFP4_API nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t cols,
                                     uint8_t* scales_swizzled, size_t swizzled_bytes,
                                     nvfp4_stream_t stream) {

@@ -11,6 +11,9 @@
 // scale itself (no inter-CTA counter, nothing to reset), then one thread quantizes
 // one 16-element block: 64 (fp32) or 32 (bf16) contiguous bytes in, 8 packed bytes
 // and one scale byte out.  Both passes are HBM-bound.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include <mutex>
 
 #include "../../include/nvfp4.h"
@@ -156,6 +159,85 @@ quantize_kernel(const void* __restrict__ src, int64_t rows, int64_t cols,
     }
 }
 
+// ---- FP8 (E4M3, one fp32 scale per 128 x 128 tile) sources --------------------------------
+// A value of such a tensor, as the NVFP4 quantizer sees it: e4m3(byte) * tile scale in one
+// fp32 round-to-nearest-even product, then rounded to bf16 (the checkpoint goes FP8 -> BF16
+// -> NVFP4).  E4M3 values are exact in f16, so the pair conversion loses nothing.
+
+// row and first column of 16-byte group i (cols % 16 == 0: a group lies inside one
+// 128-column tile and takes one scale); 32-bit division while the indices fit
+__device__ __forceinline__ float fp8_group_scale(const float* __restrict__ bs, int64_t cols,
+                                                 int64_t i) {
+    const int64_t gpr = cols >> 4;  // groups per row
+    int64_t r;
+    if (i <= 0xFFFFFFFFll && gpr <= 0xFFFFFFFFll) r = (uint32_t)i / (uint32_t)gpr;
+    else r = i / gpr;
+    const int64_t c = (i - r * gpr) << 4;
+    return __ldg(bs + (r >> 7) * ((cols + 127) >> 7) + (c >> 7));
+}
+
+// the 16 values of a group: bytes -> f16 pairs (hardware), fp32 products, bf16 pairs (RNE)
+__device__ __forceinline__ void fp8_group_values(const uint4 v, float s, float (&t)[16]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t h2 = cvt_e4m3x2_f16x2((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(f.x, s), __fmul_rn(f.y, s));
+        t[2 * j] = __low2float(b);
+        t[2 * j + 1] = __high2float(b);
+    }
+}
+
+// Pass 1.  RN(e * s) and the bf16 rounding are monotone in |e| and odd in e, and a
+// non-negative E4M3 byte orders like its value, so a group's largest |value| is
+// bf16(RN(max|e| * |s|)): one byte-wise max, then one product.
+__global__ void __launch_bounds__(kThreads)
+amax_fp8_b128_kernel(const uint8_t* __restrict__ src, const float* __restrict__ bs,
+                     int64_t cols, int64_t ngroups, float* __restrict__ partials) {
+    float m = 0.0f;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < ngroups;
+         i += (int64_t)gridDim.x * kThreads) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(src) + i);
+        const float s = fabsf(fp8_group_scale(bs, cols, i));
+        uint32_t b = __vmaxu4(__vmaxu4(v.x & 0x7F7F7F7Fu, v.y & 0x7F7F7F7Fu),
+                              __vmaxu4(v.z & 0x7F7F7F7Fu, v.w & 0x7F7F7F7Fu));
+        b = max(max(b & 0xFFu, (b >> 8) & 0xFFu), max((b >> 16) & 0xFFu, b >> 24));
+        m = fmaxf(m, __bfloat162float(__float2bfloat16_rn(__fmul_rn(e4m3_to_f32(b), s))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float red[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float r = red[0];
+#pragma unroll
+        for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
+        partials[blockIdx.x] = r;
+    }
+}
+
+// One thread per 16-element block, as quantize_kernel, scales row-major.
+__global__ void __launch_bounds__(kThreads)
+quantize_fp8_b128_kernel(const uint8_t* __restrict__ src, const float* __restrict__ bs,
+                         int64_t cols, int64_t ngroups, const float* __restrict__ partials,
+                         int npartials, uint8_t* __restrict__ packed,
+                         uint8_t* __restrict__ scales, float* __restrict__ g_out) {
+    const float g = cta_global_scale(nullptr, partials, npartials);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < ngroups;
+         i += (int64_t)gridDim.x * kThreads) {
+        float t[16];
+        fp8_group_values(__ldcs(reinterpret_cast<const uint4*>(src) + i),
+                         fp8_group_scale(bs, cols, i), t);
+        uint32_t lo, hi;
+        const uint32_t s8 = quantize_block16(t, g, lo, hi);
+        reinterpret_cast<uint2*>(packed)[i] = make_uint2(lo, hi);
+        scales[i] = (uint8_t)s8;
+    }
+}
+
 // One thread per 16-byte line of the swizzled layout: line i of atom (rb, ka) holds
 // rows rb*128 + i + {0, 32, 64, 96}, scale columns ka*4 .. ka*4+3.
 __global__ void __launch_bounds__(kThreads)
@@ -237,6 +319,18 @@ cudaError_t launch_quantize(const void* src, bool src_bf16, int64_t rows, int64_
         if (swizzled_scales) NVFP4_Q(false, true); else NVFP4_Q(false, false);
     }
 #undef NVFP4_Q
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_fp8_b128(const uint8_t* src, const float* block_scales,
+                                     int64_t rows, int64_t cols, uint8_t* packed,
+                                     uint8_t* scales, float* g_out, float* partials,
+                                     int npartials, cudaStream_t stream, const DevInfo& dev) {
+    const int64_t ngroups = rows * (cols / 16);
+    amax_fp8_b128_kernel<<<npartials, kThreads, 0, stream>>>(src, block_scales, cols, ngroups,
+                                                             partials);
+    quantize_fp8_b128_kernel<<<grid_for(ngroups, dev, 8), kThreads, 0, stream>>>(
+        src, block_scales, cols, ngroups, partials, npartials, packed, scales, g_out);
     return cudaGetLastError();
 }
 

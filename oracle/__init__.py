@@ -16,6 +16,10 @@ How each function is pinned (tests/test_oracle_*):
   quantize                   hand-worked blocks (tests/golden), exact round trips of
                              every code x every finite scale, zero / tiny blocks,
                              element error bounds on random data.
+  dequant_fp8_block128       hand-worked bf16 ties (tests/golden), per-tile powers of
+                             two that expose the tile index, every byte against the
+                             E4M3 closed form, torch's float8_e4m3fn decode and bf16
+                             cast on random data.
   repack                     hand-derived byte offsets, bijection, zero padding; the
                              tensor-core W4A4 result on the GPU reads the same layout.
   linear_w4a16 / _w4a4       exact rational brute force on tiny shapes, one-hot and
@@ -93,6 +97,7 @@ def _load():
             "orc_linear_w4a4_pairs": (ctypes.c_int, [P, P, F, I64, I64, P, P,
                                                      F, I64, P, P, I64, P, P]),
             "orc_num_threads": (ctypes.c_int, []),
+            "orc_dequant_fp8_block128": (None, [P, P, I64, I64, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -184,6 +189,23 @@ def quantize(src, global_scale: float | None = None):
     if rc != 0:
         raise ValueError("oracle quantize: non-finite input, bad global scale or cols % 16")
     return packed, scales, float(g[0])
+
+
+def dequant_fp8_block128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """R10: E4M3 bytes [R, C] and fp32 tile scales [ceil(R/128), ceil(C/128)] -> the bf16
+    tensor bf16(e4m3(q) * s) as uint16 bit patterns [R, C]."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    rows, cols = q.shape
+    assert s.shape == ((rows + 127) // 128, (cols + 127) // 128)
+    out = np.empty((rows, cols), dtype=np.uint16)
+    _load().orc_dequant_fp8_block128(_ptr(q), _ptr(s), rows, cols, _ptr(out))
+    return out
+
+
+def quantize_fp8_block128(q: np.ndarray, s: np.ndarray):
+    """FP8 block-128 weights -> BF16 -> NVFP4 (R10, then R1-R9): (packed, scales, g)."""
+    return quantize(dequant_fp8_block128(q, s))
 
 
 def repack_bytes(rows: int, cols: int) -> int:

@@ -49,6 +49,12 @@
  *       in fp64; for activations quantized to NVFP4 (W4A4), x is replaced by its
  *       dequantized value.
  *   R9  non-finite inputs violate the precondition; the quantizer reports them.
+ *   R10 FP8 "e4m3 block-128" source (the MTP checkpoint, FlashRT
+ *       docs/qwen36_usage.md, env-var table, FLASHRT_QWEN36_MTP_CKPT_DIR: FP8 e4m3
+ *       block-128, converted FP8 -> BF16 -> NVFP4): one fp32 scale per 128 x 128
+ *       tile, stored [ceil(R/128), ceil(C/128)] row-major, which multiplies the E4M3
+ *       value; the product is one fp32 round-to-nearest-even multiply, then rounded
+ *       to bf16 (nearest even), and the bf16 tensor is quantized by R1-R9.
  *
  * Built with strict IEEE semantics (-O2 -ffp-contract=off, no fast-math): every
  * fp32 operation below is one correctly rounded operation.
@@ -167,6 +173,22 @@ ORC_EXPORT uint16_t orc_round_bf16(double v) {
 
 ORC_EXPORT void orc_round_bf16_array(const double* v, int64_t n, uint16_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_round_bf16(v[i]);
+}
+
+/* R10: FP8 E4M3 bytes q [rows, cols] with fp32 tile scales s [ceil(rows/128),
+ * ceil(cols/128)] -> bf16 bit patterns of bf16(e4m3(q) * s), the tensor that the FP8
+ * -> BF16 -> NVFP4 chain hands to the quantizer.  NaN bytes stay NaN (the quantizer
+ * then rejects the tensor, R9). */
+ORC_EXPORT void orc_dequant_fp8_block128(const uint8_t* q, const float* s, int64_t rows,
+                                         int64_t cols, uint16_t* out) {
+    const int64_t tiles_per_row = (cols + 127) / 128;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            const float v = (float)orc_e4m3_value(q[r * cols + c]); /* exact */
+            const float p = v * s[(r / 128) * tiles_per_row + c / 128];
+            out[r * cols + c] = orc_round_bf16((double)p);          /* p is exact in fp64 */
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------- */

@@ -98,6 +98,33 @@ def random_x(M: int, K: int, seed: int, scale: float = 1.0) -> torch.Tensor:
     return (torch.randn(M, K, generator=gen, dtype=torch.float32) * scale).to(torch.bfloat16)
 
 
+def random_fp8_block128(rows: int, cols: int, seed: int, kind: str = "normal"):
+    """An FP8 "e4m3 block-128" weight: (E4M3 bytes uint8 [rows, cols], fp32 tile scales
+    [ceil(rows/128), ceil(cols/128)]), on the CPU.
+
+    kind "normal": bytes of N(0, 1) * 64 draws (clamped to +-448) as torch's
+    float8_e4m3fn stores them, like a checkpoint whose tiles were scaled to use the
+    format's range; tile scales 2^U(-14, -8) (weights of magnitude about 0.02).
+    kind "uniform": every non-NaN byte equally likely (the widest spread of magnitudes
+    inside a block), tile scales 2^U(-14, -4).
+    """
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    nt = ((rows + 127) // 128, (cols + 127) // 128)
+    if kind == "normal":
+        v = (torch.randn(rows, cols, generator=gen, dtype=torch.float32) * 64.0).clamp(-448.0, 448.0)
+        q = v.to(torch.float8_e4m3fn).view(torch.uint8)
+        e = torch.rand(nt, generator=gen, dtype=torch.float64) * 6.0 - 14.0
+    elif kind == "uniform":
+        q = torch.randint(0, 254, (rows, cols), generator=gen, dtype=torch.int64)
+        q = q + (q >= 0x7F).to(torch.int64)  # skip 0x7F; 254 values cover 0x00..0xFE
+        q = q.to(torch.uint8)
+        e = torch.rand(nt, generator=gen, dtype=torch.float64) * 10.0 - 14.0
+    else:
+        raise ValueError(kind)
+    s = torch.exp2(e).to(torch.float32)
+    return q.numpy().copy(), s.numpy().copy()
+
+
 def random_w(N: int, K: int, seed: int, std: float = 0.02) -> torch.Tensor:
     gen = torch.Generator(device="cpu").manual_seed(seed)
     return torch.randn(N, K, generator=gen, dtype=torch.float32) * std

@@ -86,6 +86,25 @@ def test_quantize_rejects(lib):
     assert _q(lib, wsb=16) == WORKSPACE
 
 
+def _q8(lib, src=16, bs=20, rows=4, cols=32, packed=32, scales=48, g=64, ws=4096,
+        wsb=1 << 20):
+    v = lambda a: None if a is None else ctypes.c_void_p(a)
+    return lib.nvfp4_quantize_fp8_block128(v(src), v(bs), rows, cols, v(packed), v(scales),
+                                           v(g), v(ws), wsb, None)
+
+
+def test_quantize_fp8_block128_rejects(lib):
+    assert _q8(lib, src=None) == NULL
+    assert _q8(lib, bs=None) == NULL
+    assert _q8(lib, ws=None) == NULL
+    assert _q8(lib, cols=24) == SHAPE
+    assert _q8(lib, rows=0) == SHAPE
+    assert _q8(lib, src=17) == ALIGN
+    assert _q8(lib, bs=22) == ALIGN
+    assert _q8(lib, scales=40) == ALIGN
+    assert _q8(lib, wsb=16) == WORKSPACE
+
+
 def _r(lib, src=16, rows=4, cols=32, out=32, nbytes=None):
     v = lambda a: None if a is None else ctypes.c_void_p(a)
     if nbytes is None:

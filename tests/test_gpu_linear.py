@@ -16,7 +16,7 @@ from synth import WORKLOADS, make_inputs, random_x, workload_inputs
 pytestmark = pytest.mark.gpu
 
 
-def run_linear(x, wq, ws, gw, K, y_dtype, mode="w4a16", gx=None):
+def run_linear(x, wq, ws, gw, K, y_dtype, mode="w4a16", gx=None, static_weights=False):
     M = x.shape[0]
     N = wq.shape[0]
     d_wq, d_swz, d_g = upload_weights(wq, ws, gw, K)
@@ -25,7 +25,8 @@ def run_linear(x, wq, ws, gw, K, y_dtype, mode="w4a16", gx=None):
     wsb = nv.nvfp4_workspace_bytes(1, M, K, N, nv.NVFP4_W4A4 if mode == "w4a4" else nv.NVFP4_W4A16)
     ws_t = torch.zeros(max(wsb, 16), dtype=torch.uint8, device="cuda") if wsb else None
     d_gx = None if gx is None else torch.tensor([gx], dtype=torch.float32, device="cuda")
-    nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, mode=mode, x_global_scale=d_gx, workspace=ws_t)
+    nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, mode=mode, x_global_scale=d_gx, workspace=ws_t,
+                    static_weights=static_weights)
     torch.cuda.synchronize()
     assert nv.nvfp4_workspace_error(ws_t) == 0
     return y, ws_t
@@ -231,3 +232,31 @@ def test_static_weights_flag_w4a4_small_m():
         assert nv.nvfp4_workspace_error(work) == 0
         outs.append(y.cpu())
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("M", list(range(1, 17)))
+def test_every_small_m(M):
+    # the small-M curve: every M the GEMV / skinny / mma.sync kernels take, on a shape
+    # with a ragged row count and several K chunks per warp
+    x, w = make_inputs(M, 2080, 1203, seed=300 + M, outliers=True)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, _ = run_linear(x, wq, ws, gw, 2080, torch.bfloat16, static_weights=(M % 2 == 0))
+    y_ref, ab = oracle.linear_w4a16(x, wq, ws, gw)
+    check_tolerance(y_to_f64(y), y_ref, ab, "M%d" % M)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_wide_n(M):
+    # an lm-head-like output: N = 131075 rows (ragged), K = 1024, sampled outputs plus the
+    # first and last 4096 of every row of y
+    K, N = 1024, 131075
+    x, w = make_inputs(M, K, N, seed=400 + M)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    del w
+    y, _ = run_linear(x, wq, ws, gw, K, torch.bfloat16, static_weights=True)
+    rng = np.random.default_rng(M)
+    edge = np.concatenate([np.arange(4096), np.arange(N - 4096, N)])
+    pm = np.concatenate([rng.integers(0, M, 8192), np.repeat(np.arange(M), edge.size)])
+    pn = np.concatenate([rng.integers(0, N, 8192), np.tile(edge, M)])
+    y_ref, ab = oracle.linear_w4a16_pairs(x, wq, ws, gw, pm, pn)
+    check_tolerance(y_to_f64(y)[pm, pn], y_ref, ab, "wide N M%d" % M)

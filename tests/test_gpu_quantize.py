@@ -12,7 +12,7 @@ import nvfp4_weight_quantized_quantize_gb300 as nv
 import oracle
 from conftest import GOLDEN
 from helpers import to_dev
-from synth import make_inputs, random_w, workload_inputs
+from synth import make_inputs, random_fp8_block128, random_w, workload_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -178,3 +178,70 @@ def test_e4m3_rounding_window_and_strided():
     nv.nvfp4_encode_elements(d, None, out)
     want = _oracle_encode_chunked(oracle.e4m3_encode, host.view(np.float32))
     np.testing.assert_array_equal(out.cpu().numpy(), want)
+
+
+# ---- FP8 (E4M3, block-128) weights -> BF16 -> NVFP4 ------------------------------------
+
+def gpu_quantize_fp8(q: np.ndarray, s: np.ndarray):
+    rows, cols = q.shape
+    packed = torch.empty(rows, cols // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows, cols // 16, dtype=torch.uint8, device="cuda")
+    g = torch.empty(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(nv.nvfp4_workspace_bytes(0, rows, cols), dtype=torch.uint8, device="cuda")
+    nv.nvfp4_quantize_fp8_block128(torch.from_numpy(q).cuda(), torch.from_numpy(s).cuda(),
+                                   packed, scales, g, ws)
+    torch.cuda.synchronize()
+    return packed.cpu().numpy(), scales.cpu().numpy(), float(g.item())
+
+
+def assert_same_fp8_quantization(q: np.ndarray, s: np.ndarray):
+    p, sc, g = gpu_quantize_fp8(q, s)
+    po, so, go = oracle.quantize_fp8_block128(q, s)
+    assert g == go
+    np.testing.assert_array_equal(sc, so)
+    np.testing.assert_array_equal(p, po)
+
+
+@pytest.mark.parametrize("rows,cols,seed,kind", [
+    (1, 16, 0, "normal"), (5, 48, 1, "uniform"), (129, 272, 2, "normal"),
+    (130, 400, 3, "uniform"), (257, 1040, 4, "normal"), (300, 4096, 5, "uniform"),
+])
+def test_fp8_block128_ragged(rows, cols, seed, kind):
+    assert_same_fp8_quantization(*random_fp8_block128(rows, cols, seed, kind))
+
+
+def test_fp8_block128_edge_tiles():
+    # tiles with a zero scale (signed zeros), scales that make fp32 and bf16 subnormals,
+    # and the bytes of the hand-worked cases (signed zero, subnormal, +-448) in one column
+    q, s = random_fp8_block128(200, 272, 6, "uniform")
+    s[0, 0] = 0.0
+    s[0, 1] = 2.0 ** -125
+    s[1, 2] = 2.0 ** -120
+    h = json.load(open(os.path.join(GOLDEN, "fp8_block128.json")))
+    for i, case in enumerate(h["cases"]):
+        q[130 + i, 5] = int(case["q"], 16)
+    assert_same_fp8_quantization(q, s)
+
+
+def test_fp8_block128_all_zero_scales():
+    q, s = random_fp8_block128(64, 160, 7, "uniform")
+    s[:] = 0.0
+    p, sc, g = gpu_quantize_fp8(q, s)
+    assert g == 1.0 and not sc.any()
+    po, so, go = oracle.quantize_fp8_block128(q, s)
+    np.testing.assert_array_equal(p, po)  # sign bits of the negative zeros
+
+
+def test_fp8_block128_full_size():
+    # the decode projection's shape (17408 x 5120) as a checkpoint-like FP8 tensor
+    assert_same_fp8_quantization(*random_fp8_block128(17408, 5120, 8, "normal"))
+
+
+def test_fp8_block128_subnormal_tensor():
+    # every product an fp32 / bf16 subnormal: the global scale, the block scales and the
+    # codes all hang on the subnormal bf16 roundings
+    q, s = random_fp8_block128(256, 512, 9, "uniform")
+    s[:] = 2.0 ** -130
+    s[1, 2] = 2.0 ** -133
+    s[0, 3] = 2.0 ** -127
+    assert_same_fp8_quantization(q, s)
