@@ -787,6 +787,9 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     const size_t budget = dev.smem_optin - 2048;
     int stages = 8;
     while (stages > 2 && pipe_smem(K, rows_max, rps, stages, ngroups) > budget) --stages;
+    // a CTA with many rows (a wide N) keeps a large slot area: shorter stages, in whole
+    // steps, where two full ones do not fit beside it
+    while (rps > L && pipe_smem(K, rows_max, rps, stages, ngroups) > budget) rps -= L;
     const size_t smem = pipe_smem(K, rows_max, rps, stages, ngroups);
     if (smem + 2048 > dev.smem_optin) return cudaSuccess;
     static std::atomic<uint64_t> configured{0};
@@ -858,28 +861,6 @@ cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
                                                   w_static, stream, dev, &launched);
         if (e != cudaSuccess || launched) return e;
         return launch_mma<1>(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, stream, dev);
-    }
-    // 9 <= M <= 16: tokens 0..7 through the skinny kernel, then tokens 8..M-1 through it
-    // again (the M = 1 GEMV for a single one).  W is streamed twice, the second time
-    // partly from L2, and the second launch starts streaming under the first.  Each
-    // output depends on its own token only, so the split changes no result.
-    {
-        bool launched = false;
-        cudaError_t e = launch_skinny_w4a16(x, 8, K, wq, wsz, gw, gx, N, y, y_bf16, err,
-                                            w_static, stream, dev, &launched);
-        if (e != cudaSuccess) return e;
-        if (launched) {
-            const uint16_t* x2 = x + (int64_t)8 * K;
-            void* y2 = static_cast<uint8_t*>(y) + (int64_t)8 * N * (y_bf16 ? 2 : 4);
-            if (M == 9)
-                return launch_m1(x2, K, wq, wsz, gw, gx, N, y2, y_bf16, err, w_static, stream,
-                                 dev);
-            e = launch_skinny_w4a16(x2, M - 8, K, wq, wsz, gw, gx, N, y2, y_bf16, err,
-                                    w_static, stream, dev, &launched);
-            // the second call sees the same K and N, so it launches too
-            if (e != cudaSuccess || launched) return e;
-            return cudaErrorLaunchFailure;
-        }
     }
     return launch_mma<2>(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, stream, dev);
 }

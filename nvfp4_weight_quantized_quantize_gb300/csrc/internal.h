@@ -53,6 +53,9 @@ cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
 
 constexpr int kGemvMaxM = 16;
 
+// Whether launch_skinny_w4a16 takes calls with this K (its ring fits shared memory).
+bool skinny_w4a16_takes(int K, const DevInfo& dev);
+
 // 2 <= M <= 8 W4A16 skinny GEMM streaming W through a shared-memory ring, tensor cores
 // for the arithmetic.  wrm: the row-major part of the repacked scales.  Sets *launched
 // when it took the call (K small enough for its ring); otherwise the caller falls back.

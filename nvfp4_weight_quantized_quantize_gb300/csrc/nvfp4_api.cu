@@ -76,6 +76,23 @@ size_t repack_bytes(int64_t rows, int64_t cols) {
     return repack_atom_bytes(rows, cols) + (size_t)((rows * (cols / 16) + 15) / 16 * 16) + 16;
 }
 
+// M <= 16 on the small-M kernels.  The skinny kernel takes at most 8 tokens; where it
+// takes this K, 9 <= M <= 16 runs as tokens 0..7 and then tokens 8..M-1 (the M = 1 GEMV
+// for one): W is streamed twice, the second time partly from L2 and under the first
+// launch.  Each output depends on its own token only, so the split changes no result.
+cudaError_t small_m(const uint16_t* x, int M, int K, const uint8_t* wq, const uint8_t* wsz,
+                    const float* gw, const float* gx, int N, void* y, bool ybf, uint32_t* err,
+                    bool w_static, cudaStream_t stream, const DevInfo& d) {
+    if (M <= 8 || !skinny_w4a16_takes(K, d))
+        return launch_gemv_w4a16(x, M, K, wq, wsz, gw, gx, N, y, ybf, err, w_static, stream, d);
+    const cudaError_t e =
+        launch_gemv_w4a16(x, 8, K, wq, wsz, gw, gx, N, y, ybf, err, w_static, stream, d);
+    if (e != cudaSuccess) return e;
+    return launch_gemv_w4a16(x + (int64_t)8 * K, M - 8, K, wq, wsz, gw, gx, N,
+                             static_cast<uint8_t*>(y) + (int64_t)8 * N * (ybf ? 2 : 4), ybf,
+                             err, w_static, stream, d);
+}
+
 int partial_count(int64_t n, const DevInfo& d) {
     int p = amax_partial_count(n, d.sm_count);
     return p > kMaxPartials ? kMaxPartials : p;
@@ -258,10 +275,9 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
 
     if (mode == NVFP4_W4A16) {
         if (M <= kGemvMaxM)
-            return from_cuda(launch_gemv_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
-                                               w_global_scale, nullptr, (int)N, y, ybf,
-                                               static_cast<uint32_t*>(workspace), w_static,
-                                               stream, d));
+            return from_cuda(small_m(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                     w_global_scale, nullptr, (int)N, y, ybf,
+                                     static_cast<uint32_t*>(workspace), w_static, stream, d));
         return from_cuda(launch_gemm_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
                                            w_global_scale, (int)N, y, ybf,
                                            static_cast<uint8_t*>(workspace), stream, d));
@@ -276,10 +292,9 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
                                     partial_count(M * K, d), deq, stream, d);
     if (e != cudaSuccess) return from_cuda(e);
     if (M <= kGemvMaxM)
-        return from_cuda(launch_gemv_w4a16(deq, (int)M, (int)K, w_packed, w_scales_swizzled,
-                                           w_global_scale, gx, (int)N, y, ybf,
-                                           reinterpret_cast<uint32_t*>(ws), w_static, stream,
-                                           d));
+        return from_cuda(small_m(deq, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                 w_global_scale, gx, (int)N, y, ybf,
+                                 reinterpret_cast<uint32_t*>(ws), w_static, stream, d));
     return from_cuda(launch_gemm_w4a4(ws + L.xq, ws + L.xs, gx, (int)M, (int)K, w_packed,
                                       w_scales_swizzled, w_global_scale, (int)N, y, ybf,
                                       reinterpret_cast<uint32_t*>(ws), ws + L.sk, stream, d));

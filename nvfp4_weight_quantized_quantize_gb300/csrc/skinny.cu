@@ -402,6 +402,14 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
 
 }  // namespace
 
+bool skinny_w4a16_takes(int K, const DevInfo& dev) {
+    const int rowchunks = K / 32;
+    const int cg = (rowchunks + 3) / 4 <= kSkMaxGroups ? 4 : 8;  // chunks per warp (U = 1, 2)
+    const int ngroups = (rowchunks + cg - 1) / cg;
+    if (ngroups > kSkMaxGroups) return false;
+    return sk_smem(K, ngroups, 2, 1) + 2048 <= dev.smem_optin;  // the smallest ring
+}
+
 cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                                 const uint8_t* wrm, const float* gw, const float* gx, int N,
                                 void* y, bool y_bf16, uint32_t* err, bool w_static,

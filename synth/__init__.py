@@ -125,6 +125,18 @@ def random_fp8_block128(rows: int, cols: int, seed: int, kind: str = "normal"):
     return q.numpy().copy(), s.numpy().copy()
 
 
+def random_nvfp4_weights(N: int, K: int, seed: int):
+    """Already-encoded NVFP4 weights drawn directly (no quantizer involved): packed codes
+    uint8 [N, K/2] with every nibble uniform over the 16 codes, E4M3 scale bytes uint8
+    [N, K/16] uniform over 0x10 .. 0x5F (normal values 2^-5 .. 2^4 * 1.875), and a global
+    scale 2^-8.  For linear tests at sizes where quantizing a float tensor on the CPU
+    would take too long."""
+    rng = np.random.default_rng(seed)
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scales = rng.integers(0x10, 0x60, (N, K // 16), dtype=np.uint8)
+    return packed, scales, 2.0 ** -8
+
+
 def random_w(N: int, K: int, seed: int, std: float = 0.02) -> torch.Tensor:
     gen = torch.Generator(device="cpu").manual_seed(seed)
     return torch.randn(N, K, generator=gen, dtype=torch.float32) * std
