@@ -458,6 +458,47 @@ def measure_rows(torch, nv, setup):
             "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
             "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4)}
         del cps, p, z
+    # the fused MLP activation on a 512-token chunk: silu(gate) * up -> NVFP4 from the
+    # gate/up output [512, 34816] (5 rotating copies, 178 MB > L2), dynamic and static g;
+    # then the down projection on those NVFP4 activations (K 17408, N 5120, 3 weight
+    # copies, 150 MB)
+    from synth import random_gate_up
+    Mf, If = 512, 17408
+    gus = [random_gate_up(Mf, If, 50).cuda()]
+    gus += [gus[0].clone() for _ in range(4)]
+    hq = torch.empty(Mf, If // 2, dtype=torch.uint8, device="cuda")
+    hs = torch.empty((Mf + 127) // 128 * 128 * ((If // 16 + 3) // 4 * 4), dtype=torch.uint8,
+                     device="cuda")
+    hg = torch.empty(1, dtype=torch.float32, device="cuda")
+    hws = torch.empty(nv.nvfp4_workspace_bytes(0, Mf, If), dtype=torch.uint8, device="cuda")
+    hb = Mf * 2 * If * 2 + Mf * If // 2 + Mf * If // 16 + 4
+    ms = time_graph(torch, lambda i: nv.nvfp4_silu_mul_quantize(gus[i % 5], hq, hs, hg,
+                                                                workspace=hws), 10, 5)
+    rows["f1_silu_mul_quant_dynamic_%dx%d" % (Mf, If)] = {"GB/s": round(hb / ms / 1e6, 1),
+                                                          "us": round(ms * 1e3, 1)}
+    gstat = torch.tensor([0.01], dtype=torch.float32, device="cuda")
+    hg2 = torch.empty(1, dtype=torch.float32, device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_silu_mul_quantize(gus[i % 5], hq, hs, hg2, gstat),
+                    10, 5)
+    rows["f1_silu_mul_quant_static_%dx%d" % (Mf, If)] = {"GB/s": round(hb / ms / 1e6, 1),
+                                                         "us": round(ms * 1e3, 1)}
+    del gus
+    nv.nvfp4_silu_mul_quantize(random_gate_up(Mf, If, 51).cuda(), hq, hs, hg, workspace=hws)
+    wl = WORKLOADS["prefill_b"]
+    _, w = workload_inputs("prefill_b")
+    p, _, z, gg = nv.quantize_weight(w.cuda())
+    del w
+    cps = [(p, z)] + [(p.clone(), z.clone()) for _ in range(2)]
+    y = torch.empty(Mf, wl.N, dtype=torch.bfloat16, device="cuda")
+    wsv = torch.zeros(nv.nvfp4_workspace_bytes(1, Mf, If, wl.N, nv.NVFP4_W4A4),
+                      dtype=torch.uint8, device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_linear_nvfp4_x(hq, hs, hg, cps[i % 3][0],
+                                                             cps[i % 3][1], gg, y, wsv), 6, 5)
+    tf = 2.0 * Mf * wl.N * If / (ms * 1e-3) / 1e12
+    rows["f1_down_proj_nvfp4_x_M%d_K%d_N%d" % (Mf, If, wl.N)] = {
+        "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
+        "frac_fp4_nominal": round(tf / FP4_NOMINAL_TFLOPS, 4)}
+    del cps, p, z
     # a6 activation quantization (bf16 x 2048 x 5120) and a7 the W4A4 block-scaled GEMM
     # (the call quantizes x itself, so its time includes a6)
     wl = WORKLOADS["w4a4"]

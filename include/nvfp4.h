@@ -224,6 +224,64 @@ nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K, const uint8_t* w_
                           const float* x_global_scale, void* workspace,
                           size_t workspace_bytes, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_silu_mul_quantize -- NVFP4 activations of silu(gate) * up, fused.
+ *
+ * Defines: the activation step between the fused gate/up projection and the down
+ * projection (FlashRT docs/qwen36_usage.md, env-var table: FLASHRT_QWEN36_FUSE_MLP_GATE_UP,
+ * FLASHRT_QWEN36_FUSE_SILU_MUL_QUANT).  The pages name the fusion without its arithmetic;
+ * the reading taken here:
+ *   h[m][i] = (g / (1 + exp(-g))) * u,  g = gate_up[m][i], u = gate_up[m][I + i],
+ * each step one fp32 round-to-nearest-even operation, with exp a fixed fp32 sequence
+ * (Cody-Waite reduction, Taylor series to the 7th power; exp(x) = +inf above 88 and 0
+ * below -87), so that the codes are reproducible bit for bit.  h stays in registers and
+ * is quantized as nvfp4_quantize quantizes an fp32 source (with the given global scale
+ * when there is one), the scales going straight to the tensor-core atom layout.
+ * Arguments:
+ *   gate_up         bf16 [M, 2I] row-major: gate in columns [0, I), up in [I, 2I).
+ *   M, I            M >= 1, I >= 16, I % 16 == 0 (I % 32 == 0 to feed nvfp4_linear_nvfp4_x).
+ *   packed          out [M, I/2] bytes.
+ *   scales_swizzled out, the atom part of the nvfp4_repack layout for an [M, I] tensor:
+ *                   ceil(M/128)*128 * ceil(I/64)*4 bytes (scales_bytes at least that);
+ *                   padding rows and blocks are written as zero.
+ *   global_scale    out, g (device); a copy of *given_global_scale when that is given.
+ *   given_global_scale  NULL: g = amax|h| / 2688 (two kernels, h computed twice);
+ *                   else a static activation scale (device, finite, > 0; one kernel).
+ *   workspace       >= nvfp4_workspace_bytes(0, M, I, 0, 0) bytes when g is dynamic;
+ *                   may be NULL with a given scale.
+ * Alignment: gate_up, packed, scales_swizzled, workspace 16 bytes; the scales 4 bytes.
+ * Non-finite gate/up values give unspecified codes.
+ */
+nvfp4_status nvfp4_silu_mul_quantize(const void* gate_up, int64_t M, int64_t I,
+                                     uint8_t* packed, uint8_t* scales_swizzled,
+                                     size_t scales_bytes, float* global_scale,
+                                     const float* given_global_scale, void* workspace,
+                                     size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_linear_nvfp4_x -- y = x . W^T with x already in NVFP4 (the down projection fed
+ * by nvfp4_silu_mul_quantize).
+ *
+ *   y[m,n] = g_x * g_w * sum_k e2m1(qx[m,k]) e4m3(sx[m,k/16]) e2m1(qw[n,k]) e4m3(sw[n,k/16])
+ * Arguments:
+ *   x_packed           [M, K/2] codes; x_scales_swizzled the atom layout of an [M, K]
+ *                      tensor (as nvfp4_silu_mul_quantize writes it); x_global_scale g_x
+ *                      (device).
+ *   w_*, N, y, y_dtype as for nvfp4_linear.
+ *   flags              0 or NVFP4_STATIC_WEIGHTS.
+ *   workspace          >= nvfp4_workspace_bytes(1, M, K, N, NVFP4_W4A4) bytes, first
+ *                      4 bytes the error word.
+ * M > 16 runs the block-scaled tensor-core GEMM on x's codes and scales directly;
+ * M <= 16 writes x's exact bf16 value e2m1 * e4m3 into the workspace and runs the
+ * small-M W4A16 kernels with g_x folded into the output scale.
+ */
+nvfp4_status nvfp4_linear_nvfp4_x(const uint8_t* x_packed, const uint8_t* x_scales_swizzled,
+                                  const float* x_global_scale, int64_t M, int64_t K,
+                                  const uint8_t* w_packed, const uint8_t* w_scales_swizzled,
+                                  const float* w_global_scale, int64_t N, void* y,
+                                  nvfp4_dtype y_dtype, int flags, void* workspace,
+                                  size_t workspace_bytes, nvfp4_stream_t stream);
+
 /* ---- host-only helpers: no device work ---------------------------------------- */
 
 /* Bytes of the swizzled scale layout for a [rows, cols] tensor (0 on bad sizes). */

@@ -29,7 +29,8 @@ STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ER
 EXPORTS = ("nvfp4_quantize", "nvfp4_repack", "nvfp4_linear", "nvfp4_repack_bytes",
            "nvfp4_workspace_bytes", "nvfp4_w4a4_workspace_layout", "nvfp4_workspace_error",
            "nvfp4_status_str", "nvfp4_encode_elements", "nvfp4_quantize_noalloc",
-           "nvfp4_last_cuda_error", "nvfp4_quantize_fp8_block128")
+           "nvfp4_last_cuda_error", "nvfp4_quantize_fp8_block128", "nvfp4_silu_mul_quantize",
+           "nvfp4_linear_nvfp4_x")
 
 
 class Nvfp4Error(RuntimeError):
@@ -65,6 +66,8 @@ def load(path: str = LIB_PATH):
         "nvfp4_quantize_noalloc": (I, [P, I, I64, I64, P, P, P, P]),
         "nvfp4_last_cuda_error": (ctypes.c_char_p, []),
         "nvfp4_quantize_fp8_block128": (I, [P, P, I64, I64, P, P, P, P, SZ, P]),
+        "nvfp4_silu_mul_quantize": (I, [P, I64, I64, P, P, SZ, P, P, P, SZ, P]),
+        "nvfp4_linear_nvfp4_x": (I, [P, P, P, I64, I64, P, P, P, I64, P, I, I, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -194,6 +197,40 @@ def nvfp4_linear(x: torch.Tensor, w_packed: torch.Tensor, w_scales_swizzled: tor
                              _p(w_global_scale), N, _p(y), _dtype_code(y.dtype), m,
                              _p(x_global_scale), _p(workspace), wsb, _stream(stream))
     _check(st, "nvfp4_linear")
+
+
+def nvfp4_silu_mul_quantize(gate_up: torch.Tensor, packed: torch.Tensor,
+                            scales_swizzled: torch.Tensor, global_scale: torch.Tensor,
+                            given_global_scale: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, stream=None) -> None:
+    """bf16 gate_up [M, 2I] (gate, then up) -> NVFP4 codes of silu(gate) * up, scale atoms
+    and the global scale (dynamic, or a copy of the given static one)."""
+    M, I2 = gate_up.shape
+    if gate_up.dtype != torch.bfloat16 or I2 % 2:
+        raise ValueError("gate_up must be bf16 [M, 2I]")
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().nvfp4_silu_mul_quantize(_p(gate_up), M, I2 // 2, _p(packed), _p(scales_swizzled),
+                                        scales_swizzled.numel() * scales_swizzled.element_size(),
+                                        _p(global_scale), _p(given_global_scale), _p(workspace),
+                                        wsb, _stream(stream))
+    _check(st, "nvfp4_silu_mul_quantize")
+
+
+def nvfp4_linear_nvfp4_x(x_packed: torch.Tensor, x_scales_swizzled: torch.Tensor,
+                         x_global_scale: torch.Tensor, w_packed: torch.Tensor,
+                         w_scales_swizzled: torch.Tensor, w_global_scale: torch.Tensor,
+                         y: torch.Tensor, workspace: torch.Tensor, stream=None,
+                         static_weights: bool = False) -> None:
+    """y = x . W^T with NVFP4 x (codes [M, K/2], scale atoms, g_x)."""
+    M, K = x_packed.shape[0], x_packed.shape[1] * 2
+    N = w_packed.shape[0]
+    st = load().nvfp4_linear_nvfp4_x(_p(x_packed), _p(x_scales_swizzled), _p(x_global_scale), M,
+                                     K, _p(w_packed), _p(w_scales_swizzled), _p(w_global_scale),
+                                     N, _p(y), _dtype_code(y.dtype),
+                                     NVFP4_STATIC_WEIGHTS if static_weights else 0,
+                                     _p(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
+    _check(st, "nvfp4_linear_nvfp4_x")
 
 
 def nvfp4_encode_elements(inp: torch.Tensor, e2m1_out: torch.Tensor | None,

@@ -131,6 +131,31 @@ __device__ __forceinline__ uint32_t quantize_block16(const float (&t)[16], float
     return s8;
 }
 
+// Global scale seen by every CTA: *given_g, or amax / 2688 from the partials.
+__device__ __forceinline__ float cta_global_scale(const float* __restrict__ given_g,
+                                                  const float* __restrict__ partials,
+                                                  int npartials) {
+    __shared__ float g_sh;
+    if (given_g) {
+        if (threadIdx.x == 0) g_sh = *given_g;
+    } else {
+        float m = 0.0f;
+        for (int i = threadIdx.x; i < npartials; i += blockDim.x) m = fmaxf(m, partials[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        __shared__ float red[32];
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float r = red[0];
+            for (int i = 1; i < (int)(blockDim.x / 32); ++i) r = fmaxf(r, red[i]);
+            g_sh = global_scale_from_amax(r);
+        }
+    }
+    __syncthreads();
+    return g_sh;
+}
+
 // ---- swizzled scale layout ---------------------------------------------------------
 // Tensor-core block-scale layout for 16-element blocks: 512-byte atoms of 128 rows x 4
 // scale columns; line (r % 32) of 16 bytes holds rows r%32 + {0,32,64,96}, 4 bytes each;

@@ -35,6 +35,18 @@ cudaError_t launch_quantize_fp8_b128(const uint8_t* src, const float* block_scal
                                      uint8_t* scales, float* g_out, float* partials,
                                      int npartials, cudaStream_t stream, const DevInfo& dev);
 
+// h = silu(gate) * up from bf16 gate_up [M, 2I] (gate columns [0, I)), quantized to NVFP4:
+// codes [M, I/2], scales in the tensor-core atoms (rows padded to 128, blocks to 4, zero
+// padding), g_out.  Pass 1 (amax partials) only when given_g is null.
+cudaError_t launch_silu_mul_quantize(const uint16_t* gate_up, int64_t M, int64_t I,
+                                     uint8_t* packed, uint8_t* scales, float* g_out,
+                                     const float* given_g, float* partials, int npartials,
+                                     cudaStream_t stream, const DevInfo& dev);
+
+// NVFP4 activations (codes [M, K/2], scale atoms) -> bf16 e2m1 * e4m3 [M, K] (exact).
+cudaError_t launch_dequant_x(const uint8_t* xq, const uint8_t* xs, int64_t M, int64_t K,
+                             uint16_t* out, cudaStream_t stream, const DevInfo& dev);
+
 cudaError_t launch_repack(const uint8_t* scales, int64_t rows, int64_t cols, uint8_t* out,
                           cudaStream_t stream, const DevInfo& dev);
 

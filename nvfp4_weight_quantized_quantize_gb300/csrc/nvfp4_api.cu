@@ -300,6 +300,76 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
                                       reinterpret_cast<uint32_t*>(ws), ws + L.sk, stream, d));
 }
 
+NVFP4_API nvfp4_status nvfp4_silu_mul_quantize(const void* gate_up, int64_t M, int64_t I,
+                                               uint8_t* packed, uint8_t* scales_swizzled,
+                                               size_t scales_bytes, float* global_scale,
+                                               const float* given_global_scale,
+                                               void* workspace, size_t workspace_bytes,
+                                               nvfp4_stream_t stream) {
+    if (!gate_up || !packed || !scales_swizzled || !global_scale) return NVFP4_ERR_NULL;
+    if (!given_global_scale && !workspace) return NVFP4_ERR_NULL;
+    if (M < 1 || I < 16 || I % 16 != 0 || M > kMaxDim || I > kMaxDim) return NVFP4_ERR_SHAPE;
+    if (scales_bytes < repack_atom_bytes(M, I)) return NVFP4_ERR_SHAPE;
+    if (!aligned(gate_up, 16) || !aligned(packed, 16) || !aligned(scales_swizzled, 16) ||
+        !aligned(global_scale, 4) || (given_global_scale && !aligned(given_global_scale, 4)) ||
+        (workspace && !aligned(workspace, 16)))
+        return NVFP4_ERR_ALIGN;
+    if (!given_global_scale && workspace_bytes < nvfp4_workspace_bytes(0, M, I, 0, NVFP4_W4A16))
+        return NVFP4_ERR_WORKSPACE;
+    DevInfo d;
+    nvfp4_status st = current_device(&d);
+    if (st != NVFP4_OK) return st;
+    float* partials = workspace ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                                           kHeaderBytes)
+                                : nullptr;
+    return from_cuda(launch_silu_mul_quantize(static_cast<const uint16_t*>(gate_up), M, I,
+                                              packed, scales_swizzled, global_scale,
+                                              given_global_scale, partials,
+                                              partial_count(M * I, d), stream, d));
+}
+
+NVFP4_API nvfp4_status nvfp4_linear_nvfp4_x(const uint8_t* x_packed,
+                                            const uint8_t* x_scales_swizzled,
+                                            const float* x_global_scale, int64_t M, int64_t K,
+                                            const uint8_t* w_packed,
+                                            const uint8_t* w_scales_swizzled,
+                                            const float* w_global_scale, int64_t N, void* y,
+                                            nvfp4_dtype y_dtype, int flags, void* workspace,
+                                            size_t workspace_bytes, nvfp4_stream_t stream) {
+    if (!x_packed || !x_scales_swizzled || !x_global_scale || !w_packed || !w_scales_swizzled ||
+        !w_global_scale || !y || !workspace)
+        return NVFP4_ERR_NULL;
+    if (y_dtype != NVFP4_F32 && y_dtype != NVFP4_BF16) return NVFP4_ERR_DTYPE;
+    if (flags & ~NVFP4_STATIC_WEIGHTS) return NVFP4_ERR_DTYPE;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return NVFP4_ERR_SHAPE;
+    if (!aligned(x_packed, 16) || !aligned(x_scales_swizzled, 16) || !aligned(w_packed, 16) ||
+        !aligned(w_scales_swizzled, 16) || !aligned(y, 16) || !aligned(workspace, 16) ||
+        !aligned(x_global_scale, 4) || !aligned(w_global_scale, 4))
+        return NVFP4_ERR_ALIGN;
+    if (workspace_bytes < nvfp4_workspace_bytes(1, M, K, N, NVFP4_W4A4))
+        return NVFP4_ERR_WORKSPACE;
+    DevInfo d;
+    nvfp4_status st = current_device(&d);
+    if (st != NVFP4_OK) return st;
+    const bool ybf = y_dtype == NVFP4_BF16;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const W4A4Layout L = w4a4_layout(M, K, N);
+    if (M <= kGemvMaxM) {
+        uint16_t* deq = reinterpret_cast<uint16_t*>(ws + L.deq);
+        cudaError_t e = launch_dequant_x(x_packed, x_scales_swizzled, M, K, deq, stream, d);
+        if (e != cudaSuccess) return from_cuda(e);
+        return from_cuda(small_m(deq, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                 w_global_scale, x_global_scale, (int)N, y, ybf,
+                                 reinterpret_cast<uint32_t*>(ws),
+                                 (flags & NVFP4_STATIC_WEIGHTS) != 0, stream, d));
+    }
+    return from_cuda(launch_gemm_w4a4(x_packed, x_scales_swizzled, x_global_scale, (int)M,
+                                      (int)K, w_packed, w_scales_swizzled, w_global_scale,
+                                      (int)N, y, ybf, reinterpret_cast<uint32_t*>(ws), ws + L.sk,
+                                      stream, d));
+}
+
 NVFP4_API nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t* e2m1_out,
                                              uint8_t* e4m3_out, nvfp4_stream_t stream) {
     if (!in && n > 0) return NVFP4_ERR_NULL;

@@ -20,6 +20,9 @@ How each function is pinned (tests/test_oracle_*):
                              two that expose the tile index, every byte against the
                              E4M3 closed form, torch's float8_e4m3fn decode and bf16
                              cast on random data.
+  exp_f32 / silu_mul         exp within 3 ulp of fp64 exp over a dense sweep, exact at 0
+                             and the clamps; silu * up within a few ulp of the fp64
+                             definition; zero, saturated and signed-zero cases.
   repack                     hand-derived byte offsets, bijection, zero padding; the
                              tensor-core W4A4 result on the GPU reads the same layout.
   linear_w4a16 / _w4a4       exact rational brute force on tiny shapes, one-hot and
@@ -98,6 +101,9 @@ def _load():
                                                      F, I64, P, P, I64, P, P]),
             "orc_num_threads": (ctypes.c_int, []),
             "orc_dequant_fp8_block128": (None, [P, P, I64, I64, P]),
+            "orc_exp_f32": (F, [F]),
+            "orc_silu_mul_f32": (F, [F, F]),
+            "orc_silu_mul": (None, [P, I64, I64, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -206,6 +212,30 @@ def dequant_fp8_block128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
 def quantize_fp8_block128(q: np.ndarray, s: np.ndarray):
     """FP8 block-128 weights -> BF16 -> NVFP4 (R10, then R1-R9): (packed, scales, g)."""
     return quantize(dequant_fp8_block128(q, s))
+
+
+def exp_f32(x: float) -> float:
+    """R11's fp32 exp (Cody-Waite reduction, degree-7 Taylor polynomial)."""
+    return float(_load().orc_exp_f32(float(x)))
+
+
+def silu_mul_f32(g: float, u: float) -> float:
+    return float(_load().orc_silu_mul_f32(float(g), float(u)))
+
+
+def silu_mul(gate_up) -> np.ndarray:
+    """R11: bf16 gate_up [M, 2I] (torch bf16 or uint16 bits) -> fp32 h [M, I]."""
+    a = _bf16_bits(gate_up)
+    M, I2 = a.shape
+    assert I2 % 2 == 0
+    h = np.empty((M, I2 // 2), dtype=np.float32)
+    _load().orc_silu_mul(_ptr(a), M, I2 // 2, _ptr(h))
+    return h
+
+
+def silu_mul_quantize(gate_up, global_scale: float | None = None):
+    """R11 then R1-R9: (packed [M, I/2], scales [M, I/16] row-major, g)."""
+    return quantize(silu_mul(gate_up), global_scale)
 
 
 def repack_bytes(rows: int, cols: int) -> int:

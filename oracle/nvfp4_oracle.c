@@ -55,6 +55,14 @@
  *       tile, stored [ceil(R/128), ceil(C/128)] row-major, which multiplies the E4M3
  *       value; the product is one fp32 round-to-nearest-even multiply, then rounded
  *       to bf16 (nearest even), and the bf16 tensor is quantized by R1-R9.
+ *   R11 fused silu(gate) * up -> NVFP4 activations (FlashRT docs/qwen36_usage.md,
+ *       env-var table, FLASHRT_QWEN36_FUSE_SILU_MUL_QUANT, after the fused gate/up GEMM
+ *       of FLASHRT_QWEN36_FUSE_MLP_GATE_UP): the GEMM's bf16 output [M, 2I] holds gate
+ *       in columns [0, I) and up in [I, 2I); h = (g / (1 + exp(-g))) * u in fp32, one
+ *       correctly rounded operation per step, and the fp32 h goes straight to R1-R9
+ *       (no bf16 copy in between: the fusion keeps h in registers).  exp is the fp32
+ *       method of orc_exp_f32 below, the same steps on both sides, because the E2M1
+ *       and E4M3 roundings of h hang on its last bit.
  *
  * Built with strict IEEE semantics (-O2 -ffp-contract=off, no fast-math): every
  * fp32 operation below is one correctly rounded operation.
@@ -261,6 +269,61 @@ ORC_EXPORT int orc_quantize(const void* src, int src_is_bf16, int64_t rows, int6
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Fused silu(gate) * up activations (R11)                                   */
+/* ------------------------------------------------------------------------- */
+
+/* exp(x) in fp32 by W. J. Cody and W. Waite's argument reduction ("Software Manual
+ * for the Elementary Functions", 1980): n = rint(x * log2(e)), r = x - n * ln2 with ln2
+ * split into a 16-bit head (so n * head is exact) and a tail, then e^r from its Taylor
+ * series to r^7 (|r| <= ln2/2 + a little: the next term is below 2^-27 relative),
+ * evaluated by Horner's rule with fused multiply-adds, times 2^n.  Inputs are clamped
+ * first: x > 88 gives +inf and x < -87 gives 0 (n then stays in [-126, 127], so 2^n is
+ * a normal float and the last multiply is one correctly rounded operation).  Every
+ * step is one fp32 operation in this order; the kernels take the same steps. */
+ORC_EXPORT float orc_exp_f32(float x) {
+    /* fp32 constants, written as hexadecimal floats: log2(e) and ln 2 rounded to
+     * nearest; the head of ln 2 keeps 16 significant bits, the tail is ln 2 - head
+     * rounded to nearest; the Taylor coefficients 1/k! rounded to nearest */
+    const float log2e = 0x1.715476p+0f;
+    const float ln2_hi = 0x1.62e4p-1f;
+    const float ln2_lo = 0x1.7f7d1cp-20f;
+    float n, r, p, two_n;
+    uint32_t bits;
+    if (x > 88.0f) return INFINITY;
+    if (x < -87.0f) return 0.0f;
+    n = rintf(x * log2e);
+    r = fmaf(-n, ln2_hi, x);
+    r = fmaf(-n, ln2_lo, r);
+    p = 0x1.a01a02p-13f;            /* 1/5040 */
+    p = fmaf(p, r, 0x1.6c16c2p-10f); /* 1/720 */
+    p = fmaf(p, r, 0x1.111112p-7f);  /* 1/120 */
+    p = fmaf(p, r, 0x1.555556p-5f);  /* 1/24 */
+    p = fmaf(p, r, 0x1.555556p-3f);  /* 1/6 */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    bits = (uint32_t)((int32_t)n + 127) << 23;
+    memcpy(&two_n, &bits, 4);
+    return p * two_n;
+}
+
+/* h = silu(g) * u = (g / (1 + exp(-g))) * u, each step one fp32 RN operation. */
+ORC_EXPORT float orc_silu_mul_f32(float g, float u) {
+    const float e = orc_exp_f32(-g);
+    const float den = 1.0f + e;
+    const float sg = g / den;
+    return sg * u;
+}
+
+/* R11: gate_up bf16 [M, 2I] (gate columns [0, I), up [I, 2I)) -> h fp32 [M, I]. */
+ORC_EXPORT void orc_silu_mul(const uint16_t* gate_up, int64_t M, int64_t I, float* h) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t i = 0; i < I; ++i)
+            h[m * I + i] = orc_silu_mul_f32(orc_bf16_to_f32(gate_up[m * 2 * I + i]),
+                                            orc_bf16_to_f32(gate_up[m * 2 * I + I + i]));
 }
 
 /* ------------------------------------------------------------------------- */

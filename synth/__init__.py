@@ -125,6 +125,16 @@ def random_fp8_block128(rows: int, cols: int, seed: int, kind: str = "normal"):
     return q.numpy().copy(), s.numpy().copy()
 
 
+def random_gate_up(M: int, I: int, seed: int) -> torch.Tensor:
+    """Output of a fused gate/up projection, bf16 [M, 2I]: gate ~ N(0, 3) in columns
+    [0, I) (pre-activations reaching well into both tails of silu), up ~ N(0, 1) in
+    [I, 2I)."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    gate = torch.randn(M, I, generator=gen, dtype=torch.float32) * 3.0
+    up = torch.randn(M, I, generator=gen, dtype=torch.float32)
+    return torch.cat([gate, up], dim=1).to(torch.bfloat16)
+
+
 def random_nvfp4_weights(N: int, K: int, seed: int):
     """Already-encoded NVFP4 weights drawn directly (no quantizer involved): packed codes
     uint8 [N, K/2] with every nibble uniform over the 16 codes, E4M3 scale bytes uint8

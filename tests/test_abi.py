@@ -105,6 +105,45 @@ def test_quantize_fp8_block128_rejects(lib):
     assert _q8(lib, wsb=16) == WORKSPACE
 
 
+def _sq(lib, gu=16, M=4, I=32, packed=32, sc=48, scb=512, g=64, given=None, ws=4096,
+        wsb=1 << 20):
+    v = lambda a: None if a is None else ctypes.c_void_p(a)
+    return lib.nvfp4_silu_mul_quantize(v(gu), M, I, v(packed), v(sc), scb, v(g), v(given),
+                                       v(ws), wsb, None)
+
+
+def test_silu_mul_quantize_rejects(lib):
+    assert _sq(lib, gu=None) == NULL
+    assert _sq(lib, g=None) == NULL
+    assert _sq(lib, ws=None) == NULL            # dynamic scale needs the workspace
+    assert _sq(lib, I=24) == SHAPE
+    assert _sq(lib, M=0) == SHAPE
+    assert _sq(lib, scb=511) == SHAPE           # 128 rows x 4 blocks of atoms
+    assert _sq(lib, gu=24) == ALIGN
+    assert _sq(lib, given=66, ws=None) == ALIGN
+    assert _sq(lib, wsb=16) == WORKSPACE
+
+
+def _lx(lib, xq=16, xs=32, gx=48, M=4, K=64, wq=64, wsz=80, gw=96, N=8, y=112, ydt=1, flags=0,
+        ws=4096, wsb=1 << 20):
+    v = lambda a: None if a is None else ctypes.c_void_p(a)
+    return lib.nvfp4_linear_nvfp4_x(v(xq), v(xs), v(gx), M, K, v(wq), v(wsz), v(gw), N, v(y),
+                                    ydt, flags, v(ws), wsb, None)
+
+
+def test_linear_nvfp4_x_rejects(lib):
+    assert _lx(lib, xq=None) == NULL
+    assert _lx(lib, gx=None) == NULL
+    assert _lx(lib, ws=None) == NULL
+    assert _lx(lib, ydt=3) == DTYPE
+    assert _lx(lib, flags=1) == DTYPE
+    assert _lx(lib, K=48) == SHAPE
+    assert _lx(lib, N=0) == SHAPE
+    assert _lx(lib, xs=40) == ALIGN
+    assert _lx(lib, gx=50) == ALIGN
+    assert _lx(lib, wsb=64) == WORKSPACE
+
+
 def _r(lib, src=16, rows=4, cols=32, out=32, nbytes=None):
     v = lambda a: None if a is None else ctypes.c_void_p(a)
     if nbytes is None:
