@@ -627,6 +627,45 @@ def run_one_workload(name: str, calls: int = 3):
 
     build_lib.build()
     nv.load()
+    if name == "fp8_requant":
+        # FP8 block-128 -> NVFP4 on the decode_a shape (17408 x 5120)
+        from synth import random_fp8_block128
+        q8, s8 = random_fp8_block128(17408, 5120, 1)
+        q8d, s8d = torch.from_numpy(q8).cuda(), torch.from_numpy(s8).cuda()
+        packed = torch.empty(17408, 2560, dtype=torch.uint8, device="cuda")
+        scales = torch.empty(17408, 320, dtype=torch.uint8, device="cuda")
+        g = torch.empty(1, dtype=torch.float32, device="cuda")
+        ws = torch.empty(nv.nvfp4_workspace_bytes(0, 17408, 5120), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(calls):
+            nv.nvfp4_quantize_fp8_block128(q8d, s8d, packed, scales, g, ws)
+        torch.cuda.synchronize()
+        print("ran %d calls of %s" % (calls, name), flush=True)
+        return
+    if name == "mlp_act":
+        # the 512-token MLP chunk: silu(gate) * up -> NVFP4 (dynamic g), then the down
+        # projection (K 17408, N 5120) on those activations
+        from synth import random_gate_up
+        M, I, N = 512, 17408, 5120
+        gu = random_gate_up(M, I, 50).cuda()
+        hq = torch.empty(M, I // 2, dtype=torch.uint8, device="cuda")
+        hs = torch.empty((M + 127) // 128 * 128 * ((I // 16 + 3) // 4 * 4), dtype=torch.uint8,
+                         device="cuda")
+        hg = torch.empty(1, dtype=torch.float32, device="cuda")
+        hws = torch.empty(nv.nvfp4_workspace_bytes(0, M, I), dtype=torch.uint8, device="cuda")
+        _, w = workload_inputs("prefill_b")
+        packed, _, swz, g = nv.quantize_weight(w.cuda())
+        del w
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        work = torch.zeros(nv.nvfp4_workspace_bytes(1, M, I, N, nv.NVFP4_W4A4),
+                           dtype=torch.uint8, device="cuda")
+        for _ in range(calls):
+            nv.nvfp4_silu_mul_quantize(gu, hq, hs, hg, workspace=hws)
+            nv.nvfp4_linear_nvfp4_x(hq, hs, hg, packed, swz, g, y, work)
+        torch.cuda.synchronize()
+        assert nv.nvfp4_workspace_error(work) == 0
+        print("ran %d calls of %s" % (calls, name), flush=True)
+        return
     wl = WORKLOADS[name]
     x, w = workload_inputs(name)
     packed, _, swz, g = nv.quantize_weight(w.cuda())
@@ -659,7 +698,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only-workload", default=None,
-                    help="run a few calls of one workload and exit (for ncu captures)")
+                    help="run a few calls of one workload and exit (for ncu captures): a "
+                         "workload name, fp8_requant or mlp_act")
     args = ap.parse_args()
     global STATIC_W
     STATIC_W = bool(args.static_weights)
