@@ -57,7 +57,7 @@ constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
-constexpr uint32_t kNumBars = 3 * kStages + 4 + 1;
+constexpr uint32_t kNumBars = 4 * kStages + 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
@@ -89,6 +89,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
     auto accempty = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
     const uint32_t drain = bar0 + 8u * (2 * kStages + 4);
     auto sfull = [&](int s) { return bar0 + 8u * (2 * kStages + 5 + s); };
+    auto sland = [&](int s) { return bar0 + 8u * (3 * kStages + 5 + s); };  // scales landed
     auto bar_ptr = [&](uint32_t a) { return reinterpret_cast<uint64_t*>(base + (a - base_s)); };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
@@ -105,6 +106,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
         mbar_init(bar_ptr(drain), 1);
         for (int s = 0; s < kStages; ++s) mbar_init(bar_ptr(sfull(s)), 4);
+        for (int s = 0; s < kStages; ++s) mbar_init(bar_ptr(sland(s)), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -134,28 +136,32 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     // x rows of the tile: scale row blocks 2 mb and 2 mb + 1 (the second one
                     // only when it exists; rows past M are masked in the epilogue)
                     const bool two = 2 * mb + 1 < x_row_blocks;
-                    mbar_arrive_expect_tx(bar_ptr(full(s)),
-                                          kABytes + kBBytes + sfb * (two ? 3u : 2u));
+                    // the scale atoms first, on their own barrier: the scale writers move
+                    // them into TMEM while the code boxes are still landing
+                    mbar_arrive_expect_tx(bar_ptr(sland(s)), sfb * (two ? 3u : 2u));
+                    bulk_g2s(base + kOffSfa + s * kSfaBytes,
+                             wsz + ((size_t)nb * natoms_row + 4 * kb) * kAtomBytes, sfb,
+                             bar_ptr(sland(s)));
+                    bulk_g2s(base + kOffSfb + s * kSfbBytes,
+                             xsz + ((size_t)(2 * mb) * natoms_row + 4 * kb) * kAtomBytes, sfb,
+                             bar_ptr(sland(s)));
+                    if (two)
+                        bulk_g2s(base + kOffSfb + s * kSfbBytes + 4 * kAtomBytes,
+                                 xsz + ((size_t)(2 * mb + 1) * natoms_row + 4 * kb) * kAtomBytes,
+                                 sfb, bar_ptr(sland(s)));
+                    mbar_arrive_expect_tx(bar_ptr(full(s)), kABytes + kBBytes);
                     tc::tma_load_2d(base_s + kOffA + s * kABytes, &tmap_w, kb * (kBK / 2),
                                     nb * kBN, full(s));
                     tc::tma_load_2d(base_s + kOffB + s * kBBytes, &tmap_x, kb * (kBK / 2),
                                     mb * kBM, full(s));
-                    bulk_g2s(base + kOffSfa + s * kSfaBytes,
-                             wsz + ((size_t)nb * natoms_row + 4 * kb) * kAtomBytes, sfb,
-                             bar_ptr(full(s)));
-                    bulk_g2s(base + kOffSfb + s * kSfbBytes,
-                             xsz + ((size_t)(2 * mb) * natoms_row + 4 * kb) * kAtomBytes, sfb,
-                             bar_ptr(full(s)));
-                    if (two)
-                        bulk_g2s(base + kOffSfb + s * kSfbBytes + 4 * kAtomBytes,
-                                 xsz + ((size_t)(2 * mb + 1) * natoms_row + 4 * kb) * kAtomBytes,
-                                 sfb, bar_ptr(full(s)));
                     issued = it + 1;
                 }
             }
             // every copy issued has landed before the CTA moves on to exit
-            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
+                mbar_wait_bounded(bar_ptr(sland(i % kStages)), (i / kStages) & 1, kWaitLimitNs);
                 mbar_wait_bounded(bar_ptr(full(i % kStages)), (i / kStages) & 1, kWaitLimitNs);
+            }
         }
     } else if (warp == 1) {
         // ---------------- MMA issue ----------------
@@ -206,7 +212,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % kStages;
                 if (!__all_sync(0xffffffffu,
-                                tc::wait_or_abort(full(s), (it / kStages) & 1, abort_flag, err))) {
+                                tc::wait_or_abort(sland(s), (it / kStages) & 1, abort_flag, err))) {
                     ok = false;
                     break;
                 }
