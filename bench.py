@@ -405,6 +405,20 @@ def measure_rows(torch, nv, setup):
         rows["a4_verify_%s_M7_K%d_N%d" % (name, wl.K, wl.N)] = {
             "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
         del cps, p, z
+    # W4A4 at decode (decode_a weights, 4 copies): a static activation scale quantizes x
+    # inside the GEMV; a dynamic one runs the amax and quantize passes first
+    sh = setup.shapes[0]
+    wsa = torch.zeros(nv.nvfp4_workspace_bytes(1, 1, sh["K"], sh["N"], nv.NVFP4_W4A4),
+                      dtype=torch.uint8, device="cuda")
+    gxs = torch.tensor([0.004], dtype=torch.float32, device="cuda")
+    for tag, gxa in (("static_fused", gxs), ("dynamic", None)):
+        ms = time_graph(torch, lambda i, gxa=gxa: nv.nvfp4_linear(
+            sh["x"], sh["copies"][i % setup.copies][0], sh["copies"][i % setup.copies][1],
+            sh["g"], sh["ys"][i % setup.copies], mode="w4a4", x_global_scale=gxa,
+            workspace=wsa, static_weights=STATIC_W), 4 * setup.copies, 50)
+        b = algo_bytes(1, sh["K"], sh["N"])
+        rows["f2_w4a4_%s_M1_K%d_N%d" % (tag, sh["K"], sh["N"])] = {
+            "GB/s": round(b / ms / 1e6, 1), "us": round(ms * 1e3, 2)}
     # the small-M curve: M = 1 .. 16 on the verify_a weights (K 5120, N 34816; 3 copies)
     wl = WORKLOADS["verify_a"]
     _, w = workload_inputs("verify_a")

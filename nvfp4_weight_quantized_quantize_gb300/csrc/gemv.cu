@@ -229,7 +229,7 @@ __host__ __device__ __forceinline__ size_t pipe_slot_bytes(int rows_max, int ngr
 
 // Each CTA releases the next launch on the stream (programmatic dependent launch) once its
 // producer has issued its last copy, so the next kernel's prologue overlaps this one's tail.
-template <int G>
+template <int G, bool kXQ>
 __global__ void __launch_bounds__(kPipeMaxThreads, 1)
 gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict__ wq,
                     const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
@@ -328,6 +328,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     for (int q = 0; q < 4; ++q)
         xv[q] = cvalid ? *reinterpret_cast<const uint4*>(x + 32 * c + 8 * q)
                        : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (kXQ) quantize_chunk_static(xv, *gx);
     float am = 0.0f, mn = __int_as_float(0x7f800000);  // max, smallest nonzero
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -344,7 +345,8 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     const int e1 = e / 2, e2 = e - e / 2;
     const float f1 = __int_as_float((e1 + 127) << 23), f2 = __int_as_float((e2 + 127) << 23);
     const float u1 = __int_as_float((127 - e1) << 23), u2 = __int_as_float((127 - e2) << 23);
-    const bool inexact = pow2_scale(mn, f1, f2) < 7.62939453125e-06f;
+    // (e2m1 * e4m3 values span less than 2^22: never inexact after the rescale)
+    const bool inexact = !kXQ && pow2_scale(mn, f1, f2) < 7.62939453125e-06f;
     const bool any_inexact = __any_sync(0xffffffffu, inexact);  // this warp's lanes
     uint32_t xh[16];                       // x'[32c .. 32c+32) as 16 fp16 pairs
 #pragma unroll
@@ -766,7 +768,7 @@ size_t pipe_smem(int K, int rows_max, int rps, int stages, int ngroups) {
            2 * (size_t)stages * 8;
 }
 
-template <int G>
+template <int G, bool kXQ>
 cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8_t* wrm,
                         const float* gw, const float* gx, int N, void* y, bool y_bf16,
                         uint32_t* err, bool w_static, cudaStream_t stream, const DevInfo& dev,
@@ -793,7 +795,7 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     const size_t smem = pipe_smem(K, rows_max, rps, stages, ngroups);
     if (smem + 2048 > dev.smem_optin) return cudaSuccess;
     static std::atomic<uint64_t> configured{0};
-    cudaError_t e = opt_in_smem(gemv_m1_pipe_kernel<G>, dev, configured);
+    cudaError_t e = opt_in_smem(gemv_m1_pipe_kernel<G, kXQ>, dev, configured);
     if (e != cudaSuccess) return e;
     // launched as a programmatic dependent: its prologue and first L2 prefetches overlap
     // the tail of the kernel before it on the stream
@@ -807,7 +809,7 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G>, x, K, wq, wrm, gw, gx, N,
+    e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G, kXQ>, x, K, wq, wrm, gw, gx, N,
                            y, y_bf16 ? 1 : 0, rows_max, rps, stages, w_static ? 1 : 0, err);
     *launched = true;
     return e != cudaSuccess ? e : cudaGetLastError();
@@ -822,13 +824,13 @@ cudaError_t launch_m1(const uint16_t* x, int K, const uint8_t* wq, const uint8_t
     bool launched = false;
     cudaError_t e = cudaSuccess;
     if (rowchunks >= 8 * 8 && (rowchunks + 7) / 8 <= 31)
-        e = launch_pipe<8>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
+        e = launch_pipe<8, false>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
                            &launched);
     else if (rowchunks >= 8 * 16 && (rowchunks + 15) / 16 <= 31)
-        e = launch_pipe<16>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
+        e = launch_pipe<16, false>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
                             &launched);
     else if (rowchunks >= 8 * 32 && (rowchunks + 31) / 32 <= 31)
-        e = launch_pipe<32>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
+        e = launch_pipe<32, false>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev,
                             &launched);
     if (e != cudaSuccess || launched) return e;
     static std::atomic<uint64_t> configured{0};
@@ -846,6 +848,30 @@ cudaError_t launch_m1(const uint16_t* x, int K, const uint8_t* wq, const uint8_t
 }
 
 }  // namespace
+
+cudaError_t launch_gemv_w4a4_static(const uint16_t* x, int M, int K, const uint8_t* wq,
+                                    const uint8_t* wsz_all, const float* gw, const float* gx,
+                                    int N, void* y, bool y_bf16, uint32_t* err, bool w_static,
+                                    cudaStream_t stream, const DevInfo& dev, bool* launched) {
+    *launched = false;
+    const int64_t atom = (int64_t)((N + 127) / 128 * 128) * ((K / 16 + 3) / 4 * 4);
+    const uint8_t* wsz = wsz_all + atom;
+    if (M >= 2)
+        return launch_skinny_w4a16(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static,
+                                   stream, dev, launched, true);
+    if (M != 1) return cudaSuccess;
+    const int rowchunks = K / 32;
+    if (rowchunks >= 8 * 8 && (rowchunks + 7) / 8 <= 31)
+        return launch_pipe<8, true>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream,
+                                    dev, launched);
+    if (rowchunks >= 8 * 16 && (rowchunks + 15) / 16 <= 31)
+        return launch_pipe<16, true>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream,
+                                     dev, launched);
+    if (rowchunks >= 8 * 32 && (rowchunks + 31) / 32 <= 31)
+        return launch_pipe<32, true>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream,
+                                     dev, launched);
+    return cudaSuccess;
+}
 
 cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz_all, const float* gw, const float* gx, int N,

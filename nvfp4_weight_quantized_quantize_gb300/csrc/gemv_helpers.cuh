@@ -50,6 +50,40 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
 }
 
 // exponent e with amax * 2^e in [2^14, 2^15) (0 for amax == 0)
+// W4A4 with a static activation scale g, fused into the small-M kernels: the 32 bf16
+// values of a lane's chunk of x (two 16-element blocks) are quantized to NVFP4 with g, as
+// the quantizer would, and replaced by e2m1(code) * e4m3(scale).  bf16 holds those exactly
+// (at most 5 significant bits, magnitudes in [2^-10, 2688]); g stays out of them and in
+// y's scale.
+__device__ __forceinline__ void quantize_chunk_static(uint4 (&v)[4], float g) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float t[16];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint32_t w[4] = {v[2 * h + q].x, v[2 * h + q].y, v[2 * h + q].z, v[2 * h + q].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                t[8 * q + 2 * j] = bf16_to_f32(w[j] & 0xFFFFu);
+                t[8 * q + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
+            }
+        }
+        uint32_t lo, hi;
+        const float s = e4m3_to_f32(quantize_block16(t, g, lo, hi));
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            // elements 2j and 2j + 1: nibbles 2j, 2j + 1 of lo (j < 4) or hi
+            const uint32_t w = j < 4 ? lo : hi;
+            const float a = __fmul_rn(e2m1_to_f32((w >> (8 * (j & 3))) & 15u), s);
+            const float b = __fmul_rn(e2m1_to_f32((w >> (8 * (j & 3) + 4)) & 15u), s);
+            o[j] = (uint32_t)f32_to_bf16_rne(a) | ((uint32_t)f32_to_bf16_rne(b) << 16);
+        }
+        v[2 * h] = make_uint4(o[0], o[1], o[2], o[3]);
+        v[2 * h + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
 __device__ __forceinline__ int chunk_exponent(float amax) {
     if (!(amax > 0.0f)) return 0;
     int E;

@@ -65,6 +65,15 @@ cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
 
 constexpr int kGemvMaxM = 16;
 
+// W4A4 at 1 <= M <= 8 with a static activation scale *gx, the quantization of x fused into
+// the M = 1 GEMV or the skinny kernel (bf16 x in, no pre-pass, nothing in the workspace but
+// the error word).  Sets *launched when a fused kernel took the call; otherwise nothing
+// was enqueued and the caller quantizes x first.
+cudaError_t launch_gemv_w4a4_static(const uint16_t* x, int M, int K, const uint8_t* wq,
+                                    const uint8_t* wsz_all, const float* gw, const float* gx,
+                                    int N, void* y, bool y_bf16, uint32_t* err, bool w_static,
+                                    cudaStream_t stream, const DevInfo& dev, bool* launched);
+
 // Whether launch_skinny_w4a16 takes calls with this K (its ring fits shared memory).
 bool skinny_w4a16_takes(int K, const DevInfo& dev);
 
@@ -74,7 +83,8 @@ bool skinny_w4a16_takes(int K, const DevInfo& dev);
 cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                                 const uint8_t* wrm, const float* gw, const float* gx, int N,
                                 void* y, bool y_bf16, uint32_t* err, bool w_static,
-                                cudaStream_t stream, const DevInfo& dev, bool* launched);
+                                cudaStream_t stream, const DevInfo& dev, bool* launched,
+                                bool x_quant_static = false);
 
 // M > 16 W4A16 GEMM on the tensor cores (tcgen05, TMA).  wsz: the atom part of the
 // repacked scales (offset 0 of the repacked buffer).  y = *gw * x . W^T.

@@ -282,6 +282,15 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
                                            w_global_scale, (int)N, y, ybf,
                                            static_cast<uint8_t*>(workspace), stream, d));
     }
+    // W4A4 at M <= 8 with a static activation scale: the quantization of x is fused into
+    // the small-M kernels (no pre-pass; the same codes and scales as below)
+    if (x_global_scale && M <= 8) {
+        bool launched = false;
+        const cudaError_t e = launch_gemv_w4a4_static(
+            xb, (int)M, (int)K, w_packed, w_scales_swizzled, w_global_scale, x_global_scale,
+            (int)N, y, ybf, static_cast<uint32_t*>(workspace), w_static, stream, d, &launched);
+        if (e != cudaSuccess || launched) return from_cuda(e);
+    }
     // W4A4: quantize x into the workspace (bit-exact with nvfp4_quantize + nvfp4_repack)
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const W4A4Layout L = w4a4_layout(M, K, N);

@@ -56,7 +56,7 @@ __host__ __device__ __forceinline__ size_t sk_smem(int K, int ngroups, int stage
            (size_t)stages * (8 + 8 + 4 * kSkMaxRgs);  // full, empty barriers; row-group counters
 }
 
-template <int U>
+template <int U, bool kXQ>
 __global__ void __launch_bounds__(kSkMaxThreads, 1)
 skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* __restrict__ wq,
                    const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
@@ -169,6 +169,23 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
         for (int j = 0; j < 8; ++j)
             raw[u][j] = ok ? *reinterpret_cast<const uint2*>(xp + 4 * j) : make_uint2(0u, 0u);
     }
+    if constexpr (kXQ) {
+        // W4A4 with a static activation scale: each chunk's two blocks quantized here
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                v[q] = make_uint4(raw[u][2 * q].x, raw[u][2 * q].y, raw[u][2 * q + 1].x,
+                                  raw[u][2 * q + 1].y);
+            quantize_chunk_static(v, *gx);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                raw[u][2 * q] = make_uint2(v[q].x, v[q].y);
+                raw[u][2 * q + 1] = make_uint2(v[q].z, v[q].w);
+            }
+        }
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -188,8 +205,9 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
     const int eg = chunk_exponent(am);  // token g's exponent in this warp
+    // (e2m1 * e4m3 values span less than 2^22: never inexact after the rescale)
     const bool any_inexact =
-        __any_sync(0xffffffffu, times_pow2(mn, eg) < 7.62939453125e-06f);
+        __any_sync(0xffffffffu, !kXQ && times_pow2(mn, eg) < 7.62939453125e-06f);
     // every token's exponent and 2^-e in this warp (token m's lanes are 4m .. 4m + 3), in
     // the warp's own shared-memory row
     {
@@ -344,7 +362,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
 
 namespace {
 
-template <int U>
+template <int U, bool kXQ>
 cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
                             const uint8_t* wrm, const float* gw, const float* gx, int N, void* y,
                             bool y_bf16, uint32_t* err, bool w_static, cudaStream_t stream,
@@ -376,9 +394,9 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
     const uint64_t bit = 1ull << (dev.device & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, skinny_pipe_kernel<U>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, skinny_pipe_kernel<U, kXQ>);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(skinny_pipe_kernel<U>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(skinny_pipe_kernel<U, kXQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(dev.smem_optin - fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
@@ -393,7 +411,7 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_pipe_kernel<U>, x, M, K, wq, wrm, gw, gx, N,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_pipe_kernel<U, kXQ>, x, M, K, wq, wrm, gw, gx, N,
                                        y, y_bf16 ? 1 : 0, stages, rgs, w_static ? 1 : 0,
                                        err);
     *launched = true;
@@ -413,16 +431,27 @@ bool skinny_w4a16_takes(int K, const DevInfo& dev) {
 cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                                 const uint8_t* wrm, const float* gw, const float* gx, int N,
                                 void* y, bool y_bf16, uint32_t* err, bool w_static,
-                                cudaStream_t stream, const DevInfo& dev, bool* launched) {
+                                cudaStream_t stream, const DevInfo& dev, bool* launched,
+                                bool x_quant_static) {
     *launched = false;
     if (M < 2 || M > 8) return cudaSuccess;
+    if (x_quant_static) {
+        const int rowchunks = K / 32;
+        if ((rowchunks + 3) / 4 <= kSkMaxGroups)
+            return launch_skinny_u<1, true>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                            w_static, stream, dev, launched);
+        if ((rowchunks + 7) / 8 <= kSkMaxGroups)
+            return launch_skinny_u<2, true>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                            w_static, stream, dev, launched);
+        return cudaSuccess;
+    }
     // at most kSkMaxGroups consumer warps: 4 or 8 chunks of K per warp
     const int rowchunks = K / 32;
     if ((rowchunks + 3) / 4 <= kSkMaxGroups)
-        return launch_skinny_u<1>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, w_static, stream,
+        return launch_skinny_u<1, false>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, w_static, stream,
                                   dev, launched);
     if ((rowchunks + 7) / 8 <= kSkMaxGroups)
-        return launch_skinny_u<2>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, w_static, stream,
+        return launch_skinny_u<2, false>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, w_static, stream,
                                   dev, launched);
     return cudaSuccess;
 }

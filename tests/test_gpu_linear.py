@@ -94,6 +94,9 @@ def test_w4a4_small_m(M, K, N, gx):
     wq, ws, gw = oracle.quantize(w.numpy())
     y, ws_t = run_linear(x, wq, ws, gw, K, torch.bfloat16, mode="w4a4", gx=gx)
     y_ref, ab, xq, xs, gxo = oracle.linear_w4a4(x, wq, ws, gw, gx)
+    check_tolerance(y_to_f64(y), y_ref, ab, "w4a4 M%d" % M)
+    if gx is not None and M <= 8:
+        return  # quantized inside the small-M kernel: nothing lands in the workspace
     # the in-call activation quantization is bit-exact: codes, swizzled scales, g_x
     o_xq, o_xs, o_gx = nv.nvfp4_w4a4_workspace_layout(M, K)
     wsh = ws_t.cpu().numpy()
@@ -101,7 +104,31 @@ def test_w4a4_small_m(M, K, N, gx):
     nb = oracle.repack_atom_bytes(M, K)
     np.testing.assert_array_equal(wsh[o_xs:o_xs + nb], oracle.repack(xs, K)[:nb])
     assert wsh[o_gx:o_gx + 4].view(np.float32)[0] == np.float32(gxo)
-    check_tolerance(y_to_f64(y), y_ref, ab, "w4a4 M%d" % M)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 96, 70), (1, 2080, 333), (1, 5120, 1000),
+                                   (1, 17408, 300), (3, 96, 70), (3, 5120, 600), (8, 2080, 129),
+                                   (8, 17408, 40)])
+def test_w4a4_static_scale_fused(M, K, N):
+    # W4A4 with a static activation scale at M <= 8 quantizes x inside the GEMV / skinny
+    # kernel.  Its output must equal, bit for bit, the linear on the same activations
+    # quantized by the oracle (the products are the same exact values), and the oracle
+    # within the tolerance.
+    gx = 0.004
+    x, w = make_inputs(M, K, N, seed=500 + M + K)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y, _ = run_linear(x, wq, ws, gw, K, torch.bfloat16, mode="w4a4", gx=gx, static_weights=True)
+    y_ref, ab, xq, xs, gxo = oracle.linear_w4a4(x, wq, ws, gw, gx)
+    check_tolerance(y_to_f64(y), y_ref, ab, "fused w4a4 M%d K%d" % (M, K))
+    d_wq, d_swz, d_g = upload_weights(wq, ws, gw, K)
+    d_xs = to_dev(oracle.repack(xs, K)[:oracle.repack_atom_bytes(M, K)].copy())
+    y2 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    work = torch.zeros(nv.nvfp4_workspace_bytes(1, M, K, N, nv.NVFP4_W4A4), dtype=torch.uint8,
+                       device="cuda")
+    nv.nvfp4_linear_nvfp4_x(to_dev(xq), d_xs, torch.tensor([gxo], device="cuda"), d_wq, d_swz,
+                            d_g, y2, work)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)
 
 
 def test_repeated_calls_are_deterministic():
