@@ -41,6 +41,24 @@ FP4_NOMINAL_TFLOPS = 13500.0  # dense FP4 tensor peak of a GB300 (nominal, not m
 # set from --static-weights: the decode/verify calls pass NVFP4_STATIC_WEIGHTS
 STATIC_W = False
 
+def max_over_ranks(ms: float, dist, device: str) -> float:
+    """The job's duration: the largest of the ranks' timed regions (every rank leaves the
+    region through a barrier, so the slowest replica ends it).  `dist` is None for one
+    process; `device` is where the collective's tensor lives ("cuda" for NCCL, "cpu" for
+    gloo)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(bytes_per_step: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the bytes every replica streamed over the job's duration."""
+    return bytes_per_step * steps * world / (ms * 1e-3) / 1e9
+
+
 def algo_bytes(M, K, N, y_bytes=2):
     return N * K // 2 + N * K // 16 + M * K * 2 + M * N * y_bytes + 4
 
@@ -225,13 +243,8 @@ def run_ours(args, rank, world, dist):
     clocks = sampler.stop() if sampler else None
     ms = t0.elapsed_time(t1)
     launch_ms = [e[2 * j].elapsed_time(e[2 * j + 1]) for e in ev for j in range(len(S))]
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-
-    total_bytes = setup.bytes_per_step * args.steps * world
-    value = total_bytes / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(ms, dist, "cuda")
+    value = job_gbps(setup.bytes_per_step, args.steps, world, ms)
 
     # end to end: host x -> device, both calls, y -> host, every step
     e2e = run_e2e(torch, nv, setup, args)
