@@ -7,8 +7,8 @@
 // Bound by HBM (each weight is read once for all M rows of x), so the kernel streams W the
 // way the M = 1 kernel does, and does the arithmetic on the tensor cores:
 //   - one CTA per SM owns a contiguous run of 16-row groups; a producer warp fills a ring
-//     of stages (one 16-row group each: its codes and its row-major scale bytes, two bulk
-//     copies, mbarrier-gated, bounded waits);
+//     of stages (up to four 16-row groups each: their codes and their row-major scale
+//     bytes, two bulk copies, mbarrier-gated, bounded waits);
 //   - consumer warp w owns the K columns [w CG, (w+1) CG) (CG = 4 U chunks of 32) for the
 //     whole kernel, so its slice of x -- the B fragments of mma.sync m16n8k16, fp16 after a
 //     per-token power-of-two rescale -- is built once and stays in registers;
@@ -16,11 +16,13 @@
 //     and g + 8; MMA j (0..7) takes elements 4j .. 4j+3 of those chunks for its k-slots
 //     {2t, 2t+1, 2t+8, 2t+9} (any bijection works when A and B use the same one), with the
 //     block scale folded into A (e2m1 * e4m3 is exact in fp16);
-//   - each warp leaves its 16 x 8 partial tile in a per-stage slot; the warp whose arrival
-//     completes the stage's count adds the slots in warp order (deterministic) and writes
-//     the 16 rows of y.  No warp waits for another.
+//   - each warp leaves its 16 x 8 partial tile of a row group in a per-stage slot; the warp
+//     whose arrival completes the row group's count adds the slots in warp order
+//     (deterministic) and writes the 16 rows of y.  No warp waits for another.
 // x values that fp16 cannot hold exactly after the rescale (more than about 2^31 below
 // the token's maximum) make every warp add the exact fp32 residual of its slice.
+// W4A4 with a static activation scale (the kXQ instantiations): each lane first quantizes
+// its chunks of x to NVFP4 and keeps e2m1 * e4m3, which the rescale carries exactly.
 #include <cuda_fp16.h>
 
 #include <algorithm>
