@@ -16,15 +16,17 @@
 // codes per row: one 128-byte swizzle row).  One 256-column fp32 accumulator (the rest of
 // TMEM holds the scales of the stages in flight), so the MMAs of a tile start once the
 // epilogue has read the previous one.  Warp roles:
-//   warp 0      TMA producer: per K step the two 128 x 128-byte code boxes (128-byte
-//               swizzle) and the W and x scale atoms of those 256 K (bulk copies);
+//   warp 0      TMA producer: per K step the W and x scale atoms of those 256 K (bulk
+//               copies, first, on a barrier of their own), then the two 128 x 128-byte
+//               code boxes (128-byte swizzle);
 //   warp 1      allocates TMEM (the accumulator + a scale area per stage) and, from one
 //               thread, issues 4 x 128x256x64 block-scaled MMAs per stage once its codes
 //               and its scales are in place;
 //   warps 2-5   epilogue (shared with the W4A16 GEMM): x gx gw, y fp32 or bf16;
-//   warps 6-9   scale writers: each thread loads row (lane) of the stage's 12 atoms (4 of
-//               W, 2 x 4 of x) from shared memory and stores them to its TMEM lane
-//               (keeping these copies off the MMA thread's in-order tcgen05 queue).
+//   warps 6-9   scale writers: once a stage's atoms have landed (while its codes may still
+//               be in flight), each thread loads row (lane) of the 12 atoms (4 of W,
+//               2 x 4 of x) from shared memory and stores them to its TMEM lane (keeping
+//               these copies off the MMA thread's in-order tcgen05 queue).
 // Work split, stream-K fixup, bounded waits and error reporting as in the W4A16 GEMM.
 #include <cuda.h>
 

@@ -11,6 +11,12 @@
 // scale itself (no inter-CTA counter, nothing to reset), then one thread quantizes
 // one 16-element block: 64 (fp32) or 32 (bf16) contiguous bytes in, 8 packed bytes
 // and one scale byte out.  Both passes are HBM-bound.
+//
+// FP8 checkpoints ("e4m3 block-128": E4M3 bytes with one fp32 scale per 128 x 128 tile)
+// take the same two passes through their own kernels (amax_fp8_b128_kernel,
+// quantize_fp8_b128_kernel): each value is bf16(e4m3 * tile scale), the chain FP8 ->
+// BF16 -> NVFP4, without writing the bf16 tensor.  With 1 byte read per element these
+// are bound by instruction issue rather than by HBM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
