@@ -194,6 +194,9 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *   W4A4:  x is first quantized like nvfp4_quantize (global scale = its amax / 2688,
  *          or *x_global_scale when given) into the workspace; then
  *          y = g_x g_w * sum_b sx[m,b] sw[n,b] sum_{k in b} e2m1(qx) e2m1(qw).
+ *          With a given x_global_scale and M <= 8, the M = 1 GEMV and the skinny GEMM
+ *          quantize x themselves (same codes and scales, no pre-pass); x's codes are
+ *          then not written to the workspace.
  * Accumulation is fp32.  Expected accuracy: |y - y_ref| <= 1e-3 * sum_k |x_k w_k|
  * + 2^-8 |y_ref| for bf16 y.
  * Arguments:
@@ -214,9 +217,11 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *                      zero before the first call; every call that completes without a
  *                      device error leaves them zero) and fp32 partial tiles.  After a
  *                      device error (nvfp4_workspace_error != 0), zero-fill it again.
- * Kernels: M = 1 pipelined GEMV; 2 <= M <= 8 streamed skinny GEMM (mma.sync); M <= 16
- * otherwise the mma.sync skinny GEMM; M > 16 the tcgen05 GEMMs (W4A16: W dequantized to
- * bf16 per tile; W4A4: block-scaled kind::mxf4nvf4).  Results are deterministic.
+ * Kernels: M = 1 pipelined GEMV; 2 <= M <= 8 streamed skinny GEMM (mma.sync); 9 <= M <=
+ * 16 the skinny GEMM on tokens 0..7 and again on the rest where it takes the K, else an
+ * mma.sync GEMM reading W from global memory; M > 16 the tcgen05 GEMMs (W4A16: W
+ * dequantized to bf16 per tile; W4A4: block-scaled kind::mxf4nvf4).  Results are
+ * deterministic.
  */
 nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K, const uint8_t* w_packed,
                           const uint8_t* w_scales_swizzled, const float* w_global_scale,
@@ -294,7 +299,9 @@ size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N, nvfp4_mode
 /* Where nvfp4_linear in W4A4 mode leaves the quantized activations inside its
  * workspace: packed codes [M, K/2] at *xq_offset, the scales in the tensor-core
  * layout (part 1 of nvfp4_repack's layout, Rp*Cp bytes) at *xs_offset and g_x (one
- * float) at *gx_offset.  They are valid once the call has completed.  Returns NVFP4_OK or
+ * float) at *gx_offset.  They are valid once the call has completed, except after a
+ * call with a given x_global_scale and M <= 8, where the small-M kernel may have
+ * quantized x itself and left these areas untouched.  Returns NVFP4_OK or
  * NVFP4_ERR_SHAPE. */
 nvfp4_status nvfp4_w4a4_workspace_layout(int64_t M, int64_t K, size_t* xq_offset,
                                          size_t* xs_offset, size_t* gx_offset);
