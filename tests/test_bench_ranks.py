@@ -56,3 +56,24 @@ def test_reference_arm_runs_on_rank_zero_only():
     class A:
         steps, warmup = 1, 0
     assert bench.run_reference(A(), 1, 2) is None
+
+
+def test_reference_arm_line_keeps_the_contract():
+    # `bench.py --impl reference` on the host cores: one JSON line with the arm's metric,
+    # unit and direction, its cpu_baseline and an e2e with no host<->device bytes
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.abspath(bench.__file__))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "3"], capture_output=True, text=True,
+                         timeout=600, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] >= 3
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
