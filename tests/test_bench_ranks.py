@@ -77,3 +77,11 @@ def test_reference_arm_line_keeps_the_contract():
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_algorithmic_bytes_of_the_workloads():
+    # packed nibbles + E4M3 scales + x (bf16) + y (bf16) + the global scale, per call
+    assert bench.algo_bytes(1, 5120, 17408) == 50_180_100     # decode, either shape
+    assert bench.algo_bytes(1, 17408, 5120) == 50_180_100
+    assert bench.algo_bytes(7, 5120, 34816) == 100_829_188    # MTP verify
+    assert bench.algo_bytes(7, 5120, 6144) == 17_852_420
