@@ -9,7 +9,7 @@ rotate over several copies (> 2x L2 in total) so every call streams from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle (the reference arm of this build) on a bounded
+--impl reference times the CPU oracle (the reference arm) on a bounded
 sample of the same workload.  Under torchrun with N > 1 every rank runs an independent
 replica ("replicas only": the projection needs no exchange); value = all ranks' bytes
 over the slowest rank's time.
