@@ -44,6 +44,42 @@ def test_every_declared_symbol_is_exported(lib):
     assert exported == set(declared_functions())
 
 
+def test_header_is_plain_c():
+    # the boundary is a C ABI: the header alone must compile as C99 and as C++
+    for lang, std in (("c", "-std=c99"), ("c++", "-std=c++17")):
+        out = subprocess.run(["gcc", std, "-Wall", "-Wextra", "-pedantic", "-Werror",
+                              "-fsyntax-only", "-x", lang, HEADER], capture_output=True,
+                             text=True)
+        assert out.returncode == 0, out.stderr
+
+
+def test_c_program_links_and_calls_host_helpers(lib, tmp_path):
+    # a plain C caller links against the library and uses the host-only helpers (no
+    # device work): sizes, status strings and a rejected call
+    src = tmp_path / "caller.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include "nvfp4.h"
+int main(void) {
+    if (nvfp4_repack_bytes(17408, 5120) != (size_t)2 * 17408 * 320 + 16) return 1;
+    if (nvfp4_workspace_bytes(1, 1, 48, 4, NVFP4_W4A16) != (size_t)-1) return 2;
+    if (nvfp4_linear(NULL, 1, 64, NULL, NULL, NULL, 8, NULL, NVFP4_BF16, NVFP4_W4A16, NULL,
+                     NULL, 0, NULL) != NVFP4_ERR_NULL) return 3;
+    puts(nvfp4_status_str(NVFP4_ERR_SHAPE));
+    return 0;
+}
+""")
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(nv.LIB_PATH)
+    out = subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe),
+                          "-L", libdir, "-lnvfp4", "-Wl,-rpath," + libdir],
+                         capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    assert run.stdout.strip() == nv.nvfp4_status_str(2)
+
+
 def test_status_strings(lib):
     for code in range(10):
         assert nv.nvfp4_status_str(code).startswith(nv.STATUS[code])
