@@ -17,6 +17,10 @@ Qwen3.x serving; the fused gate+up projection doubles N):
   prefill_b   512   17408  5120   bf16  4     same
   w4a4        2048  5120   17408  bf16  5     x quantized to NVFP4 inside the call
 
+Beyond these: FP8 block-128 checkpoints (random_fp8_block128), fused gate/up outputs
+(random_gate_up) and already-encoded NVFP4 weights (random_nvfp4_weights) for the
+conversion, activation and wide-N cases.
+
 Draw order with ``torch.Generator(device='cpu').manual_seed(seed)``: W ~ N(0, 0.02)
 fp32 first, then x ~ N(0, 1) fp32, then the outlier positions (uniform without
 replacement: sequential draws with repeats discarded; the entries keep their sign
