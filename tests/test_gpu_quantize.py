@@ -47,6 +47,18 @@ def test_hand_worked_tensor():
     np.testing.assert_array_equal(p, [[int(v, 16) for v in r] for r in h["expected_packed_hex"]])
 
 
+def test_scale_op_order_tensors():
+    # g not a power of two, block quotients within one ulp of an E4M3 midpoint: only
+    # the product-first order bmax / (6 g) gives the fixture's bytes
+    fx = json.load(open(os.path.join(GOLDEN, "scale_op_order.json")))
+    for case in fx["cases"]:
+        t = torch.tensor([[float(v) for v in case["input"]]], dtype=torch.float32)
+        p, s, g = gpu_quantize(t)
+        assert float(g).hex() == case["expected_global_scale"], case["name"]
+        assert ["%02X" % b for b in s[0]] == case["expected_scales_hex"], case["name"]
+        assert ["%02X" % b for b in p[0]] == case["expected_packed_hex"], case["name"]
+
+
 @pytest.mark.parametrize("rows,cols,seed", [(1, 16, 0), (3, 48, 1), (129, 80, 2),
                                             (256, 512, 3), (1000, 1040, 4)])
 def test_ragged_shapes_fp32(rows, cols, seed):
