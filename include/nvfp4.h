@@ -114,14 +114,16 @@ nvfp4_status nvfp4_quantize(const void* src, nvfp4_dtype src_dtype, int64_t rows
  * is a fixed array in device memory owned by the library, which every GPU that loads
  * the library keeps until the process exits.  Arguments are those of nvfp4_quantize
  * without the workspace.
- *   - The first call on a device looks up the array's device address (one
- *     cudaGetSymbolAddress with that device current) and caches it; make that first
- *     call before any stream capture.
+ *   - The first call in a CUDA context (the first on a device, and the first after a
+ *     cudaDeviceReset or under another context made current) looks up the array's
+ *     device address there (one cudaGetSymbolAddress) and caches it under that
+ *     context's id; make that first call before any stream capture.  A reset unloads
+ *     the library's device code, and the next call looks the address up again.
  *   - Every call on a device shares the one array and leaves its contents behind;
  *     nothing in it has to start at zero.  Calls whose kernels overlap on the GPU
  *     (on different streams, or from different threads) race on it: order them.
- *   - A call that would need more than 2048 first-pass partials returns
- *     NVFP4_ERR_WORKSPACE (not reachable on GPUs with fewer than 256 SMs).
+ *   - The first pass runs at most 2048 CTAs; a larger tensor is split over them (each
+ *     strides over the whole input), exactly as nvfp4_quantize caps its own count.
  *   - It calls no allocating function (no cudaMalloc, no cudaFree).
  */
 nvfp4_status nvfp4_quantize_noalloc(const void* src, nvfp4_dtype src_dtype, int64_t rows,

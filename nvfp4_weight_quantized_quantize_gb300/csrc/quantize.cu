@@ -379,21 +379,71 @@ constexpr int kNoAllocPartials = 2048;
 static __device__ __align__(256) float g_noalloc_partials[kNoAllocPartials];
 
 std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[64] = {};
 
-// Device address of g_noalloc_partials on `device` (the current device).  In host code
-// the array's name only stands in for the symbol; the address a kernel can use comes
-// from cudaGetSymbolAddress, looked up once per device and cached.
-cudaError_t noalloc_scratch(int device, float** out) {
-    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[device]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_partials);
-        if (e != cudaSuccess) return e;
-        g_noalloc_ptr[device] = static_cast<float*>(p);
+// cuCtxGetCurrent / cuCtxGetId, reached through the runtime so that the library needs
+// no link-time dependency on the driver library.
+typedef int (*CtxGetCurrentFn)(void**);
+typedef int (*CtxGetIdFn)(void*, unsigned long long*);
+
+// Identity of the calling thread's current context.  A context that a device reset
+// destroyed is never given the same id again, so an address cached under an id cannot
+// outlive the module load it came from.
+cudaError_t current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (!get_current || !get_id) {
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000,
+                                                         cudaEnableDefault, &q1);
+        if (e != cudaSuccess || q1 != cudaDriverEntryPointSuccess || !f1)
+            return e != cudaSuccess ? e : cudaErrorNotSupported;
+        e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+        if (e != cudaSuccess || q2 != cudaDriverEntryPointSuccess || !f2)
+            return e != cudaSuccess ? e : cudaErrorNotSupported;
+        get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+        get_id = reinterpret_cast<CtxGetIdFn>(f2);
     }
-    *out = g_noalloc_ptr[device];
+    void* ctx = nullptr;
+    if (get_current(&ctx) != 0 || !ctx) return cudaErrorDeviceUninitialized;
+    if (get_id(ctx, id) != 0) return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
+
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    float* ptr;
+};
+constexpr int kScratchEntries = 64;
+ScratchEntry g_noalloc_cache[kScratchEntries] = {};
+int g_noalloc_next = 0;
+
+// Device address of g_noalloc_partials in the current context.  In host code the array's
+// name only stands in for the symbol; the address a kernel can use comes from
+// cudaGetSymbolAddress, looked up once per context (the first call on a device, and the
+// first after a device reset or under another context made current) and cached under
+// the context's id.
+cudaError_t noalloc_scratch(float** out) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    unsigned long long id = 0;
+    cudaError_t e = current_context_id(&id);
+    if (e == cudaSuccess) {
+        for (int i = 0; i < kScratchEntries; ++i)
+            if (g_noalloc_cache[i].ptr && g_noalloc_cache[i].ctx_id == id) {
+                *out = g_noalloc_cache[i].ptr;
+                return cudaSuccess;
+            }
+    }
+    // the lookup also makes the device's primary context current if none was yet
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_partials);
+    if (e != cudaSuccess) return e;
+    e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    g_noalloc_cache[g_noalloc_next] = {id, static_cast<float*>(p)};
+    g_noalloc_next = (g_noalloc_next + 1) % kScratchEntries;
+    *out = static_cast<float*>(p);
     return cudaSuccess;
 }
 
@@ -415,12 +465,13 @@ extern "C" __attribute__((visibility("default"))) nvfp4_status nvfp4_quantize_no
     DevInfo d;
     const nvfp4_status st = (nvfp4_status)query_device(&d);
     if (st != NVFP4_OK) return st;
-    // pass 1 runs one CTA per partial; a call that would need more partials than the
-    // array holds is refused (it cannot happen below 256 SMs)
-    const int np = amax_partial_count(rows * cols, d.sm_count);
-    if (np > kNoAllocPartials) return NVFP4_ERR_WORKSPACE;
+    // pass 1 runs one CTA per partial, each striding over the whole input, so capping
+    // the count at the array's size changes only how the work is split, as
+    // nvfp4_quantize caps it at its workspace's
+    int np = amax_partial_count(rows * cols, d.sm_count);
+    if (np > kNoAllocPartials) np = kNoAllocPartials;
     float* partials = nullptr;
-    if (noalloc_scratch(d.device, &partials) != cudaSuccess) {
+    if (noalloc_scratch(&partials) != cudaSuccess) {
         cudaGetLastError();
         return NVFP4_ERR_CUDA;
     }
