@@ -204,21 +204,19 @@ def run_ours(args, rank, world, dist):
             if events is not None:
                 events[2 * j + 1].record()
 
-    # timed region: a CUDA graph of G steps replayed, then EV eager steps with CUDA events
-    # around every launch (per-launch kernel durations for the roofline)
-    EV = min(8, args.steps)
-    KG = args.steps - EV
-    G = min(KG, 64) if KG > 0 else 0
-    while G > 1 and KG % G:
-        G -= 1
-    graph = capture(torch, step, G) if G else None
-    reps = KG // G if G else 0
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(S))] for _ in range(EV)]
+    # timed region: every one of the K steps runs as a CUDA-graph replay of the production
+    # path (a graph of G steps replayed K // G times, then a graph of the K % G remaining
+    # steps), so each launch runs back to back with its programmatic-launch overlap
+    G = min(args.steps, 256)
+    reps, tail = divmod(args.steps, G)
+    graph = capture(torch, step, G)
+    graph_tail = capture(torch, lambda i: step(reps * G + i), tail) if tail else None
 
     for i in range(max(args.warmup, 3)):
         step(i)
-    if graph:
-        graph.replay()
+    graph.replay()
+    if graph_tail:
+        graph_tail.replay()
     torch.cuda.synchronize()
     sampler = ClockSampler(gpu_uuid(torch, dev)) if rank == 0 else None
     if sampler:
@@ -229,22 +227,30 @@ def run_ours(args, rank, world, dist):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    tg = torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(reps):
         graph.replay()
-    tg.record()
-    for i in range(EV):
-        step(KG + i, ev[i])
+    if graph_tail:
+        graph_tail.replay()
     t1.record()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     ms = t0.elapsed_time(t1)
-    launch_ms = [e[2 * j].elapsed_time(e[2 * j + 1]) for e in ev for j in range(len(S))]
+    ms_local = ms
     ms = max_over_ranks(ms, dist, "cuda")
     value = job_gbps(setup.bytes_per_step, args.steps, world, ms)
+
+    # per-launch durations of eager launches bracketed by CUDA events, outside the timed
+    # region (events between launches break the programmatic-launch overlap, so these
+    # read longer than the launches of the graph)
+    EV = 8
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(S))] for _ in range(EV)]
+    for i in range(EV):
+        step(i, ev[i])
+    torch.cuda.synchronize()
+    launch_ms = [e[2 * j].elapsed_time(e[2 * j + 1]) for e in ev for j in range(len(S))]
 
     # end to end: host x -> device, both calls, y -> host, every step
     e2e = run_e2e(torch, nv, setup, args)
@@ -252,15 +258,12 @@ def run_ours(args, rank, world, dist):
     out = None
     if rank == 0:
         pk, pk_src = peaks()
-        # a step is nothing but launches of the GEMV kernel, so in the graph part of the
-        # timed region the kernel's average launch duration is that time / launches; the
-        # launches run back to back (each may start its prologue under the previous one's
-        # tail).  Eager launches bracketed by events are reported beside it.
+        # a step is nothing but launches of the GEMV kernel, so the kernel's average launch
+        # duration is the timed region / launches; the launches run back to back (each may
+        # start its prologue under the previous one's tail).  Eager launches bracketed by
+        # events are reported beside it.
         eager_launch_s = statistics.mean(launch_ms) * 1e-3
-        if graph:
-            avg_launch_s = t0.elapsed_time(tg) * 1e-3 / (reps * G * len(S))
-        else:
-            avg_launch_s = eager_launch_s
+        avg_launch_s = ms_local * 1e-3 / (args.steps * len(S))
         achieved = statistics.mean(setup.bytes_per_launch) / avg_launch_s / 1e9
         traffic = read_traffic()
         out = {
@@ -278,16 +281,17 @@ def run_ours(args, rank, world, dist):
                        "l2": "inputs larger than L2: %d rotating weight copies (%.0f MB)"
                              % (setup.copies, setup.bytes_per_step * setup.copies / 1e6),
                        "parallelism": "replicas only (dp%d)" % world,
-                       "timing": "CUDA graph of %d steps replayed %d times + %d eager "
-                                 "steps with per-launch CUDA events" % (G, reps, EV)},
+                       "timing": "every timed step a CUDA-graph replay: a graph of %d steps "
+                                 "replayed %d times%s" % (G, reps, (" + a graph of the %d "
+                                                                    "remaining steps" % tail)
+                                                          if tail else "")},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(achieved / pk["hbm_gbs"], 4),
                          "traffic": traffic, "peak_source": pk_src,
                          "kernel": "gemv_m1_pipe_kernel",
                          "launch_us": round(avg_launch_s * 1e6, 2),
-                         "launch_timing": "graph part of the timed region / launches"
-                                          if graph else "eager launches with CUDA events",
+                         "launch_timing": "timed region (CUDA-graph replays) / launches",
                          "eager_launch_us": round(eager_launch_s * 1e6, 2)},
             "e2e": e2e,
             "gpu_launches": len(S) * args.steps,
@@ -593,14 +597,35 @@ def oracle_decode_inputs():
     return out
 
 
+def oracle_slab(data, frac: float):
+    """One timed unit of the oracle: the first `frac` of each decode shape's output rows
+    (a contiguous slab of W rows, all M = 1 outputs of it), through the oracle's linear,
+    which spreads the rows over every host thread.  Returns (run, algorithmic bytes)."""
+    slabs = []
+    for x, wq, ws, gw in data:
+        n = max(1, min(wq.shape[0], int(round(wq.shape[0] * frac))))
+        slabs.append((x, wq[:n], ws[:n], gw, n))
+    nbytes = sum(algo_bytes(1, x.shape[1], n) for x, _, _, _, n in slabs)
+
+    def run():
+        for x, wq, ws, gw, _ in slabs:
+            oracle_linear(x, wq, ws, gw)
+
+    return run, nbytes, [n for *_, n in slabs]
+
+
+def oracle_linear(x, wq, ws, gw):
+    import oracle
+    return oracle.linear_w4a16(x, wq, ws, gw)
+
+
 def cpu_baseline(seconds: float = 10.0):
     import oracle
     data = oracle_decode_inputs()
-    nbytes = sum(algo_bytes(1, x.shape[1], wq.shape[0]) for x, wq, _, _ in data)
+    run, nbytes, _ = oracle_slab(data, 1.0)
     reps, t0 = 0, time.perf_counter()
     while True:
-        for x, wq, ws, gw in data:
-            oracle.linear_w4a16(x, wq, ws, gw)
+        run()
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -611,31 +636,36 @@ def cpu_baseline(seconds: float = 10.0):
                       % reps}
 
 
-def run_reference(args, rank, world):
+def run_reference(args, rank, world, budget_s: float = 90.0):
+    """The reference arm: the CPU oracle on the host cores.  A step is one pass over the
+    same workload (both decode shapes, M = 1); where --steps full passes would take longer
+    than budget_s, every step takes the same contiguous slab of each shape's rows, sized to
+    the budget (at least 64 rows per host thread, so every thread has work)."""
     if rank != 0:
         return None
-    import numpy as np
-
     import oracle
     data = oracle_decode_inputs()
-    rows_per_shape = 32
-    rng = np.random.default_rng(0)
-    picks = [rng.integers(0, wq.shape[0], rows_per_shape) for _, wq, _, _ in data]
-    nbytes = sum(algo_bytes(1, x.shape[1], rows_per_shape) for x, _, _, _ in data)
-
-    def step():
-        for (x, wq, ws, gw), pn in zip(data, picks):
-            oracle.linear_w4a16_pairs(x, wq, ws, gw, np.zeros_like(pn), pn)
-
+    probe, _, _ = oracle_slab(data, 1.0)
+    t0 = time.perf_counter()
+    probe()
+    full_s = time.perf_counter() - t0
+    frac = min(1.0, budget_s / max(1e-9, full_s * (args.steps + args.warmup)))
+    min_rows = 64 * oracle.num_threads()
+    frac = max(frac, min(1.0, min_rows / min(wq.shape[0] for _, wq, _, _ in data)))
+    run, nbytes, rows = oracle_slab(data, frac)
     for _ in range(args.warmup):
-        step()
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        run()
     el = time.perf_counter() - t0
     value = nbytes * args.steps / el / 1e9
-    sample = ("%d output rows of each decode shape per step (bytes of those rows: nibbles, "
-              "scales, x, y)" % rows_per_shape)
+    if frac >= 1.0:
+        sample = "every step one full pass over both decode shapes (M=1, all N outputs, fp64)"
+    else:
+        sample = ("every step the first %d and %d output rows of the two decode shapes (a "
+                  "contiguous slab of W rows; the bytes of those rows: nibbles, scales, x, "
+                  "y)" % tuple(rows))
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
