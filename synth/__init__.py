@@ -19,7 +19,9 @@ Qwen3.x serving; the fused gate+up projection doubles N):
 
 Beyond these: FP8 block-128 checkpoints (random_fp8_block128), fused gate/up outputs
 (random_gate_up) and already-encoded NVFP4 weights (random_nvfp4_weights) for the
-conversion, activation and wide-N cases.
+conversion, activation and wide-N cases; x with one nonzero per 16-block
+(sparse_block_x) and weights with nonzero codes and a few scale values
+(structured_nvfp4_weights) for the exact-parity cases.
 
 Draw order with ``torch.Generator(device='cpu').manual_seed(seed)``: W ~ N(0, 0.02)
 fp32 first, then x ~ N(0, 1) fp32, then the outlier positions (uniform without
@@ -149,6 +151,35 @@ def random_nvfp4_weights(N: int, K: int, seed: int):
     packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
     scales = rng.integers(0x10, 0x60, (N, K // 16), dtype=np.uint8)
     return packed, scales, 2.0 ** -8
+
+
+def sparse_block_x(M: int, K: int, seed: int) -> torch.Tensor:
+    """bf16 x [M, K] with exactly one nonzero element in every 16-element block of every
+    row, at a uniform position, with a value drawn uniformly from +-{0.5, 1, 2, 4}.  With
+    such x every block of K adds a nonzero term to each output, and the exact result of
+    a small sum of such terms is representable in fp32 (the exact-parity tests)."""
+    rng = np.random.default_rng(seed)
+    nb = K // 16
+    x = np.zeros((M, nb, 16), dtype=np.float32)
+    pos = rng.integers(0, 16, (M, nb))
+    val = rng.choice(np.array([0.5, 1.0, 2.0, 4.0], dtype=np.float32), (M, nb))
+    val *= np.where(rng.integers(0, 2, (M, nb)) == 1, -1.0, 1.0).astype(np.float32)
+    np.put_along_axis(x, pos[:, :, None], val[:, :, None], axis=2)
+    return torch.from_numpy(x.reshape(M, K)).to(torch.bfloat16)
+
+
+def structured_nvfp4_weights(N: int, K: int, seed: int):
+    """Already-encoded NVFP4 weights for the exact-parity tests: every nibble a nonzero
+    code (magnitude bits 1..7, either sign), scale bytes drawn uniformly from the E4M3
+    encodings of 0.5, 0.75, 1 and 2 (0x30, 0x34, 0x38, 0x40), global scale 2^-5.
+    Returns (packed uint8 [N, K/2], scales uint8 [N, K/16] row-major, global scale)."""
+    rng = np.random.default_rng(seed)
+    mag = rng.integers(1, 8, (N, K), dtype=np.uint8)
+    sign = rng.integers(0, 2, (N, K), dtype=np.uint8) << 3
+    nib = mag | sign
+    packed = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    scales = rng.choice(np.array([0x30, 0x34, 0x38, 0x40], dtype=np.uint8), (N, K // 16))
+    return packed, scales, 2.0 ** -5
 
 
 def random_w(N: int, K: int, seed: int, std: float = 0.02) -> torch.Tensor:
