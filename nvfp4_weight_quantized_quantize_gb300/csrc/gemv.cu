@@ -214,6 +214,7 @@ gemv_m1_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict_
 // and lets the copies it issued land before it exits.
 constexpr int kPipeMaxThreads = 1024;
 constexpr int kPipeStageTarget = 80 * 1024;  // bytes of codes per stage (whole rows)
+constexpr int kPipeFirstStage = 16 * 1024;   // bytes of codes of the first, short stage
 constexpr int kLeanUnroll = 2;  // unroll of the predicate-free step loop
 
 // exact x * 2^e for a bf16 value (two multiplies keep 2^e representable for any e)
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(kPipeMaxThreads, 1)
 gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict__ wq,
                     const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
                     const float* __restrict__ gx, int N, void* __restrict__ y, int y_bf16,
-                    int rows_max, int rps, int stages, int w_static,
+                    int rows_max, int rps, int rfirst, int stages, int w_static,
                     uint32_t* __restrict__ err) {
     constexpr int L = 32 / G;              // rows per step
     extern __shared__ __align__(128) uint8_t smem[];
@@ -254,7 +255,13 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     const int64_t r0 = (int64_t)N * blockIdx.x / gridDim.x;
     const int64_t r1 = (int64_t)N * (blockIdx.x + 1) / gridDim.x;
     const int nrows = (int)(r1 - r0);
-    const int nst = (nrows + rps - 1) / rps;
+    // stage 0 holds the first rfirst rows (a short stage that lands early, so that the
+    // consumers start as soon as x is in registers), every later stage rps rows
+    const int nst = nrows <= rfirst ? 1 : 1 + (nrows - rfirst + rps - 1) / rps;
+    auto stage_beg = [&](int it) { return it == 0 ? 0 : rfirst + (it - 1) * rps; };
+    auto stage_rows = [&](int it) {
+        return min(it == 0 ? rfirst : rps, nrows - stage_beg(it));
+    };
     const int64_t rowb = K >> 1, rows_sb = K >> 4;  // code and scale bytes per row
 
     if (threadIdx.x == 0) {
@@ -274,12 +281,17 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
             // first ring's worth of codes only heads for L2 while the previous kernel on the
             // stream may still run (a prefetch cannot observe stale data: L2 is the point of
             // coherence), and every read that lands in shared memory comes after the wait.
+            // x heads for L2 too (16-byte aligned, K * 2 bytes: a multiple of 64), so that the
+            // consumers' loads of it after the wait hit L2 rather than queue behind the
+            // weight stream in HBM; weight copies are marked evict-first for the same reason
+            prefetch_l2(x, (uint32_t)K * 2u);
             if (!w_static) {
                 for (int it = 0; it < min(nst, stages); ++it)
-                    prefetch_l2(wq + (r0 + (int64_t)it * rps) * rowb,
-                                (uint32_t)(min(rps, nrows - it * rps) * rowb));
+                    prefetch_l2(wq + (r0 + (int64_t)stage_beg(it)) * rowb,
+                                (uint32_t)(stage_rows(it) * rowb));
                 pdl_wait_prior_grid();
             }
+            const uint64_t pol = l2_evict_first_policy();
             int issued = 0;
             for (int it = 0; it < nst; ++it) {
                 const int s = it % stages;
@@ -290,16 +302,17 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                     break;
                 }
                 if (abort_flag) break;
-                const int nr = min(rps, nrows - it * rps);
-                const int64_t rbeg = r0 + (int64_t)it * rps;
+                const int nr = stage_rows(it);
+                const int64_t rbeg = r0 + (int64_t)stage_beg(it);
                 const uint32_t wbytes = (uint32_t)(nr * rowb);
                 // scale bytes of these rows, copied from a 16-byte boundary
                 const int64_t s_lo = (rbeg * rows_sb) & ~(int64_t)15;
                 const int64_t s_hi = ((rbeg + nr) * rows_sb + 15) & ~(int64_t)15;
                 mbar_arrive_expect_tx(&full[s], wbytes + (uint32_t)(s_hi - s_lo));
                 uint8_t* st = ring + (size_t)s * sbytes_stage;
-                bulk_g2s(st, wq + rbeg * rowb, wbytes, &full[s]);
-                bulk_g2s(st + (size_t)rps * rowb, wrm + s_lo, (uint32_t)(s_hi - s_lo), &full[s]);
+                bulk_g2s_hint(st, wq + rbeg * rowb, wbytes, &full[s], pol);
+                bulk_g2s_hint(st + (size_t)rps * rowb, wrm + s_lo, (uint32_t)(s_hi - s_lo),
+                              &full[s], pol);
                 issued = it + 1;
             }
             // every copy of this CTA is in flight: the next kernel on the stream may now
@@ -374,8 +387,9 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
         }
         if (__any_sync(0xffffffffu, abort_flag != 0)) break;
         const uint8_t* st = ring + (size_t)s * sbytes_stage;
-        const int nr = min(rps, nrows - it * rps);
-        const int64_t rbeg = r0 + (int64_t)it * rps;
+        const int nr = stage_rows(it);
+        const int sbeg = stage_beg(it);
+        const int64_t rbeg = r0 + (int64_t)sbeg;
         const uint8_t* sst = st + (size_t)rps * rowb + ((rbeg * rows_sb) & 15);
         // whole steps of L rows with every lane on a real chunk and no residual pass run
         // without predicates; the rest of a short last stage takes the predicated loop
@@ -383,7 +397,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
         if (lean_rows > 0) {
             const uint8_t* wp = st + ((size_t)rsub * rowchunks + c) * 16;
             const uint8_t* sp = sst + (size_t)rsub * rows_sb + 2 * c;
-            float* sl = slots + (size_t)(it * rps + rsub) * ngroups + warp;
+            float* sl = slots + (size_t)(sbeg + rsub) * ngroups + warp;
             const int wstep = L * rowchunks * 16, sstep = L * rows_sb, slstep = L * ngroups;
             const int nsteps = lean_rows / L;
 #pragma unroll kLeanUnroll
@@ -460,7 +474,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
 #pragma unroll
             for (int o = G / 2; o > 0; o >>= 1) pv += __shfl_xor_sync(0xffffffffu, pv, o);
             if ((lane % G) == 0 && rl < nr)
-                slots[(it * rps + rl) * ngroups + warp] = pv;
+                slots[(sbeg + rl) * ngroups + warp] = pv;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -794,6 +808,10 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     while (rps > L && pipe_smem(K, rows_max, rps, stages, ngroups) > budget) rps -= L;
     const size_t smem = pipe_smem(K, rows_max, rps, stages, ngroups);
     if (smem + 2048 > dev.smem_optin) return cudaSuccess;
+    // the first stage: whole steps of L rows, about kPipeFirstStage bytes of codes
+    int rfirst = (kPipeFirstStage / (K / 2) + L - 1) / L * L;
+    if (rfirst < L) rfirst = L;
+    if (rfirst > rps) rfirst = rps;
     static std::atomic<uint64_t> configured{0};
     cudaError_t e = opt_in_smem(gemv_m1_pipe_kernel<G, kXQ>, dev, configured);
     if (e != cudaSuccess) return e;
@@ -810,7 +828,8 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G, kXQ>, x, K, wq, wrm, gw, gx, N,
-                           y, y_bf16 ? 1 : 0, rows_max, rps, stages, w_static ? 1 : 0, err);
+                           y, y_bf16 ? 1 : 0, rows_max, rps, rfirst, stages,
+                           w_static ? 1 : 0, err);
     *launched = true;
     return e != cudaSuccess ? e : cudaGetLastError();
 }
