@@ -535,6 +535,40 @@ def measure_rows(torch, nv, setup):
         "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
         "frac_fp4_nominal": round(tf / FP4_NOMINAL_TFLOPS, 4)}
     del cps, p, z
+    # f1 fused: the gate/up projection of a 512-token chunk (K 5120 -> 2 x 17408, the
+    # prefill_a weights as [gate; up]) with silu(gate) * up quantized to NVFP4 in the GEMM's
+    # epilogue (static scale), against the two-kernel chain it replaces (the GEMM writing
+    # bf16 gu, then the activation quantizer)
+    wl = WORKLOADS["prefill_a"]
+    x, w = workload_inputs("prefill_a")
+    p, _, z, gg = nv.quantize_weight(w.cuda())
+    del w
+    cps = [(p, z), (p.clone(), z.clone())]
+    xd = x.cuda()
+    If = wl.N // 2
+    hq2 = torch.empty(wl.M, If // 2, dtype=torch.uint8, device="cuda")
+    hs2 = torch.empty((wl.M + 127) // 128 * 128 * ((If // 16 + 3) // 4 * 4), dtype=torch.uint8,
+                      device="cuda")
+    wsf = torch.zeros(nv.nvfp4_workspace_bytes(2, wl.M, wl.K, If), dtype=torch.uint8,
+                      device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_linear_silu_mul_quantize(
+        xd, cps[i % 2][0], cps[i % 2][1], gg, gstat, hq2, hs2, wsf), 4, 5)
+    tf = 2.0 * wl.M * wl.N * wl.K / (ms * 1e-3) / 1e12
+    rows["f1_gate_up_silu_quant_fused_M%d_K%d_I%d" % (wl.M, wl.K, If)] = {
+        "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
+        "frac_bf16_peak": round(tf / pk["bf16_tflops"], 4)}
+    gu2 = torch.empty(wl.M, wl.N, dtype=torch.bfloat16, device="cuda")
+    wsg = torch.zeros(nv.nvfp4_workspace_bytes(1, wl.M, wl.K, wl.N), dtype=torch.uint8,
+                      device="cuda")
+
+    def chain(i):
+        nv.nvfp4_linear(xd, cps[i % 2][0], cps[i % 2][1], gg, gu2, workspace=wsg)
+        nv.nvfp4_silu_mul_quantize(gu2, hq2, hs2, hg2, gstat)
+
+    ms = time_graph(torch, chain, 4, 5)
+    rows["f1_gate_up_then_silu_quant_two_kernels_M%d_K%d_I%d" % (wl.M, wl.K, If)] = {
+        "us": round(ms * 1e3, 1)}
+    del cps, p, z, gu2
     # a6 activation quantization (bf16 x 2048 x 5120) and a7 the W4A4 block-scaled GEMM
     # (the call quantizes x itself, so its time includes a6)
     wl = WORKLOADS["w4a4"]

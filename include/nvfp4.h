@@ -289,13 +289,59 @@ nvfp4_status nvfp4_linear_nvfp4_x(const uint8_t* x_packed, const uint8_t* x_scal
                                   nvfp4_dtype y_dtype, int flags, void* workspace,
                                   size_t workspace_bytes, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_linear_silu_mul_quantize -- the MLP's gate/up projection with its activation
+ * quantized to NVFP4 in the same pass (the epilogue of the gate/up GEMM).
+ *
+ * Defines: FlashRT docs/qwen36_usage.md, env-var table: FLASHRT_QWEN36_FUSE_MLP_GATE_UP
+ * (gate and up as one NVFP4 GEMM, for checkpoints whose gate and up share their scales)
+ * followed by FLASHRT_QWEN36_FUSE_SILU_MUL_QUANT (silu(gate) * up quantized to NVFP4 for
+ * the down projection).  With gu = the bf16 output of the gate/up projection,
+ *   gu = bf16(x . W^T)  [M, 2I], gate in columns [0, I), up in [I, 2I)
+ * (each output rounded to bf16 once, as nvfp4_linear with a bf16 y rounds it), the call
+ * writes h = silu(gate) * up quantized with the static global scale *h_global_scale --
+ * exactly what nvfp4_silu_mul_quantize(gu, ..., given_global_scale = h_global_scale)
+ * writes -- without writing gu to memory.
+ * Arguments:
+ *   x                 bf16 [M, K] row-major; M >= 1, K >= 32, K % 32 == 0.
+ *   w_packed, w_scales_swizzled, w_global_scale: the stacked weight [gate; up] of 2I rows
+ *                     and K columns with one global scale, as nvfp4_quantize and
+ *                     nvfp4_repack produce it.
+ *   I                 columns of h: I >= 16, I % 16 == 0 (I % 32 == 0 to feed
+ *                     nvfp4_linear_nvfp4_x).
+ *   h_global_scale    the static global scale of h (device float, finite, > 0); the down
+ *                     projection takes the same pointer as its x_global_scale.
+ *   h_packed          out [M, I/2] codes.
+ *   h_scales_swizzled out, the tensor-core scale atoms of an [M, I] tensor (padding rows
+ *                     and blocks written as zero); h_scales_bytes at least
+ *                     ceil(M/128)*128 * ceil(I/64)*4.
+ *   flags             0 or NVFP4_STATIC_WEIGHTS (as for nvfp4_linear).
+ *   workspace         >= nvfp4_workspace_bytes(2, M, K, I, 0) bytes; first 4 bytes the
+ *                     error word; zeroed once when allocated.
+ * Alignment: x, the weights, h_packed, h_scales_swizzled, workspace 16 bytes; the global
+ * scales 4 bytes.
+ * Dispatch: M > 16 with I % 128 == 0 runs one tcgen05 GEMM whose tiles pair 64 gate rows
+ * with the 64 matching up rows; its epilogue rounds both to bf16, forms h and quantizes it
+ * (nothing but the codes and scales reaches memory).  Other shapes write gu into the
+ * workspace with nvfp4_linear's kernels and quantize it with nvfp4_silu_mul_quantize's.
+ */
+nvfp4_status nvfp4_linear_silu_mul_quantize(const void* x, int64_t M, int64_t K,
+                                            const uint8_t* w_packed,
+                                            const uint8_t* w_scales_swizzled,
+                                            const float* w_global_scale, int64_t I,
+                                            const float* h_global_scale, uint8_t* h_packed,
+                                            uint8_t* h_scales_swizzled, size_t h_scales_bytes,
+                                            int flags, void* workspace, size_t workspace_bytes,
+                                            nvfp4_stream_t stream);
+
 /* ---- host-only helpers: no device work ---------------------------------------- */
 
 /* Bytes of the swizzled scale layout for a [rows, cols] tensor (0 on bad sizes). */
 size_t nvfp4_repack_bytes(int64_t rows, int64_t cols);
 
 /* Workspace bytes: op 0 = nvfp4_quantize(rows=M, cols=K), op 1 = nvfp4_linear(M, K,
- * N, mode).  0 when no workspace is needed; (size_t)-1 on bad arguments. */
+ * N, mode), op 2 = nvfp4_linear_silu_mul_quantize(M, K, I = N; mode ignored).  0 when no
+ * workspace is needed; (size_t)-1 on bad arguments. */
 size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N, nvfp4_mode mode);
 
 /* Where nvfp4_linear in W4A4 mode leaves the quantized activations inside its

@@ -30,7 +30,7 @@ EXPORTS = ("nvfp4_quantize", "nvfp4_repack", "nvfp4_linear", "nvfp4_repack_bytes
            "nvfp4_workspace_bytes", "nvfp4_w4a4_workspace_layout", "nvfp4_workspace_error",
            "nvfp4_status_str", "nvfp4_encode_elements", "nvfp4_quantize_noalloc",
            "nvfp4_last_cuda_error", "nvfp4_quantize_fp8_block128", "nvfp4_silu_mul_quantize",
-           "nvfp4_linear_nvfp4_x")
+           "nvfp4_linear_nvfp4_x", "nvfp4_linear_silu_mul_quantize")
 
 
 class Nvfp4Error(RuntimeError):
@@ -68,6 +68,8 @@ def load(path: str = LIB_PATH):
         "nvfp4_quantize_fp8_block128": (I, [P, P, I64, I64, P, P, P, P, SZ, P]),
         "nvfp4_silu_mul_quantize": (I, [P, I64, I64, P, P, SZ, P, P, P, SZ, P]),
         "nvfp4_linear_nvfp4_x": (I, [P, P, P, I64, I64, P, P, P, I64, P, I, I, P, SZ, P]),
+        "nvfp4_linear_silu_mul_quantize": (I, [P, I64, I64, P, P, P, I64, P, P, P, SZ, I, P,
+                                               SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -231,6 +233,24 @@ def nvfp4_linear_nvfp4_x(x_packed: torch.Tensor, x_scales_swizzled: torch.Tensor
                                      _p(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream))
     _check(st, "nvfp4_linear_nvfp4_x")
+
+
+def nvfp4_linear_silu_mul_quantize(x: torch.Tensor, w_packed: torch.Tensor,
+                                   w_scales_swizzled: torch.Tensor, w_global_scale: torch.Tensor,
+                                   h_global_scale: torch.Tensor, h_packed: torch.Tensor,
+                                   h_scales_swizzled: torch.Tensor, workspace: torch.Tensor,
+                                   stream=None, static_weights: bool = False) -> None:
+    """The gate/up projection (W = [gate; up], 2I rows) with silu(gate) * up quantized to
+    NVFP4 (static global scale) in the same pass: h codes [M, I/2] and scale atoms."""
+    M, K = x.shape
+    I = w_packed.shape[0] // 2
+    st = load().nvfp4_linear_silu_mul_quantize(
+        _p(x), M, K, _p(w_packed), _p(w_scales_swizzled), _p(w_global_scale), I,
+        _p(h_global_scale), _p(h_packed), _p(h_scales_swizzled),
+        h_scales_swizzled.numel() * h_scales_swizzled.element_size(),
+        NVFP4_STATIC_WEIGHTS if static_weights else 0, _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nvfp4_linear_silu_mul_quantize")
 
 
 def nvfp4_encode_elements(inp: torch.Tensor, e2m1_out: torch.Tensor | None,

@@ -8,47 +8,20 @@
 // one correctly rounded operation per step, and quantized by the NVFP4 block rule without
 // being stored: pass 1 writes amax partials of |h| (skipped with a static global scale),
 // pass 2 recomputes h per 16-element block and writes codes and tensor-core scale atoms.
-//
-// The NVFP4 codes of h hang on the last bit of exp, so exp is not the library's expf
-// (which is not correctly rounded) but a fixed sequence of fp32 operations: W. J. Cody
-// and W. Waite's argument reduction ("Software Manual for the Elementary Functions",
-// 1980) and the Taylor series of e^r to r^7, with the constants rounded to nearest.
+// silu(g) * u is the fixed sequence of fp32 operations of silu.cuh (its exp is not the
+// library's expf), which the gate/up GEMM's fused epilogue shares.
 #include <cuda_fp16.h>
 
 #include "../../include/nvfp4.h"
 #include "common.cuh"
 #include "gemv_helpers.cuh"
 #include "internal.h"
+#include "silu.cuh"
 
 namespace nvfp4 {
 namespace {
 
 constexpr int kThreads = 256;
-
-// exp(x) in fp32: n = rint(x log2 e); r = x - n ln2 (ln2 as a 16-bit head, so n * head is
-// exact, plus a tail); e^r by Horner's rule on 1/k!, k <= 7 (|r| <= ln2/2 + a little);
-// times 2^n.  x > 88 gives +inf and x < -87 gives 0, which keeps 2^n a normal float.
-__device__ __forceinline__ float exp_cody_waite(float x) {
-    if (x > 88.0f) return __int_as_float(0x7f800000);
-    if (x < -87.0f) return 0.0f;
-    const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
-    float r = __fmaf_rn(-n, 0x1.62e4p-1f, x);
-    r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
-    float p = 0x1.a01a02p-13f;
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    const float e = exp_cody_waite(-g);
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, e)), u);
-}
 
 // the 16 values of h in block b of row m (gate at column 16 b, up at I + 16 b)
 __device__ __forceinline__ void h_block(const uint16_t* __restrict__ gu, int64_t I, int64_t m,
@@ -108,7 +81,7 @@ quantize_silu_kernel(const uint16_t* __restrict__ gu, int64_t M, int64_t I,
                      const float* __restrict__ given_g, uint8_t* __restrict__ packed,
                      uint8_t* __restrict__ scales, float* __restrict__ g_out) {
     const float g = cta_global_scale(given_g, partials, npartials);
-    if (blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
+    if (g_out && blockIdx.x == 0 && threadIdx.x == 0) *g_out = g;
     const int64_t cb_n = I >> 4, cp4 = (cb_n + 3) >> 2;
     const int64_t cb_iter = cp4 << 2, nblk = ((M + 127) >> 7 << 7) * cb_iter;
     for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < nblk;

@@ -42,6 +42,7 @@
 
 #include <atomic>
 
+#include "silu.cuh"
 #include "tcgen05.cuh"
 
 namespace nvfp4 {
@@ -60,16 +61,26 @@ constexpr int kTmemCols = 512;
 constexpr uint32_t kXBytes = kBM * kBK * 2;       // 32 KB
 constexpr uint32_t kABytes = kBN * kBK * 2;       // 16 KB
 constexpr uint32_t kCodeBytes = kBN * kBK / 2;    // 4 KB
-constexpr uint32_t kScaleBytes = 512;             // one 128 x 4 scale atom
-constexpr uint32_t kOffX = 0;
-constexpr uint32_t kOffA = kOffX + kStages * kXBytes;
-constexpr uint32_t kOffCode = kOffA + kStages * kABytes;
-constexpr uint32_t kOffScale = kOffCode + kStages * kCodeBytes;
-constexpr uint32_t kOffBar = kOffScale + kStages * kScaleBytes;
-constexpr uint32_t kNumBars = 3 * kStages + 4 + 1;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemUsed = kOffMisc + 16;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+constexpr uint32_t kAtomBytes = 512;              // one 128 x 4 scale atom
+
+// Shared-memory layout.  The fused gate/up variant takes two scale atoms per stage (the
+// gate rows' and the up rows' 128-row blocks) and two exchange tiles through which the
+// gate warps of the epilogue hand silu(gate) to the up warps (32 x 33 floats each).
+template <bool kFuse>
+struct Smem {
+    static constexpr uint32_t kScaleBytes = kFuse ? 2 * kAtomBytes : kAtomBytes;
+    static constexpr uint32_t kOffX = 0;
+    static constexpr uint32_t kOffA = kOffX + kStages * kXBytes;
+    static constexpr uint32_t kOffCode = kOffA + kStages * kABytes;
+    static constexpr uint32_t kOffScale = kOffCode + kStages * kCodeBytes;
+    static constexpr uint32_t kOffXch = kOffScale + kStages * kScaleBytes;
+    static constexpr uint32_t kXchBytes = kFuse ? 2 * 32 * 33 * 4 : 0;
+    static constexpr uint32_t kOffBar = kOffXch + kXchBytes;
+    static constexpr uint32_t kNumBars = 3 * kStages + 4 + 1;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr uint32_t kUsed = kOffMisc + 16;
+    static constexpr uint32_t kBytes = kUsed + 1024;  // slack for 1024-byte alignment
+};
 
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major, M x N.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -86,18 +97,104 @@ __device__ __forceinline__ uint32_t deq_bf16x2(uint32_t h2, uint32_t s16) {
     return d;
 }
 
+// Arguments of the fused gate/up variant (unused by the plain GEMM).  W is the stacked
+// [gate; up] weight [2I, K]; the CTA tile of work item nb takes gate rows 64 nb .. 64 nb + 63
+// as its W rows 0..63 and the matching up rows I + 64 nb .. as rows 64..127, so that the
+// epilogue holds gate and up of the same columns of h.
+struct FuseArgs {
+    int I = 0;                       // columns of h; I % 128 == 0
+    const float* gh = nullptr;       // static global scale of h (device)
+    uint8_t* hq = nullptr;           // h codes [M, I/2]
+    uint8_t* hs = nullptr;           // h scale atoms (rows padded to 128, blocks to 4)
+};
+
+// Row pitch (floats) of the exchange tiles: 32 values plus one, so that a warp writing a
+// row and a warp reading a column both touch 32 distinct banks.
+constexpr int kXchPitch = 33;
+
+// Epilogue of one whole tile of the fused gate/up variant.  TMEM lanes 0..63 hold gate
+// columns 64 nb + l of h, lanes 64..127 the up columns; warps q = 0, 1 read gate
+// (their 32 lanes each), warps q = 2, 3 up, for the same 32 columns of h (q & 1).  Per 32
+// accumulator columns (32 rows m of x):
+//   - the gate warps round gw * acc to bf16 (the gate/up GEMM's output) and write
+//     silu(gate) into their exchange tile, [m][i];
+//   - the up warps round their values the same way and overwrite each entry with
+//     h = silu(g) * u; then lane l takes row m = l of the tile -- the 32 columns of h it
+//     holds are two whole 16-element blocks -- and quantizes both with the quantizer's
+//     one-thread block rule and the static global scale: 16 bytes of codes, 2 scale bytes.
+// Rows past M get no codes; their scale bytes inside the last 128-row block are zero.
+__device__ __forceinline__ void epilogue_silu_quant(uint32_t acc, int q, int lane, int tile,
+                                                    int ntiles_m, float gw, const FuseArgs& fa,
+                                                    float* xch, int M, uint32_t accempty) {
+    const int nb = tile / ntiles_m, mb = tile % ntiles_m;
+    const uint32_t taddr = acc + ((uint32_t)(q * 32) << 16);
+    const float g = *fa.gh;
+    const int64_t cp4 = (fa.I / 16 + 3) / 4;
+    const int m_pad = (M + 127) / 128 * 128;
+    const int ibase = nb * 64 + (q & 1) * 32;   // this warp pair's 32 columns of h
+    float* xw = xch + (q & 1) * 32 * kXchPitch;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBM; c0 += 32) {
+        uint32_t u[32];
+        tc::tmem_ld32(taddr + c0, u);
+        if (q < 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                xw[j * kXchPitch + lane] =
+                    silu_f32(bf16_to_f32(f32_to_bf16_rne(__uint_as_float(u[j]) * gw)));
+        }
+        named_bar_sync(1, 128);
+        if (q >= 2) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float up = bf16_to_f32(f32_to_bf16_rne(__uint_as_float(u[j]) * gw));
+                xw[j * kXchPitch + lane] = __fmul_rn(xw[j * kXchPitch + lane], up);
+            }
+            __syncwarp();
+            const int m = mb * kBM + c0 + lane;
+            if (m < m_pad) {
+                uint32_t code[4], s8[2];
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    float t[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) t[k] = xw[lane * kXchPitch + 16 * hb + k];
+                    s8[hb] = quantize_block16(t, g, code[2 * hb], code[2 * hb + 1]);
+                }
+                // the two blocks are scale columns ibase/16 and ibase/16 + 1, adjacent bytes
+                // of one 4-column group of the atom
+                uint16_t* sp = reinterpret_cast<uint16_t*>(
+                    fa.hs + swizzle_offset(m, ibase / 16, cp4));
+                if (m < M) {
+                    *reinterpret_cast<uint4*>(fa.hq + (int64_t)m * (fa.I / 2) + ibase / 2) =
+                        make_uint4(code[0], code[1], code[2], code[3]);
+                    *sp = (uint16_t)(s8[0] | (s8[1] << 8));
+                } else {
+                    *sp = 0;
+                }
+            }
+        }
+        named_bar_sync(1, 128);
+    }
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) tc::arrive(accempty);
+}
+
+template <bool kFuse>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                   const __grid_constant__ CUtensorMap tmap_w, const uint8_t* __restrict__ wsz,
                   const float* __restrict__ gw, void* __restrict__ y, int y_bf16, int M, int N,
                   int nkb, int ntiles_m, int ntiles, int ntiles_sk, int p_sk, int64_t tsk,
                   uint32_t* __restrict__ err, uint32_t* __restrict__ counters,
-                  float* __restrict__ slots) {
+                  float* __restrict__ slots, FuseArgs fa) {
+    using L = Smem<kFuse>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_s - raw_s);
-    const uint32_t bar0 = base_s + kOffBar;
+    const uint32_t bar0 = base_s + L::kOffBar;
     // barrier addresses (shared space)
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto afull = [&](int s) { return bar0 + 8u * (kStages + s); };
@@ -106,8 +203,8 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
     auto accempty = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };
     const uint32_t drain = bar0 + 8u * (3 * kStages + 4);
     auto bar_ptr = [&](uint32_t a) { return reinterpret_cast<uint64_t*>(base + (a - base_s)); };
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -124,7 +221,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tc::tmem_alloc(base_s + kOffMisc, kTmemCols);
+    if (warp == 1) tc::tmem_alloc(base_s + L::kOffMisc, kTmemCols);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -143,14 +240,29 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     if (it >= kStages &&
                         !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err))
                         break;
-                    mbar_arrive_expect_tx(bar_ptr(full(s)), kXBytes + kCodeBytes + kScaleBytes);
-                    tc::tma_load_2d(base_s + kOffX + s * kXBytes, &tmap_x, kb * kBK, mb * kBM,
+                    mbar_arrive_expect_tx(bar_ptr(full(s)),
+                                          kXBytes + kCodeBytes + L::kScaleBytes);
+                    tc::tma_load_2d(base_s + L::kOffX + s * kXBytes, &tmap_x, kb * kBK, mb * kBM,
                                     full(s));
-                    tc::tma_load_2d(base_s + kOffCode + s * kCodeBytes, &tmap_w, kb * (kBK / 2),
-                                    nb * kBN, full(s));
-                    bulk_g2s(base + kOffScale + s * kScaleBytes,
-                             wsz + ((size_t)nb * nkb + kb) * kScaleBytes, kScaleBytes,
-                             bar_ptr(full(s)));
+                    uint8_t* sc = base + L::kOffScale + s * L::kScaleBytes;
+                    if constexpr (kFuse) {
+                        // 64 gate rows, then the 64 matching up rows; the scale atoms of
+                        // their two 128-row blocks (I % 128 == 0)
+                        const uint32_t cs = base_s + L::kOffCode + s * kCodeBytes;
+                        tc::tma_load_2d(cs, &tmap_w, kb * (kBK / 2), nb * 64, full(s));
+                        tc::tma_load_2d(cs + kCodeBytes / 2, &tmap_w, kb * (kBK / 2),
+                                        fa.I + nb * 64, full(s));
+                        bulk_g2s(sc, wsz + ((size_t)(nb >> 1) * nkb + kb) * kAtomBytes,
+                                 kAtomBytes, bar_ptr(full(s)));
+                        bulk_g2s(sc + kAtomBytes,
+                                 wsz + ((size_t)(fa.I / 128 + (nb >> 1)) * nkb + kb) * kAtomBytes,
+                                 kAtomBytes, bar_ptr(full(s)));
+                    } else {
+                        tc::tma_load_2d(base_s + L::kOffCode + s * kCodeBytes, &tmap_w,
+                                        kb * (kBK / 2), nb * kBN, full(s));
+                        bulk_g2s(sc, wsz + ((size_t)nb * nkb + kb) * kAtomBytes, kAtomBytes,
+                                 bar_ptr(full(s)));
+                    }
                     issued = it + 1;
                 }
             }
@@ -181,8 +293,8 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t a_s = base_s + kOffA + s * kABytes;
-                    const uint32_t x_s = base_s + kOffX + s * kXBytes;
+                    const uint32_t a_s = base_s + L::kOffA + s * kABytes;
+                    const uint32_t x_s = base_s + L::kOffX + s * kXBytes;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         tc::mma_bf16(d, tc::sw128_desc(a_s + kk * 32), tc::sw128_desc(x_s + kk * 32),
@@ -205,13 +317,23 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
         int tile, kb0, kb1;
         for (; wi.next(tile, kb0, kb1); ++lt) {
             const int b = lt & 1;
-            if (!__all_sync(0xffffffffu,
-                            tc::wait_or_abort(accfull(b), (lt >> 1) & 1, abort_flag, err)))
-                break;
-            tc::fence_after();
-            tc::epilogue_work<kBN, kBM>(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m,
-                                        kb0 == 0 && kb1 == nkb, nkb, p_sk, tsk, g, y, y_bf16, M,
-                                        N, slots, counters, accempty(b));
+            const bool ok = __all_sync(0xffffffffu,
+                                       tc::wait_or_abort(accfull(b), (lt >> 1) & 1, abort_flag,
+                                                         err));
+            if constexpr (kFuse) {
+                // the four warps meet at named barriers inside the tile: they leave together
+                // (any warp's failed wait stops all four)
+                if (named_bar_red_or(1, 128, !ok)) break;
+                tc::fence_after();
+                epilogue_silu_quant(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m, g, fa,
+                                    reinterpret_cast<float*>(base + L::kOffXch), M, accempty(b));
+            } else {
+                if (!ok) break;
+                tc::fence_after();
+                tc::epilogue_work<kBN, kBM>(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m,
+                                            kb0 == 0 && kb1 == nkb, nkb, p_sk, tsk, g, y, y_bf16,
+                                            M, N, slots, counters, accempty(b));
+            }
         }
     } else {
         // ---------------- dequantize ----------------
@@ -221,6 +343,14 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
         tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
         int tile, kb0, kb1;
         while (wi.next(tile, kb0, kb1)) {
+            // the row's line in the scale atom(s): the fused variant's rows 0..63 are gate
+            // rows of atom 0, rows 64..127 up rows of atom 1, both at row 64 (nb & 1) + r % 64
+            // of their 128-row block
+            int arow = r, aoff = 0;
+            if constexpr (kFuse) {
+                arow = (((tile / ntiles_m) & 1) << 6) | (r & 63);
+                aoff = (r >> 6) * kAtomBytes;
+            }
             bool ok = true;
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % kStages;
@@ -229,14 +359,15 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                     ok = false;
                     break;
                 }
-                const uint4 c = *reinterpret_cast<const uint4*>(base + kOffCode + s * kCodeBytes +
-                                                                r * 32 + h * 16);
+                const uint4 c = *reinterpret_cast<const uint4*>(base + L::kOffCode +
+                                                                s * kCodeBytes + r * 32 + h * 16);
                 const uint32_t sb = *reinterpret_cast<const uint16_t*>(
-                    base + kOffScale + s * kScaleBytes + (r & 31) * 16 + (r >> 5) * 4 + 2 * h);
+                    base + L::kOffScale + s * L::kScaleBytes + aoff + (arow & 31) * 16 +
+                    (arow >> 5) * 4 + 2 * h);
                 // the two block scales as f16 (e4m3 is exact in f16)
                 const uint32_t s01 = cvt_e4m3x2_f16x2(sb);
                 const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-                uint8_t* arow = base + kOffA + s * kABytes + r * 128;
+                uint8_t* arow_s = base + L::kOffA + s * kABytes + r * 128;
 #pragma unroll
                 for (int qd = 0; qd < 4; ++qd) {
                     uint32_t hh[4];
@@ -246,7 +377,8 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
                     for (int i = 0; i < 4; ++i) o[i] = deq_bf16x2(hh[i], sc);
                     const int chunk = (4 * h + qd) ^ (r & 7);
-                    *reinterpret_cast<uint4*>(arow + chunk * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(arow_s + chunk * 16) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
@@ -265,6 +397,18 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
 }
 
+template <bool kFuse>
+cudaError_t configure(const DevInfo& dev) {
+    static std::atomic<uint64_t> configured{0};
+    const uint64_t bit = 1ull << (dev.device & 63);
+    if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(gemm_w4a16_kernel<kFuse>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)Smem<kFuse>::kBytes);
+    if (e == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
 }  // namespace
 
 GemmPlan gemm_w4a16_plan(int64_t M, int64_t K, int64_t N, int sm_count) {
@@ -278,7 +422,7 @@ size_t gemm_w4a16_workspace_bytes(int64_t M, int64_t K, int64_t N) {
 cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz, const float* gw, int N, void* y, bool y_bf16,
                               uint8_t* workspace, cudaStream_t stream, const DevInfo& dev) {
-    if (dev.smem_optin < kSmemBytes) return cudaErrorInvalidConfiguration;
+    if (dev.smem_optin < Smem<false>::kBytes) return cudaErrorInvalidConfiguration;
     const GemmPlan p = gemm_w4a16_plan(M, K, N, dev.sm_count);
     CUtensorMap mx, mw;
     cudaError_t e = tc::make_map_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K,
@@ -287,21 +431,51 @@ cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
     e = tc::make_map_2d(&mw, wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)N,
                         kBK / 2, kBN, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
-    static std::atomic<uint64_t> configured{0};
-    const uint64_t bit = 1ull << (dev.device & 63);
-    if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(gemm_w4a16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured.fetch_or(bit, std::memory_order_acq_rel);
-    }
+    e = configure<false>(dev);
+    if (e != cudaSuccess) return e;
     uint32_t* err = reinterpret_cast<uint32_t*>(workspace);
     uint32_t* counters = reinterpret_cast<uint32_t*>(workspace + kGemmHeaderBytes);
     float* slots = reinterpret_cast<float*>(workspace + kGemmHeaderBytes +
                                             tc::counters_bytes(p.ntiles));
-    gemm_w4a16_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(
+    gemm_w4a16_kernel<false><<<p.grid, kThreads, Smem<false>::kBytes, stream>>>(
         mx, mw, wsz, gw, y, y_bf16 ? 1 : 0, M, N, p.nkb, p.ntiles_m, p.ntiles, p.ntiles_sk, p.p_sk,
-        p.tsk, err, counters, slots);
+        p.tsk, err, counters, slots, FuseArgs{});
+    return cudaGetLastError();
+}
+
+bool gemm_w4a16_silu_takes(int64_t M, int64_t I, const DevInfo& dev) {
+    return M > kGemvMaxM && I % 128 == 0 && dev.smem_optin >= Smem<true>::kBytes;
+}
+
+cudaError_t launch_gemm_w4a16_silu(const uint16_t* x, int M, int K, const uint8_t* wq,
+                                   const uint8_t* wsz, const float* gw, int I, const float* gh,
+                                   uint8_t* hq, uint8_t* hs, uint32_t* err, cudaStream_t stream,
+                                   const DevInfo& dev) {
+    if (!gemm_w4a16_silu_takes(M, I, dev)) return cudaErrorInvalidConfiguration;
+    // whole tiles only (each tile needs gate and up complete before the activation):
+    // 64-column pairs of h x 256 rows of x, persistent CTAs
+    GemmPlan p;
+    p.nkb = (K + kBK - 1) / kBK;
+    p.ntiles_m = (M + kBM - 1) / kBM;
+    p.ntiles = (I / 64) * p.ntiles_m;
+    p.grid = p.ntiles < dev.sm_count ? p.ntiles : dev.sm_count;
+    CUtensorMap mx, mw;
+    cudaError_t e = tc::make_map_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K,
+                                    (uint64_t)M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    e = tc::make_map_2d(&mw, wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2,
+                        (uint64_t)2 * I, kBK / 2, kBN / 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    e = configure<true>(dev);
+    if (e != cudaSuccess) return e;
+    FuseArgs fa;
+    fa.I = I;
+    fa.gh = gh;
+    fa.hq = hq;
+    fa.hs = hs;
+    gemm_w4a16_kernel<true><<<p.grid, kThreads, Smem<true>::kBytes, stream>>>(
+        mx, mw, wsz, gw, nullptr, 1, M, 2 * I, p.nkb, p.ntiles_m, p.ntiles, 0, 0, 0, err,
+        nullptr, nullptr, fa);
     return cudaGetLastError();
 }
 

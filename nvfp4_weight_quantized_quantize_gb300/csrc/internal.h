@@ -37,7 +37,8 @@ cudaError_t launch_quantize_fp8_b128(const uint8_t* src, const float* block_scal
 
 // h = silu(gate) * up from bf16 gate_up [M, 2I] (gate columns [0, I)), quantized to NVFP4:
 // codes [M, I/2], scales in the tensor-core atoms (rows padded to 128, blocks to 4, zero
-// padding), g_out.  Pass 1 (amax partials) only when given_g is null.
+// padding), g_out (may be null with a given scale).  Pass 1 (amax partials) only when
+// given_g is null.
 cudaError_t launch_silu_mul_quantize(const uint16_t* gate_up, int64_t M, int64_t I,
                                      uint8_t* packed, uint8_t* scales, float* g_out,
                                      const float* given_g, float* partials, int npartials,
@@ -100,6 +101,17 @@ size_t gemm_w4a16_workspace_bytes(int64_t M, int64_t K, int64_t N);
 cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                               const uint8_t* wsz, const float* gw, int N, void* y, bool y_bf16,
                               uint8_t* workspace, cudaStream_t stream, const DevInfo& dev);
+
+// The gate/up projection fused with the activation: W = [gate; up] stacked [2I, K] (one
+// global scale gw, wsz its atom part), h = silu(bf16(x . gate^T)) * bf16(x . up^T) quantized
+// to NVFP4 with the static global scale *gh in the GEMM's epilogue: codes hq [M, I/2], scale
+// atoms hs (rows padded to 128 and blocks to 4, padding zero).  Taken when
+// gemm_w4a16_silu_takes(M, I): M > 16 and I % 128 == 0.  err: the workspace error word.
+bool gemm_w4a16_silu_takes(int64_t M, int64_t I, const DevInfo& dev);
+cudaError_t launch_gemm_w4a16_silu(const uint16_t* x, int M, int K, const uint8_t* wq,
+                                   const uint8_t* wsz, const float* gw, int I, const float* gh,
+                                   uint8_t* hq, uint8_t* hs, uint32_t* err, cudaStream_t stream,
+                                   const DevInfo& dev);
 
 // M > 16 W4A4 GEMM (block-scaled tcgen05.mma, kind::mxf4nvf4).  xq [M, K/2] and xsz (scale
 // atoms of x) and gx come from the quantizer; wsz: the atom part of W's repacked scales.

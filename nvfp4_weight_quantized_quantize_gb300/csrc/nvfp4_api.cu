@@ -118,6 +118,27 @@ W4A4Layout w4a4_layout(int64_t M, int64_t K, int64_t N) {
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
+// nvfp4_linear_silu_mul_quantize's workspace: the fused GEMM needs only the error word;
+// otherwise the linear's own workspace (error word first), then gu bf16 [M, 2I]
+struct SiluLayout {
+    bool fused;
+    size_t gu, total;
+};
+
+SiluLayout silu_layout(int64_t M, int64_t K, int64_t I) {
+    SiluLayout L;
+    L.fused = M > kGemvMaxM && I % 128 == 0;
+    if (L.fused) {
+        L.gu = 0;
+        L.total = kHeaderBytes;
+        return L;
+    }
+    const size_t lin = M <= kGemvMaxM ? kHeaderBytes : gemm_w4a16_workspace_bytes(M, K, 2 * I);
+    L.gu = round_up(lin, 256);
+    L.total = L.gu + (size_t)(M * 2 * I * 2);
+    return L;
+}
+
 }  // namespace
 }  // namespace nvfp4
 
@@ -154,6 +175,10 @@ NVFP4_API size_t nvfp4_workspace_bytes(int op, int64_t M, int64_t K, int64_t N,
     if (op == 0) {
         if (M < 1 || K < 16 || K % 16 != 0) return (size_t)-1;
         return kHeaderBytes + (size_t)kMaxPartials * 4;
+    }
+    if (op == 2) {
+        if (M < 1 || K < 32 || K % 32 != 0 || N < 16 || N % 16 != 0) return (size_t)-1;
+        return silu_layout(M, K, N).total;
     }
     if (op != 1 || M < 1 || K < 32 || K % 32 != 0 || N < 1) return (size_t)-1;
     if (mode == NVFP4_W4A16)
@@ -335,6 +360,52 @@ NVFP4_API nvfp4_status nvfp4_silu_mul_quantize(const void* gate_up, int64_t M, i
                                               packed, scales_swizzled, global_scale,
                                               given_global_scale, partials,
                                               partial_count(M * I, d), stream, d));
+}
+
+NVFP4_API nvfp4_status nvfp4_linear_silu_mul_quantize(
+    const void* x, int64_t M, int64_t K, const uint8_t* w_packed,
+    const uint8_t* w_scales_swizzled, const float* w_global_scale, int64_t I,
+    const float* h_global_scale, uint8_t* h_packed, uint8_t* h_scales_swizzled,
+    size_t h_scales_bytes, int flags, void* workspace, size_t workspace_bytes,
+    nvfp4_stream_t stream) {
+    if (!x || !w_packed || !w_scales_swizzled || !w_global_scale || !h_global_scale ||
+        !h_packed || !h_scales_swizzled || !workspace)
+        return NVFP4_ERR_NULL;
+    if (flags & ~NVFP4_STATIC_WEIGHTS) return NVFP4_ERR_DTYPE;
+    if (M < 1 || K < 32 || K % 32 != 0 || I < 16 || I % 16 != 0 || M > kMaxDim ||
+        K > kMaxDim || I > kMaxDim / 2)
+        return NVFP4_ERR_SHAPE;
+    if (h_scales_bytes < repack_atom_bytes(M, I)) return NVFP4_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(w_packed, 16) || !aligned(w_scales_swizzled, 16) ||
+        !aligned(h_packed, 16) || !aligned(h_scales_swizzled, 16) || !aligned(workspace, 16) ||
+        !aligned(w_global_scale, 4) || !aligned(h_global_scale, 4))
+        return NVFP4_ERR_ALIGN;
+    const SiluLayout L = silu_layout(M, K, I);
+    if (workspace_bytes < L.total) return NVFP4_ERR_WORKSPACE;
+    DevInfo d;
+    nvfp4_status st = current_device(&d);
+    if (st != NVFP4_OK) return st;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (L.fused) {
+        if (!gemm_w4a16_silu_takes(M, I, d)) return NVFP4_ERR_UNSUPPORTED;
+        return from_cuda(launch_gemm_w4a16_silu(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                                w_global_scale, (int)I, h_global_scale,
+                                                h_packed, h_scales_swizzled,
+                                                reinterpret_cast<uint32_t*>(ws), stream, d));
+    }
+    uint16_t* gu = reinterpret_cast<uint16_t*>(ws + L.gu);
+    const int N = (int)(2 * I);
+    cudaError_t e = M <= kGemvMaxM
+                        ? small_m(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                  w_global_scale, nullptr, N, gu, true,
+                                  reinterpret_cast<uint32_t*>(ws),
+                                  (flags & NVFP4_STATIC_WEIGHTS) != 0, stream, d)
+                        : launch_gemm_w4a16(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
+                                            w_global_scale, N, gu, true, ws, stream, d);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(launch_silu_mul_quantize(gu, M, I, h_packed, h_scales_swizzled, nullptr,
+                                              h_global_scale, nullptr, 0, stream, d));
 }
 
 NVFP4_API nvfp4_status nvfp4_linear_nvfp4_x(const uint8_t* x_packed,

@@ -180,6 +180,37 @@ def test_linear_nvfp4_x_rejects(lib):
     assert _lx(lib, wsb=64) == WORKSPACE
 
 
+def _ls(lib, x=16, M=4, K=64, wq=32, wsz=48, gw=64, I=32, gh=80, hq=96, hs=112, hsb=512,
+        flags=0, ws=4096, wsb=1 << 20):
+    v = lambda a: None if a is None else ctypes.c_void_p(a)
+    return lib.nvfp4_linear_silu_mul_quantize(v(x), M, K, v(wq), v(wsz), v(gw), I, v(gh),
+                                              v(hq), v(hs), hsb, flags, v(ws), wsb, None)
+
+
+def test_linear_silu_mul_quantize_rejects(lib):
+    assert _ls(lib, x=None) == NULL
+    assert _ls(lib, gh=None) == NULL            # the activation scale is static
+    assert _ls(lib, hq=None) == NULL
+    assert _ls(lib, ws=None) == NULL
+    assert _ls(lib, flags=1) == DTYPE
+    assert _ls(lib, K=48) == SHAPE
+    assert _ls(lib, I=24) == SHAPE
+    assert _ls(lib, M=0) == SHAPE
+    assert _ls(lib, hsb=511) == SHAPE           # 128 rows x 4 blocks of atoms
+    assert _ls(lib, x=24) == ALIGN
+    assert _ls(lib, hs=120) == ALIGN
+    assert _ls(lib, gh=82) == ALIGN
+    assert _ls(lib, wsb=16) == WORKSPACE
+
+
+def test_linear_silu_mul_quantize_workspace_sizes():
+    # fused (M > 16, I % 128 == 0): the error word alone; otherwise room for gu [M, 2I] bf16
+    assert nv.nvfp4_workspace_bytes(2, 512, 5120, 17408) == 256
+    assert nv.nvfp4_workspace_bytes(2, 4, 5120, 17408) >= 256 + 4 * 2 * 17408 * 2
+    assert nv.nvfp4_workspace_bytes(2, 40, 64, 96) >= 40 * 2 * 96 * 2
+    assert nv.nvfp4_workspace_bytes(2, 40, 64, 24) == 2 ** 64 - 1
+
+
 def _r(lib, src=16, rows=4, cols=32, out=32, nbytes=None):
     v = lambda a: None if a is None else ctypes.c_void_p(a)
     if nbytes is None:
