@@ -594,6 +594,16 @@ def measure_rows(torch, nv, setup):
     rows["a7_w4a4_M%d_K%d_N%d_incl_act_quant" % (wl.M, wl.K, wl.N)] = {
         "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
         "frac_fp4_nominal": round(tf / FP4_NOMINAL_TFLOPS, 4)}
+    # f2: the same call with a static activation scale (one quantization pass inside the
+    # GEMM, no amax pass and no grid barrier)
+    gx4 = torch.tensor([0.002], dtype=torch.float32, device="cuda")
+    ms = time_graph(torch, lambda i: nv.nvfp4_linear(xd, cps[i % 2][0], cps[i % 2][1], gg, y,
+                                                     mode="w4a4", x_global_scale=gx4,
+                                                     workspace=wsv), 4, 5)
+    tf = 2.0 * wl.M * wl.N * wl.K / (ms * 1e-3) / 1e12
+    rows["f2_w4a4_static_scale_M%d_K%d_N%d_incl_act_quant" % (wl.M, wl.K, wl.N)] = {
+        "TFLOP/s": round(tf, 1), "us": round(ms * 1e3, 1),
+        "frac_fp4_nominal": round(tf / FP4_NOMINAL_TFLOPS, 4)}
     del cps, p, z
     torch.cuda.synchronize()
     return rows

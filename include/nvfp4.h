@@ -198,7 +198,13 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *          y = g_x g_w * sum_b sx[m,b] sw[n,b] sum_{k in b} e2m1(qx) e2m1(qw).
  *          With a given x_global_scale and M <= 8, the M = 1 GEMV and the skinny GEMM
  *          quantize x themselves (same codes and scales, no pre-pass); x's codes are
- *          then not written to the workspace.
+ *          then not written to the workspace.  At M > 16 the tensor-core GEMM quantizes
+ *          x itself: its CTAs (one per SM, launched cooperatively so that all are
+ *          resident) each quantize a share of x into the workspace -- after an amax
+ *          pass and one grid-wide barrier when the scale is dynamic -- and count
+ *          themselves done; the GEMM's loads of x wait for the count.  One kernel, the
+ *          same bytes in the workspace.  Where the device cannot hold the whole grid at
+ *          once, the call quantizes x in a kernel of its own first.
  * Accumulation is fp32.  Expected accuracy: |y - y_ref| <= 1e-3 * sum_k |x_k w_k|
  * + 2^-8 |y_ref| for bf16 y.
  * Arguments:
@@ -215,9 +221,10 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *                      256-byte header holding the sticky error word), zero-filled once
  *                      at allocation.  Calls that share a workspace must be ordered (one
  *                      stream), since W4A4 keeps the quantized x there.  For M > 16 it
- *                      also holds the tensor-core GEMM's stream-K counters (they must be
- *                      zero before the first call; every call that completes without a
- *                      device error leaves them zero) and fp32 partial tiles.  After a
+ *                      also holds the tensor-core GEMM's stream-K counters and, in
+ *                      W4A4 mode, the counters of its in-kernel quantization (they must
+ *                      be zero before the first call; every call that completes without
+ *                      a device error leaves them zero) and fp32 partial tiles.  After a
  *                      device error (nvfp4_workspace_error != 0), zero-fill it again.
  * Kernels: M = 1 pipelined GEMV; 2 <= M <= 8 streamed skinny GEMM (mma.sync); 9 <= M <=
  * 16 the skinny GEMM on tokens 0..7 and again on the rest where it takes the K, else an

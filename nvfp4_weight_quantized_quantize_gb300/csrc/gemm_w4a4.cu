@@ -4,8 +4,14 @@
 //
 //   y[m, n] = gx * gw * sum_b sx[m, b] * sw[n, b] * sum_{k in b} e2m1(qx[m, k]) * e2m1(qw[n, k])
 //
-// x has been quantized (codes [M, K/2], scale atoms, gx) by the quantizer into the
-// workspace.  tcgen05.mma kind::mxf4nvf4 with 16-element UE4M3 block scales
+// x arrives quantized (codes [M, K/2], scale atoms, gx: the NVFP4 activations of the
+// down projection), or as bf16 that the kernel quantizes itself (the kQuantX variant):
+// after its barriers and TMEM are set up, every CTA quantizes a share of x into the
+// workspace with the quantizer's block rule -- behind an amax pass and one grid-wide
+// barrier when the scale is dynamic -- and counts itself done; the TMA producer waits
+// for the count to reach the grid before its first load of x.  The grid is launched
+// cooperatively (one CTA per SM, all resident), every wait is bounded, and the last CTA
+// to finish zeroes the counters for the next call.  tcgen05.mma kind::mxf4nvf4 with 16-element UE4M3 block scales
 // (scale_vec::4X) multiplies the packed E2M1 operands straight from shared memory; the
 // scales reach TMEM in the layout the block-scaled MMA reads: one 512-byte atom of the
 // tensor-core scale layout (128 rows x 64 K, which is how the repacked scales are stored)
@@ -71,6 +77,122 @@ static_assert(kTmemSf + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 3) << 17) |
                             ((uint32_t)(kBN >> 4) << 24);
 
+// In-kernel quantization of bf16 x (the kQuantX variant): x quantized to NVFP4 by every
+// CTA of the persistent grid together, before and while the GEMM starts.
+struct QxArgs {
+    const uint16_t* x = nullptr;      // bf16 [M, K]
+    const float* gx_static = nullptr; // static global scale of x, or null: amax / 2688
+    float* gx_out = nullptr;          // g_x (written by CTA 0)
+    float* partials = nullptr;        // one amax partial per CTA (dynamic scale)
+    uint32_t* sync = nullptr;         // [0] barrier count, [1] barrier generation,
+                                      // [2] exit count, [3] CTAs whose share of x is written
+    uint8_t* xq = nullptr;            // codes [M, K/2] (the GEMM's x operand)
+    uint8_t* xs = nullptr;            // scale atoms of x (rows padded to 128, blocks to 4)
+    int K = 0;
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// generic-proxy writes to global memory made visible to (and ordered with) the async
+// proxy: the quantized x is written with plain stores and read by TMA in other CTAs
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Spin until *p reaches `target` (acquire), at most kWaitLimitNs; false on time-out.
+__device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (ld_acquire_gpu(p) >= target) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+}
+
+// Grid-wide barrier of the co-resident grid (one thread per CTA): the arrival that
+// completes the count resets it and advances the generation the others wait on.
+__device__ __forceinline__ bool grid_barrier(uint32_t* sync) {
+    volatile uint32_t* gen_p = sync + 1;
+    const uint32_t gen = *gen_p;
+    __threadfence();
+    const uint32_t old = atomicAdd(sync, 1u);
+    if (old == gridDim.x - 1) {
+        atomicExch(sync, 0u);
+        __threadfence();
+        atomicAdd(sync + 1, 1u);
+        return true;
+    }
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(sync + 1) == gen) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Quantize every 16-element block of x (rows padded to 128, blocks to 4): this CTA's share
+// is blocks b = blockIdx.x * threads + t (+ gridDim.x * threads ...), taken kQxBatch at a
+// time with all their loads in flight.  Codes go row-major, scales to the atom layout;
+// padding rows and blocks get zero scales.
+constexpr int kQxBatch = 4;
+
+__device__ __forceinline__ void quantize_x_all(const QxArgs& qa, int M, float g) {
+    const int K = qa.K;
+    const int64_t cb_n = K >> 4, cp4 = (cb_n + 3) >> 2, cb_iter = cp4 << 2;
+    const int64_t nblk = (int64_t)((M + 127) / 128 * 128) * cb_iter;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b0 < nblk;
+         b0 += kQxBatch * stride) {
+        uint4 v[kQxBatch][2];
+        int64_t r[kQxBatch], cb[kQxBatch];
+        bool real[kQxBatch];
+#pragma unroll
+        for (int u = 0; u < kQxBatch; ++u) {
+            const int64_t b = b0 + u * stride;
+            // 32-bit division while the indices fit (every realistic x)
+            r[u] = nblk <= 0xFFFFFFFFll ? (int64_t)((uint32_t)b / (uint32_t)cb_iter)
+                                        : b / cb_iter;
+            cb[u] = b - r[u] * cb_iter;
+            real[u] = b < nblk && r[u] < M && cb[u] < cb_n;
+            if (real[u]) {
+                const uint4* p = reinterpret_cast<const uint4*>(qa.x + r[u] * K + (cb[u] << 4));
+                v[u][0] = __ldg(p);
+                v[u][1] = __ldg(p + 1);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kQxBatch; ++u) {
+            if (b0 + u * stride >= nblk) break;
+            if (!real[u]) {
+                qa.xs[swizzle_offset(r[u], cb[u], cp4)] = 0;
+                continue;
+            }
+            float t[16];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const uint32_t w[4] = {v[u][q].x, v[u][q].y, v[u][q].z, v[u][q].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    t[q * 8 + 2 * j] = bf16_to_f32(w[j] & 0xFFFFu);
+                    t[q * 8 + 2 * j + 1] = bf16_to_f32(w[j] >> 16);
+                }
+            }
+            uint32_t lo, hi;
+            const uint32_t s8 = quantize_block16(t, g, lo, hi);
+            *reinterpret_cast<uint2*>(qa.xq + r[u] * (K >> 1) + (cb[u] << 3)) = make_uint2(lo, hi);
+            qa.xs[swizzle_offset(r[u], cb[u], cp4)] = (uint8_t)s8;
+        }
+    }
+}
+
+template <bool kQuantX>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  const __grid_constant__ CUtensorMap tmap_x, const uint8_t* __restrict__ wsz,
@@ -79,7 +201,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  int nkb, int natoms_row, int x_row_blocks, int ntiles_m, int ntiles,
                  int ntiles_sk, int p_sk,
                  int64_t tsk, uint32_t* __restrict__ err, uint32_t* __restrict__ counters,
-                 float* __restrict__ slots) {
+                 float* __restrict__ slots, QxArgs qa) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -118,6 +240,87 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // ---- x quantized in-kernel (kQuantX): every CTA quantizes a share of x and counts
+    // itself done; the producer waits for the count to reach the grid before its first
+    // load of x ----
+    __shared__ float gx_sh;
+    if constexpr (kQuantX) {
+        __shared__ int qx_fail;
+        if (threadIdx.x == 0) qx_fail = 0;
+        float g = 1.0f;
+        if (qa.gx_static) {
+            g = *qa.gx_static;
+        } else {
+            // amax of x: a partial per CTA, a grid barrier, then every CTA folds them
+            float am = 0.0f;
+            const int64_t nvec = (int64_t)M * qa.K / 8;
+            const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+            const uint4* xv = reinterpret_cast<const uint4*>(qa.x);
+            for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < nvec;
+                 i0 += 8 * stride) {
+                uint4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    v[u] = i0 + u * stride < nvec ? __ldg(xv + i0 + u * stride)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        am = fmaxf(am, fmaxf(fabsf(bf16_to_f32(w[j] & 0xFFFFu)),
+                                             fabsf(bf16_to_f32(w[j] >> 16))));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+            __shared__ float red[kThreads / 32];
+            if (lane == 0) red[warp] = am;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                float r = red[0];
+                for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
+                qa.partials[blockIdx.x] = r;
+                if (!grid_barrier(qa.sync)) {
+                    if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+                    qx_fail = 1;
+                }
+            }
+            __syncthreads();
+            if (!qx_fail) {
+                // every CTA's partial (read from L2: other CTAs wrote them in this kernel)
+                float m = 0.0f;
+                for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x)
+                    m = fmaxf(m, __ldcg(qa.partials + i));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                __syncthreads();
+                if (lane == 0) red[warp] = m;
+                __syncthreads();
+                float r = red[0];
+                for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
+                g = global_scale_from_amax(r);
+            }
+        }
+        if (threadIdx.x == 0) {
+            gx_sh = g;
+            if (blockIdx.x == 0) *qa.gx_out = g;
+        }
+        if (!qx_fail) {
+            quantize_x_all(qa, M, g);
+            // this CTA's share is written: publish it to the async proxy, then count it
+            fence_proxy_async_global();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomicAdd(qa.sync + 3, 1u);
+            }
+        }
+        __syncthreads();
+        if (qx_fail && threadIdx.x == 0) *abort_flag = 1;
+        __syncthreads();
+    }
+
     // scale atoms of K step kb: 4, or fewer at the end of K
     auto atoms_of = [&](int kb) { return min(4, natoms_row - 4 * kb); };
 
@@ -127,6 +330,15 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             int it = 0, issued = 0;
             tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
             int tile, kb0, kb1;
+            if constexpr (kQuantX) {
+                // every CTA's share of the quantized x is written before the first TMA read
+                if (!*abort_flag && !wait_counter(qa.sync + 3, gridDim.x)) {
+                    if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                // the other CTAs' stores, now visible, ahead of the TMA reads below
+                fence_proxy_async_global();
+            }
             while (!*abort_flag && wi.next(tile, kb0, kb1)) {
                 const int nb = tile / ntiles_m, mb = tile % ntiles_m;
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -250,7 +462,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
     } else {
         // ---------------- epilogue ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const float g = *gw * *gx;
+        const float g = *gw * (kQuantX ? gx_sh : *gx);
         int lt = 0;
         tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
         int tile, kb0, kb1;
@@ -271,18 +483,37 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
         tc::fence_after();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+    if constexpr (kQuantX) {
+        // the last CTA out (every other CTA is past all its waits) zeroes the ready counts,
+        // so the workspace is ready for the next call
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(qa.sync + 2, 1u) == gridDim.x - 1) {
+                atomicExch(qa.sync + 3, 0u);
+                atomicExch(qa.sync, 0u);
+                atomicExch(qa.sync + 2, 0u);
+            }
+        }
+    }
 }
 
-}  // namespace
-
-size_t gemm_w4a4_stream_k_bytes(int64_t M, int64_t K, int64_t N) {
-    return tc::stream_k_bytes(M, K, N, kBN, kBM, kBK);
+template <bool kQuantX>
+cudaError_t configure(const DevInfo& dev) {
+    static std::atomic<uint64_t> configured{0};
+    const uint64_t bit = 1ull << (dev.device & 63);
+    if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(gemm_w4a4_kernel<kQuantX>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kSmemBytes);
+    if (e == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
-cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M,
-                             int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
-                             void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
-                             cudaStream_t stream, const DevInfo& dev) {
+template <bool kQuantX>
+cudaError_t launch(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M, int K,
+                   const uint8_t* wq, const uint8_t* wsz, const float* gw, int N, void* y,
+                   bool y_bf16, uint32_t* err, uint8_t* sk_state, const QxArgs& qa,
+                   cudaStream_t stream, const DevInfo& dev) {
     if (dev.smem_optin < kSmemBytes) return cudaErrorInvalidConfiguration;
     const GemmPlan p = tc::make_plan(M, K, N, dev.sm_count, kBN, kBM, kBK);
     CUtensorMap mw, mx;
@@ -292,22 +523,61 @@ cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float*
     e = tc::make_map_2d(&mx, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)M,
                         kBK / 2, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    static std::atomic<uint64_t> configured{0};
-    const uint64_t bit = 1ull << (dev.device & 63);
-    if (!(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(gemm_w4a4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured.fetch_or(bit, std::memory_order_acq_rel);
-    }
+    e = configure<kQuantX>(dev);
+    if (e != cudaSuccess) return e;
     const int natoms_row = (K + 63) / 64;  // scale atoms per 128-row block
     uint32_t* counters = reinterpret_cast<uint32_t*>(sk_state);
     float* slots = reinterpret_cast<float*>(sk_state + tc::counters_bytes(p.ntiles));
-    gemm_w4a4_kernel<<<p.grid, kThreads, kSmemBytes, stream>>>(
-        mw, mx, wsz, xsz, gw, gx, y, y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, (M + 127) / 128,
-        p.ntiles_m,
-        p.ntiles, p.ntiles_sk, p.p_sk, p.tsk, err, counters, slots);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    // the in-kernel quantization has CTAs wait for one another: all of them must be
+    // resident at once (one per SM), which a cooperative launch guarantees or refuses
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = kQuantX ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, gemm_w4a4_kernel<kQuantX>, mw, mx, wsz, xsz, gw, gx, y,
+                           y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, (M + 127) / 128, p.ntiles_m,
+                           p.ntiles, p.ntiles_sk, p.p_sk, p.tsk, err, counters, slots, qa);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_w4a4_stream_k_bytes(int64_t M, int64_t K, int64_t N) {
+    return tc::stream_k_bytes(M, K, N, kBN, kBM, kBK);
+}
+
+size_t gemm_w4a4_sync_bytes(int64_t) { return 256; }
+
+cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M,
+                             int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
+                             void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
+                             cudaStream_t stream, const DevInfo& dev) {
+    return launch<false>(xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16, err, sk_state, QxArgs{},
+                         stream, dev);
+}
+
+cudaError_t launch_gemm_w4a4_quant_x(const uint16_t* x, const float* gx_static, float* gx_out,
+                                     float* partials, uint32_t* sync, uint8_t* xq, uint8_t* xsz,
+                                     int M, int K, const uint8_t* wq, const uint8_t* wsz,
+                                     const float* gw, int N, void* y, bool y_bf16, uint32_t* err,
+                                     uint8_t* sk_state, cudaStream_t stream, const DevInfo& dev) {
+    QxArgs qa;
+    qa.x = x;
+    qa.gx_static = gx_static;
+    qa.gx_out = gx_out;
+    qa.partials = partials;
+    qa.sync = sync;
+    qa.xq = xq;
+    qa.xs = xsz;
+    qa.K = K;
+    return launch<true>(xq, xsz, gx_out, M, K, wq, wsz, gw, N, y, y_bf16, err, sk_state, qa,
+                        stream, dev);
 }
 
 }  // namespace nvfp4

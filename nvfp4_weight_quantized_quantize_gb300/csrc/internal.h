@@ -119,6 +119,19 @@ cudaError_t launch_gemm_w4a16_silu(const uint16_t* x, int M, int K, const uint8_
 // counters (zero before the first call) and partial-tile slots,
 // gemm_w4a4_stream_k_bytes() of them.
 size_t gemm_w4a4_stream_k_bytes(int64_t M, int64_t K, int64_t N);
+// The same GEMM with x given as bf16 [M, K] and quantized inside the kernel: every CTA of
+// the (cooperative, co-resident) grid quantizes a share of x into xq / xsz (the layout
+// and bytes launch_quantize writes) and counts itself done in `sync`; the producers wait
+// for the count to reach the grid before their first load of x.  With
+// gx_static null the global scale is amax / 2688 of x: amax partials, then one grid-wide
+// barrier.  gx_out receives g_x.  sync: gemm_w4a4_sync_bytes(M) bytes, zero before the
+// first call and left zero by every completed call.
+size_t gemm_w4a4_sync_bytes(int64_t M);
+cudaError_t launch_gemm_w4a4_quant_x(const uint16_t* x, const float* gx_static, float* gx_out,
+                                     float* partials, uint32_t* sync, uint8_t* xq, uint8_t* xsz,
+                                     int M, int K, const uint8_t* wq, const uint8_t* wsz,
+                                     const float* gw, int N, void* y, bool y_bf16, uint32_t* err,
+                                     uint8_t* sk_state, cudaStream_t stream, const DevInfo& dev);
 cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M,
                              int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
                              void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,

@@ -99,9 +99,10 @@ int partial_count(int64_t n, const DevInfo& d) {
 }
 
 // W4A4 workspace: header | xq [M, K/2] | xs swizzled | gx (16 B) | partials | deq bf16
-// (M <= 16) | stream-K state of the tensor-core GEMM (M > 16)
+// (M <= 16) | stream-K state of the tensor-core GEMM, then the counters of its in-kernel
+// quantization of x (M > 16)
 struct W4A4Layout {
-    size_t xq, xs, gx, partials, deq, sk, total;
+    size_t xq, xs, gx, partials, deq, sk, sync, total;
 };
 
 W4A4Layout w4a4_layout(int64_t M, int64_t K, int64_t N) {
@@ -112,7 +113,8 @@ W4A4Layout w4a4_layout(int64_t M, int64_t K, int64_t N) {
     L.partials = L.gx + 256;
     L.deq = round_up(L.partials + (size_t)kMaxPartials * 4, 256);
     L.sk = round_up(L.deq + (M <= kGemvMaxM ? (size_t)(M * K * 2) : 0), 256);
-    L.total = L.sk + (M > kGemvMaxM ? gemm_w4a4_stream_k_bytes(M, K, N) : 0);
+    L.sync = L.sk + (M > kGemvMaxM ? gemm_w4a4_stream_k_bytes(M, K, N) : 0);
+    L.total = L.sync + (M > kGemvMaxM ? gemm_w4a4_sync_bytes(M) : 0);
     return L;
 }
 
@@ -320,6 +322,18 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const W4A4Layout L = w4a4_layout(M, K, N);
     float* gx = reinterpret_cast<float*>(ws + L.gx);
+    if (M > kGemvMaxM) {
+        // one kernel: x quantized by the GEMM's own CTAs, then the block-scaled GEMM
+        const cudaError_t e = launch_gemm_w4a4_quant_x(
+            xb, x_global_scale, gx, reinterpret_cast<float*>(ws + L.partials),
+            reinterpret_cast<uint32_t*>(ws + L.sync), ws + L.xq, ws + L.xs, (int)M, (int)K,
+            w_packed, w_scales_swizzled, w_global_scale, (int)N, y, ybf,
+            reinterpret_cast<uint32_t*>(ws), ws + L.sk, stream, d);
+        // a device that cannot hold the whole grid at once (SMs taken by other contexts)
+        // refuses the cooperative launch: quantize first, then the GEMM, as two kernels
+        if (e != cudaErrorCooperativeLaunchTooLarge) return from_cuda(e);
+        cudaGetLastError();
+    }
     uint16_t* deq = M <= kGemvMaxM ? reinterpret_cast<uint16_t*>(ws + L.deq) : nullptr;
     cudaError_t e = launch_quantize(x, true, M, K, ws + L.xq, ws + L.xs, true, gx,
                                     x_global_scale, reinterpret_cast<float*>(ws + L.partials),
