@@ -375,6 +375,18 @@ const char* nvfp4_status_str(nvfp4_status status);
  * (cudaGetErrorString text; "no error" if there was none).  Host-only. */
 const char* nvfp4_last_cuda_error(void);
 
+/* Test switch for the failure path of the bounded device waits; never on in production.
+ * While on (for calls from the calling thread), the pipelined M = 1 GEMV and the
+ * tensor-core GEMMs of nvfp4_linear launch with a 200 us wait limit and one role
+ * withholding an arrival: the GEMV's consumers never release a stage, the W4A16 GEMM's
+ * dequantizing warps never mark a stage ready, the W4A4 GEMM's first CTA never counts its
+ * share of the in-kernel quantized x.  A wait then runs out; the kernel sets
+ * NVFP4_DEVERR_TIMEOUT in the workspace error word, every role stops, the copies and MMAs
+ * it issued are waited for, its TMEM is freed, and it returns (y is not written in full).
+ * The CUDA context stays usable: zero-fill the workspace and call again.  Host-only; the
+ * switch is per thread. */
+void nvfp4_debug_expire_waits(int on);
+
 /*
  * nvfp4_encode_elements -- the device's element rounding on its own: for each of n
  * fp32 inputs, e2m1_out[i] = E2M1 code (as nvfp4_quantize step 3 rounds src/d) and

@@ -30,7 +30,8 @@ EXPORTS = ("nvfp4_quantize", "nvfp4_repack", "nvfp4_linear", "nvfp4_repack_bytes
            "nvfp4_workspace_bytes", "nvfp4_w4a4_workspace_layout", "nvfp4_workspace_error",
            "nvfp4_status_str", "nvfp4_encode_elements", "nvfp4_quantize_noalloc",
            "nvfp4_last_cuda_error", "nvfp4_quantize_fp8_block128", "nvfp4_silu_mul_quantize",
-           "nvfp4_linear_nvfp4_x", "nvfp4_linear_silu_mul_quantize")
+           "nvfp4_linear_nvfp4_x", "nvfp4_linear_silu_mul_quantize",
+           "nvfp4_debug_expire_waits")
 
 
 class Nvfp4Error(RuntimeError):
@@ -65,6 +66,7 @@ def load(path: str = LIB_PATH):
         "nvfp4_encode_elements": (I, [P, I64, P, P, P]),
         "nvfp4_quantize_noalloc": (I, [P, I, I64, I64, P, P, P, P]),
         "nvfp4_last_cuda_error": (ctypes.c_char_p, []),
+        "nvfp4_debug_expire_waits": (None, [I]),
         "nvfp4_quantize_fp8_block128": (I, [P, P, I64, I64, P, P, P, P, SZ, P]),
         "nvfp4_silu_mul_quantize": (I, [P, I64, I64, P, P, SZ, P, P, P, SZ, P]),
         "nvfp4_linear_nvfp4_x": (I, [P, P, P, I64, I64, P, P, P, I64, P, I, I, P, SZ, P]),
@@ -251,6 +253,12 @@ def nvfp4_linear_silu_mul_quantize(x: torch.Tensor, w_packed: torch.Tensor,
         NVFP4_STATIC_WEIGHTS if static_weights else 0, _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nvfp4_linear_silu_mul_quantize")
+
+
+def nvfp4_debug_expire_waits(on: bool) -> None:
+    """Test switch: the calling thread's next nvfp4_linear kernels make a bounded wait run
+    out (see include/nvfp4.h)."""
+    load().nvfp4_debug_expire_waits(1 if on else 0)
 
 
 def nvfp4_encode_elements(inp: torch.Tensor, e2m1_out: torch.Tensor | None,

@@ -316,4 +316,14 @@ __device__ __forceinline__ void pdl_wait_prior_grid() {
 // wall-time limit of every device-side wait: far beyond any legitimate wait
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Bounded-wait settings of one launch: the wall-time limit of the waits in which one
+// role (or CTA) waits for another, and a test switch with which one role withholds an
+// arrival, so that such a wait runs out and the error path runs (every role stops,
+// copies and MMAs in flight are drained, TMEM is freed, the error word gets
+// NVFP4_DEVERR_TIMEOUT).  stall is 0 in every production launch.
+struct WaitCfg {
+    uint64_t wait_ns = kWaitLimitNs;
+    int stall = 0;
+};
+
 }  // namespace nvfp4

@@ -188,7 +188,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                   const float* __restrict__ gw, void* __restrict__ y, int y_bf16, int M, int N,
                   int nkb, int ntiles_m, int ntiles, int ntiles_sk, int p_sk, int64_t tsk,
                   uint32_t* __restrict__ err, uint32_t* __restrict__ counters,
-                  float* __restrict__ slots, FuseArgs fa) {
+                  float* __restrict__ slots, FuseArgs fa, WaitCfg dbg) {
     using L = Smem<kFuse>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -238,7 +238,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     if (it >= kStages &&
-                        !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err))
+                        !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err, dbg.wait_ns))
                         break;
                     mbar_arrive_expect_tx(bar_ptr(full(s)),
                                           kXBytes + kCodeBytes + L::kScaleBytes);
@@ -279,7 +279,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
             for (; !*abort_flag && wi.next(tile, kb0, kb1); ++lt) {
                 const int b = lt & 1;
                 if (lt >= 2 &&
-                    !tc::wait_or_abort(accempty(b), ((lt >> 1) - 1) & 1, abort_flag, err))
+                    !tc::wait_or_abort(accempty(b), ((lt >> 1) - 1) & 1, abort_flag, err, dbg.wait_ns))
                     break;
                 tc::fence_after();
                 const uint32_t d = tmem + (uint32_t)(b * kBM);
@@ -287,8 +287,8 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
-                    if (!tc::wait_or_abort(full(s), ph, abort_flag, err) ||
-                        !tc::wait_or_abort(afull(s), ph, abort_flag, err)) {
+                    if (!tc::wait_or_abort(full(s), ph, abort_flag, err, dbg.wait_ns) ||
+                        !tc::wait_or_abort(afull(s), ph, abort_flag, err, dbg.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -319,7 +319,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
             const int b = lt & 1;
             const bool ok = __all_sync(0xffffffffu,
                                        tc::wait_or_abort(accfull(b), (lt >> 1) & 1, abort_flag,
-                                                         err));
+                                                         err, dbg.wait_ns));
             if constexpr (kFuse) {
                 // the four warps meet at named barriers inside the tile: they leave together
                 // (any warp's failed wait stops all four)
@@ -355,7 +355,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % kStages;
                 if (!__all_sync(0xffffffffu,
-                                tc::wait_or_abort(full(s), (it / kStages) & 1, abort_flag, err))) {
+                                tc::wait_or_abort(full(s), (it / kStages) & 1, abort_flag, err, dbg.wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -382,7 +382,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 }
                 tc::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0 && !dbg.stall)
                     tc::arrive(afull(s));
             }
             if (!ok) break;
@@ -439,7 +439,7 @@ cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
                                             tc::counters_bytes(p.ntiles));
     gemm_w4a16_kernel<false><<<p.grid, kThreads, Smem<false>::kBytes, stream>>>(
         mx, mw, wsz, gw, y, y_bf16 ? 1 : 0, M, N, p.nkb, p.ntiles_m, p.ntiles, p.ntiles_sk, p.p_sk,
-        p.tsk, err, counters, slots, FuseArgs{});
+        p.tsk, err, counters, slots, FuseArgs{}, current_wait_cfg());
     return cudaGetLastError();
 }
 
@@ -475,7 +475,7 @@ cudaError_t launch_gemm_w4a16_silu(const uint16_t* x, int M, int K, const uint8_
     fa.hs = hs;
     gemm_w4a16_kernel<true><<<p.grid, kThreads, Smem<true>::kBytes, stream>>>(
         mx, mw, wsz, gw, nullptr, 1, M, 2 * I, p.nkb, p.ntiles_m, p.ntiles, 0, 0, 0, err,
-        nullptr, nullptr, fa);
+        nullptr, nullptr, fa, current_wait_cfg());
     return cudaGetLastError();
 }
 

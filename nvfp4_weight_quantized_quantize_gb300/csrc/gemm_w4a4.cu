@@ -103,22 +103,23 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Spin until *p reaches `target` (acquire), at most kWaitLimitNs; false on time-out.
-__device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target) {
+// Spin until *p reaches `target` (acquire), at most limit_ns; false on time-out.
+__device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target,
+                                             uint64_t limit_ns) {
     if (ld_acquire_gpu(p) >= target) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (ld_acquire_gpu(p) >= target) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
         __nanosleep(64);
     }
 }
 
 // Grid-wide barrier of the co-resident grid (one thread per CTA): the arrival that
 // completes the count resets it and advances the generation the others wait on.
-__device__ __forceinline__ bool grid_barrier(uint32_t* sync) {
+__device__ __forceinline__ bool grid_barrier(uint32_t* sync, uint64_t limit_ns) {
     volatile uint32_t* gen_p = sync + 1;
     const uint32_t gen = *gen_p;
     __threadfence();
@@ -131,7 +132,7 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* sync) {
     }
     const uint64_t t0 = globaltimer_ns();
     while (ld_acquire_gpu(sync + 1) == gen) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
         __nanosleep(64);
     }
     return true;
@@ -201,7 +202,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                  int nkb, int natoms_row, int x_row_blocks, int ntiles_m, int ntiles,
                  int ntiles_sk, int p_sk,
                  int64_t tsk, uint32_t* __restrict__ err, uint32_t* __restrict__ counters,
-                 float* __restrict__ slots, QxArgs qa) {
+                 float* __restrict__ slots, QxArgs qa, WaitCfg dbg) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -281,7 +282,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 float r = red[0];
                 for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
                 qa.partials[blockIdx.x] = r;
-                if (!grid_barrier(qa.sync)) {
+                if (!grid_barrier(qa.sync, dbg.wait_ns)) {
                     if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
                     qx_fail = 1;
                 }
@@ -311,7 +312,9 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             // this CTA's share is written: publish it to the async proxy, then count it
             fence_proxy_async_global();
             __syncthreads();
-            if (threadIdx.x == 0) {
+            // (with the test switch on, CTA 0 withholds its count: every producer's wait
+            // for the count runs out)
+            if (threadIdx.x == 0 && !(dbg.stall && blockIdx.x == 0)) {
                 __threadfence();
                 atomicAdd(qa.sync + 3, 1u);
             }
@@ -332,7 +335,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             int tile, kb0, kb1;
             if constexpr (kQuantX) {
                 // every CTA's share of the quantized x is written before the first TMA read
-                if (!*abort_flag && !wait_counter(qa.sync + 3, gridDim.x)) {
+                if (!*abort_flag && !wait_counter(qa.sync + 3, gridDim.x, dbg.wait_ns)) {
                     if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
                     *abort_flag = 1;
                 }
@@ -344,7 +347,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     if (it >= kStages &&
-                        !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err))
+                        !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err, dbg.wait_ns))
                         break;
                     const uint32_t sfb = (uint32_t)atoms_of(kb) * kAtomBytes;
                     // x rows of the tile: scale row blocks 2 mb and 2 mb + 1 (the second one
@@ -384,7 +387,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
             int tile, kb0, kb1;
             for (; !*abort_flag && wi.next(tile, kb0, kb1); ++lt) {
-                if (lt >= 1 && !tc::wait_or_abort(accempty(0), (lt - 1) & 1, abort_flag, err))
+                if (lt >= 1 && !tc::wait_or_abort(accempty(0), (lt - 1) & 1, abort_flag, err, dbg.wait_ns))
                     break;
                 tc::fence_after();
                 const uint32_t d = tmem;
@@ -392,8 +395,8 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
-                    if (!tc::wait_or_abort(full(s), ph, abort_flag, err) ||
-                        !tc::wait_or_abort(sfull(s), ph, abort_flag, err)) {
+                    if (!tc::wait_or_abort(full(s), ph, abort_flag, err, dbg.wait_ns) ||
+                        !tc::wait_or_abort(sfull(s), ph, abort_flag, err, dbg.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -426,7 +429,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const int s = it % kStages;
                 if (!__all_sync(0xffffffffu,
-                                tc::wait_or_abort(sland(s), (it / kStages) & 1, abort_flag, err))) {
+                                tc::wait_or_abort(sland(s), (it / kStages) & 1, abort_flag, err, dbg.wait_ns))) {
                     ok = false;
                     break;
                 }
@@ -455,7 +458,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 tc::tmem_st16(col + 32, u16);
                 tc::fence_before();
                 __syncwarp();
-                if (lane == 0) tc::arrive(sfull(s));
+                if (lane == 0 && !(dbg.stall && !kQuantX)) tc::arrive(sfull(s));
             }
             if (!ok) break;
         }
@@ -468,7 +471,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
         int tile, kb0, kb1;
         for (; wi.next(tile, kb0, kb1); ++lt) {
             if (!__all_sync(0xffffffffu,
-                            tc::wait_or_abort(accfull(0), lt & 1, abort_flag, err)))
+                            tc::wait_or_abort(accfull(0), lt & 1, abort_flag, err, dbg.wait_ns)))
                 break;
             tc::fence_after();
             tc::epilogue_work<kBN, kBM>(tmem, q, lane, tile, ntiles_m, kb0 == 0 && kb1 == nkb,
@@ -542,7 +545,8 @@ cudaError_t launch(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M
     cfg.numAttrs = kQuantX ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, gemm_w4a4_kernel<kQuantX>, mw, mx, wsz, xsz, gw, gx, y,
                            y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, (M + 127) / 128, p.ntiles_m,
-                           p.ntiles, p.ntiles_sk, p.p_sk, p.tsk, err, counters, slots, qa);
+                           p.ntiles, p.ntiles_sk, p.p_sk, p.tsk, err, counters, slots, qa,
+                           current_wait_cfg());
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -236,7 +236,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                     const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
                     const float* __restrict__ gx, int N, void* __restrict__ y, int y_bf16,
                     int rows_max, int rps, int rfirst, int stages, int w_static,
-                    uint32_t* __restrict__ err) {
+                    uint32_t* __restrict__ err, WaitCfg dbg) {
     constexpr int L = 32 / G;              // rows per step
     extern __shared__ __align__(128) uint8_t smem[];
     const int rowchunks = K >> 5;          // 16-byte chunks per row
@@ -296,7 +296,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
             for (int it = 0; it < nst; ++it) {
                 const int s = it % stages;
                 if (it >= stages &&
-                    !mbar_wait_bounded(&empty[s], ((it / stages) - 1) & 1, kWaitLimitNs)) {
+                    !mbar_wait_bounded(&empty[s], ((it / stages) - 1) & 1, dbg.wait_ns)) {
                     if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
                     abort_flag = 1;
                     break;
@@ -380,7 +380,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
         // the wait's outcome and the abort flag are made warp-uniform before they steer
         // control flow: the reductions below are warp-collective
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (it / stages) & 1,
-                                                                  kWaitLimitNs));
+                                                                  dbg.wait_ns));
         if (!ok) {
             if (err && lane == 0) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
             abort_flag = 1;
@@ -428,7 +428,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
             }
             if (lean_rows == nr) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
+                if (lane == 0 && !dbg.stall) mbar_arrive(&empty[s]);
                 continue;
             }
         }
@@ -477,7 +477,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                 slots[(sbeg + rl) * ngroups + warp] = pv;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0 && !dbg.stall) mbar_arrive(&empty[s]);
     }
     named_bar_sync(1, nthreads_c);
     if (abort_flag) return;
@@ -829,7 +829,7 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G, kXQ>, x, K, wq, wrm, gw, gx, N,
                            y, y_bf16 ? 1 : 0, rows_max, rps, rfirst, stages,
-                           w_static ? 1 : 0, err);
+                           w_static ? 1 : 0, err, current_wait_cfg());
     *launched = true;
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "common.cuh"
+
 namespace nvfp4 {
 
 struct DevInfo {
@@ -136,6 +138,10 @@ cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float*
                              int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
                              void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
                              cudaStream_t stream, const DevInfo& dev);
+
+// Wait settings for the launches of the calling thread: the production limits, or (while
+// nvfp4_debug_expire_waits is on) a 200 us limit and the stall switch.
+WaitCfg current_wait_cfg();
 
 // The current device's cached properties; NVFP4_ERR_DEVICE unless it is sm_103
 // (the status is returned as an int holding an nvfp4_status).

@@ -146,6 +146,20 @@ SiluLayout silu_layout(int64_t M, int64_t K, int64_t I) {
 
 namespace nvfp4 {
 int query_device(DevInfo* out) { return (int)current_device(out); }
+
+namespace {
+thread_local bool t_expire_waits = false;
+constexpr uint64_t kDebugWaitNs = 200000;  // 200 us
+}  // namespace
+
+WaitCfg current_wait_cfg() {
+    WaitCfg w;
+    if (t_expire_waits) {
+        w.wait_ns = kDebugWaitNs;
+        w.stall = 1;
+    }
+    return w;
+}
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -474,6 +488,8 @@ NVFP4_API nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t
     if (st != NVFP4_OK) return st;
     return from_cuda(launch_encode_elements(in, n, e2m1_out, e4m3_out, stream, d));
 }
+
+NVFP4_API void nvfp4_debug_expire_waits(int on) { t_expire_waits = on != 0; }
 
 NVFP4_API const char* nvfp4_last_cuda_error(void) {
     return cudaGetErrorString(t_last_cuda_error);

@@ -139,10 +139,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // ---- bounded waits -----------------------------------------------------------------------
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag, uint32_t* err) {
+                                              volatile int* abort_flag, uint32_t* err,
+                                              uint64_t limit_ns) {
     if (*abort_flag) return false;
     if (mbar_wait_bounded(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bar)), parity,
-                          kWaitLimitNs))
+                          limit_ns))
         return true;
     if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
     *abort_flag = 1;

@@ -1,0 +1,72 @@
+"""The failure path of the bounded device waits, exercised without a GPU fault.
+
+Every wait in which one role of a kernel (or one CTA) waits for another is bounded in
+wall time; when it runs out the kernel ORs NVFP4_DEVERR_TIMEOUT into the workspace's
+error word, every role stops, the copies and MMAs already issued are waited for, TMEM is
+freed, and the kernel returns.  nvfp4_debug_expire_waits makes that happen on purpose:
+the kernels launch with a 200 us limit and one role withholds its arrival (a flag that
+nothing sets).  For each kernel with such waits the test checks that
+
+- the call returns and the stream drains (bounded time, no hang),
+- nvfp4_workspace_error reports the time-out (and clears the word),
+- the CUDA context is still usable: the next call, on the zero-filled workspace, is
+  correct against the oracle and reports no error.
+"""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_weight_quantized_quantize_gb300 as nv
+import oracle
+from helpers import check_tolerance, upload_weights, y_to_f64
+from synth import random_nvfp4_weights, random_x
+
+pytestmark = pytest.mark.gpu
+
+NVFP4_DEVERR_TIMEOUT = 0x1
+
+
+@pytest.mark.parametrize("M,K,N,mode,what", [
+    (1, 5120, 17408, "w4a16", "pipelined GEMV: the consumers never release a stage"),
+    (64, 1024, 512, "w4a16", "tcgen05 W4A16 GEMM: no stage is marked dequantized"),
+    (64, 1024, 512, "w4a4", "block-scaled GEMM: one CTA never counts its share of x"),
+])
+def test_expired_wait_reports_and_recovers(M, K, N, mode, what):
+    x = random_x(M, K, seed=M + K)
+    wq, ws, gw = random_nvfp4_weights(N, K, seed=N)
+    d_wq, d_swz, d_g = upload_weights(wq, ws, gw, K)
+    d_x = x.cuda()
+    y = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    m = nv.NVFP4_W4A4 if mode == "w4a4" else nv.NVFP4_W4A16
+    work = torch.zeros(nv.nvfp4_workspace_bytes(1, M, K, N, m), dtype=torch.uint8,
+                       device="cuda")
+    torch.cuda.synchronize()
+
+    t0 = time.perf_counter()
+    nv.nvfp4_debug_expire_waits(True)
+    try:
+        nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, mode=mode, workspace=work)
+    finally:
+        nv.nvfp4_debug_expire_waits(False)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 10.0, what
+    bits = nv.nvfp4_workspace_error(work)
+    assert bits & NVFP4_DEVERR_TIMEOUT, what
+    assert nv.nvfp4_workspace_error(work) == 0  # read once, then cleared
+
+    # the context is usable: a normal call on the zero-filled workspace is correct
+    work.zero_()
+    nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, mode=mode, workspace=work)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_workspace_error(work) == 0
+    rng = np.random.default_rng(1)
+    pm = np.concatenate([rng.integers(0, M, 2048), np.full(N, M - 1)])
+    pn = np.concatenate([rng.integers(0, N, 2048), np.arange(N)])
+    if mode == "w4a4":
+        xq, xs, gx = oracle.quantize(x)  # x as the call quantizes it (dynamic scale)
+        y_ref, ab = oracle.linear_w4a4_pairs(xq, xs, gx, wq, ws, gw, pm, pn)
+    else:
+        y_ref, ab = oracle.linear_w4a16_pairs(x, wq, ws, gw, pm, pn)
+    check_tolerance(y_to_f64(y)[pm, pn], y_ref, ab, what)
