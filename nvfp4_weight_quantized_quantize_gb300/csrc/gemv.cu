@@ -284,7 +284,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
             // x heads for L2 too (16-byte aligned, K * 2 bytes: a multiple of 64), so that the
             // consumers' loads of it after the wait hit L2 rather than queue behind the
             // weight stream in HBM; weight copies are marked evict-first for the same reason
-            prefetch_l2(x, (uint32_t)K * 2u);
+            if (blockIdx.x == 0) prefetch_l2(x, (uint32_t)K * 2u);  // once for the grid
             if (!w_static) {
                 for (int it = 0; it < min(nst, stages); ++it)
                     prefetch_l2(wq + (r0 + (int64_t)stage_beg(it)) * rowb,

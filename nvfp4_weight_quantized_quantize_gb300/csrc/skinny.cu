@@ -105,7 +105,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
         if (lane == 0) {
             // the first ring's worth of codes heads for L2 while the previous kernel on the
             // stream may still run; every read that lands in shared memory comes after the
-            // wait for it
+            // wait for it.  Weight copies are marked evict-first, so that x and y stay in L2.
             if (!w_static) {  // static weights stream before the wait
                 for (int it = 0; it < min(nst, stages); ++it) {
                     const int64_t rbeg = (int64_t)rg0 * kSkRows + (int64_t)it * srows;
@@ -114,6 +114,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                 }
                 pdl_wait_prior_grid();
             }
+            const uint64_t pol = l2_evict_first_policy();
             int issued = 0;
             for (int it = 0; it < nst; ++it) {
                 const int s = it % stages;
@@ -132,9 +133,9 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                 const int64_t s_hi = ((rbeg + nr) * rows_sb + 15) & ~(int64_t)15;
                 mbar_arrive_expect_tx(&full[s], wbytes + (uint32_t)(s_hi - s_lo));
                 uint8_t* st = ring + (size_t)s * st_bytes;
-                bulk_g2s(st, wq + rbeg * rowb, wbytes, &full[s]);
-                bulk_g2s(st + (size_t)srows * rowb, wrm + s_lo, (uint32_t)(s_hi - s_lo),
-                         &full[s]);
+                bulk_g2s_hint(st, wq + rbeg * rowb, wbytes, &full[s], pol);
+                bulk_g2s_hint(st + (size_t)srows * rowb, wrm + s_lo, (uint32_t)(s_hi - s_lo),
+                              &full[s], pol);
                 issued = it + 1;
             }
             // every copy of this CTA is in flight: the next kernel on the stream may now be
