@@ -175,6 +175,11 @@ nvfp4_status nvfp4_quantize_fp8_block128(const uint8_t* src, const float* block_
  *   2. at byte A = Rp*Cp, the row-major scales [rows, Cb] unchanged, read by the
  *      small-M kernels (which stream a row's scales next to its codes), then zero
  *      bytes up to a multiple of 16 and 16 more.
+ * Footprint: the second copy costs 1/16 byte per weight, as much as the first: with the
+ * codes (1/2 byte per weight) a repacked weight takes 0.625 bytes per weight instead of
+ * 0.5625, 11 % more (5.57 MB more for a 17408 x 5120 weight).  The small-M kernels need
+ * the row-major copy: a CTA streams a contiguous slab of rows that does not start on a
+ * 128-row block, and the atoms interleave four 32-row quarters in each 16-byte line.
  * Arguments:
  *   scales_rowmajor  [rows, cols/16] bytes.  rows >= 1, cols >= 16, cols % 16 == 0.
  *   scales_swizzled  out, exactly swizzled_bytes == nvfp4_repack_bytes(rows, cols).

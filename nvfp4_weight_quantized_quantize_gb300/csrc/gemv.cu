@@ -1,30 +1,37 @@
-// gemv.cu -- W4A16 NVFP4 GEMV (M = 1) and skinny GEMM (2 <= M <= 16): the decode and
-// MTP-verify projections.  Qwen3x-Orin README (quick start, "--projection-backend
+// gemv.cu -- W4A16 NVFP4 GEMV (M = 1) and the small-M GEMM (2 <= M <= 16) fallback: the
+// decode and MTP-verify projections.  Qwen3x-Orin README (quick start, "--projection-backend
 // sm87"): decode streams every weight once per token; FlashRT docs/qwen36_usage.md
 // (generate_own_speculative_KN_nvfp4 argument table): verify runs K + 1 rows against
 // the same weights.
 //
 //   y[m, n] = gw * (gx ? gx : 1) * sum_b s[n, b] * sum_{k in b} x[m, k] * e2m1(q[n, k])
 //
-// Both kernels are bound by HBM (0.5625 bytes of weight per multiply-add at M = 1) and
-// by the issue rate of the dequantization, so the work per weight is kept small:
+// Bound by HBM (0.5625 bytes of weight per multiply-add at M = 1) and by the issue rate
+// of the dequantization, so the work per weight is kept small:
 //   - E2M1 -> fp16 with the hardware converter (cvt.rn.f16x2.e2m1x2: one instruction
 //     per two codes, exact);
-//   - x is carried as fp16 after a power-of-two rescale per (row, K chunk) that puts the
-//     row's largest magnitude in [2^14, 2^15): every bf16 value within 2^31 of that
-//     maximum is exact in fp16.  Should any value of a chunk not be exact, the CTA adds
-//     the (exact, fp32) residual of the whole chunk in a second, slower pass, so the
-//     result never depends on the rescale;
-//   - M = 1: fp32 mixed-precision FMAs (fma.rn.f32.f16, one per weight), the 16-block
-//     scale applied once per block in fp32;
-//   - 2 <= M <= 16: mma.sync m16n8k16 (f16 x f16 -> f32) with 16 weight rows as the
-//     A operand (block scale folded in: e2m1 * e4m3 is exact in fp16) and the M rows of
-//     x as B; n8 tiles of tokens.
-// Work split (deterministic, no atomics): a grid of CTAS_PER_SM x SMs CTAs, CTA c owns
-// the contiguous row range [N c/G, N (c+1)/G) (rounded to 16-row blocks for M > 1), so
-// every CTA streams one slab of the packed weights; inside a CTA the (row, K segment)
-// work units are split evenly over the 8 warps; partial sums land in per-warp shared-
-// memory slots that are added in a fixed order.
+//   - x is carried as fp16 after a power-of-two rescale that puts the largest magnitude
+//     of the slice a lane (or warp) holds in [2^14, 2^15): every bf16 value within 2^31 of
+//     that maximum is exact in fp16.  Should any value not be exact, an exact fp32
+//     residual pass is added, so the result never depends on the rescale;
+//   - fp32 mixed-precision FMAs (fma.rn.f32.f16, one per weight), the 16-block scale
+//     applied once per block in fp32.
+// Kernels in this file:
+//   - gemv_m1_pipe_kernel (M = 1, the decode path): one CTA per SM owns a contiguous slab
+//     of rows; a producer thread streams whole-row stages (codes and row-major scales, two
+//     bulk copies each, behind full/empty mbarriers) into a shared-memory ring, the first
+//     stage short so that it lands early; consumer warps each own a fixed group of 16-byte
+//     chunks of K and keep their x in registers for the whole kernel; the lanes of a row
+//     reduce by shuffles into per-(row, warp) slots that are added in a fixed order.
+//     Launched as a programmatic dependent; every wait is bounded.
+//   - gemv_m1_kernel: M = 1 where K is outside the pipelined kernel's range (K / 32 < 64
+//     or > 992):
+//     a grid of 2 x SMs CTAs of 8 warps, (row, K segment) units split evenly over the
+//     warps, x staged in shared memory per K chunk.
+//   - gemv_mma_kernel (2 <= M <= 16 where the skinny kernel does not take the K): mma.sync
+//     m16n8k16 with 16 weight rows as A (block scale folded in: e2m1 * e4m3 is exact in
+//     fp16) and up to 16 tokens of x as B; W read from global memory.
+// All splits are deterministic (no atomics on results).
 #include <cuda_fp16.h>
 
 #include <atomic>
