@@ -62,6 +62,7 @@ constexpr uint32_t kXBytes = kBM * kBK * 2;       // 32 KB
 constexpr uint32_t kABytes = kBN * kBK * 2;       // 16 KB
 constexpr uint32_t kCodeBytes = kBN * kBK / 2;    // 4 KB
 constexpr uint32_t kAtomBytes = 512;              // one 128 x 4 scale atom
+constexpr uint32_t kFixBars = 4 * 16;             // stream-K fix-up chunk barriers, 16 per epilogue warp
 
 // Shared-memory layout.  The fused gate/up variant takes two scale atoms per stage (the
 // gate rows' and the up rows' 128-row blocks) and two exchange tiles through which the
@@ -76,11 +77,17 @@ struct Smem {
     static constexpr uint32_t kOffXch = kOffScale + kStages * kScaleBytes;
     static constexpr uint32_t kXchBytes = kFuse ? 2 * 32 * 33 * 4 : 0;
     static constexpr uint32_t kOffBar = kOffXch + kXchBytes;
-    static constexpr uint32_t kNumBars = 3 * kStages + 4 + 1;
+    static constexpr uint32_t kNumBars = 3 * kStages + 4 + 1 + kFixBars;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kUsed = kOffMisc + 16;
     static constexpr uint32_t kBytes = kUsed + 1024;  // slack for 1024-byte alignment
 };
+
+// The stream-K fix-up of a CTA's last work item stages partials in the idle stage ring:
+// a quarter of it per epilogue warp, in 4 KB chunk buffers.
+constexpr uint32_t kFixupBytes = (Smem<false>::kOffBar / 4) & ~127u;
+constexpr int kFixupBufs = (int)(kFixupBytes / 4096) < 16 ? (int)(kFixupBytes / 4096) : 16;
+static_assert(kFixupBufs >= 2, "fix-up staging");
 
 // Instruction descriptor, kind::f16: fp32 D, bf16 A and B, both K-major, M x N.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -202,6 +209,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
     auto accfull = [&](int b) { return bar0 + 8u * (3 * kStages + b); };
     auto accempty = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };
     const uint32_t drain = bar0 + 8u * (3 * kStages + 4);
+    const uint32_t fixbar0 = bar0 + 8u * (3 * kStages + 5);  // 16 per epilogue warp
     auto bar_ptr = [&](uint32_t a) { return reinterpret_cast<uint64_t*>(base + (a - base_s)); };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kOffMisc + 4);
@@ -218,6 +226,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
             mbar_init(bar_ptr(accempty(b)), 4);
         }
         mbar_init(bar_ptr(drain), 1);
+        for (uint32_t i = 0; i < kFixBars; ++i) mbar_init(bar_ptr(fixbar0 + 8u * i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -270,6 +279,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
             for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
                 mbar_wait_bounded(bar_ptr(full(i % kStages)), (i / kStages) & 1, kWaitLimitNs);
         }
+        __syncwarp();  // lane 0 ran the role alone: the warp meets the block barrier converged
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
@@ -308,6 +318,7 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
             tc::commit(drain);
             mbar_wait_bounded(bar_ptr(drain), 0, kWaitLimitNs);
         }
+        __syncwarp();  // as in the producer warp
     } else if (warp < kEpiWarp0 + 4) {
         // ---------------- epilogue ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -330,9 +341,14 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
             } else {
                 if (!ok) break;
                 tc::fence_after();
+                // on the CTA's last item the stage ring is idle: a quarter of it per warp
+                tc::WorkIter peek = wi;
+                int t_, k0_, k1_;
+                uint8_t* stage = peek.next(t_, k0_, k1_) ? nullptr : base + q * kFixupBytes;
                 tc::epilogue_work<kBN, kBM>(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m,
                                             kb0 == 0 && kb1 == nkb, nkb, p_sk, tsk, g, y, y_bf16,
-                                            M, N, slots, counters, accempty(b));
+                                            M, N, slots, counters, accempty(b), stage,
+                                            bar_ptr(fixbar0 + 128u * q), kFixupBufs, err);
             }
         }
     } else {

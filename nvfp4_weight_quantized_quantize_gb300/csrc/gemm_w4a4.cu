@@ -65,12 +65,19 @@ constexpr uint32_t kOffB = kOffA + kStages * kABytes;
 constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
 constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
-constexpr uint32_t kNumBars = 4 * kStages + 4 + 1;
+constexpr uint32_t kFixBars = 4 * 16;  // stream-K fix-up chunk barriers, 16 per epilogue warp
+constexpr uint32_t kNumBars = 4 * kStages + 4 + 1 + kFixBars;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 
 static_assert(kTmemSf + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+
+// The stream-K fix-up of a CTA's last work item stages partials in the idle stage ring:
+// a quarter of it per epilogue warp, in 4 KB chunk buffers.
+constexpr uint32_t kFixupBytes = (kOffBar / 4) & ~127u;
+constexpr int kFixupBufs = (int)(kFixupBytes / 4096) < 16 ? (int)(kFixupBytes / 4096) : 16;
+static_assert(kFixupBufs >= 2, "fix-up staging");
 
 // Instruction descriptor, block-scaled kind: E2M1 A and B, UE4M3 scales (scale type 0),
 // scale ids 0, dense K = 64 per instruction, both K-major, fp32 D, M x N.
@@ -90,12 +97,6 @@ struct QxArgs {
     uint8_t* xs = nullptr;            // scale atoms of x (rows padded to 128, blocks to 4)
     int K = 0;
 };
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 
 // generic-proxy writes to global memory made visible to (and ordered with) the async
 // proxy: the quantized x is written with plain stores and read by TMA in other CTAs
@@ -215,6 +216,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const uint32_t drain = bar0 + 8u * (2 * kStages + 4);
     auto sfull = [&](int s) { return bar0 + 8u * (2 * kStages + 5 + s); };
     auto sland = [&](int s) { return bar0 + 8u * (3 * kStages + 5 + s); };  // scales landed
+    const uint32_t fixbar0 = bar0 + 8u * (4 * kStages + 5);  // 16 per epilogue warp
     auto bar_ptr = [&](uint32_t a) { return reinterpret_cast<uint64_t*>(base + (a - base_s)); };
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
@@ -232,6 +234,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
         mbar_init(bar_ptr(drain), 1);
         for (int s = 0; s < kStages; ++s) mbar_init(bar_ptr(sfull(s)), 4);
         for (int s = 0; s < kStages; ++s) mbar_init(bar_ptr(sland(s)), 1);
+        for (uint32_t i = 0; i < kFixBars; ++i) mbar_init(bar_ptr(fixbar0 + 8u * i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -287,6 +290,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     qx_fail = 1;
                 }
             }
+            __syncwarp();  // warp 0 converged (thread 0 spun alone) before the block barrier
             __syncthreads();
             if (!qx_fail) {
                 // every CTA's partial (read from L2: other CTAs wrote them in this kernel)
@@ -380,6 +384,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                 mbar_wait_bounded(bar_ptr(full(i % kStages)), (i / kStages) & 1, kWaitLimitNs);
             }
         }
+        __syncwarp();  // lane 0 ran the role alone: the warp meets the block barrier converged
     } else if (warp == 1) {
         // ---------------- MMA issue ----------------
         if (lane == 0) {
@@ -418,6 +423,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             tc::commit(drain);
             mbar_wait_bounded(bar_ptr(drain), 0, kWaitLimitNs);
         }
+        __syncwarp();  // as in the producer warp
     } else if (warp >= kSfWarp0) {
         // ---------------- scale writers ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -474,9 +480,14 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
                             tc::wait_or_abort(accfull(0), lt & 1, abort_flag, err, dbg.wait_ns)))
                 break;
             tc::fence_after();
+            // on the CTA's last item the stage ring is idle: a quarter of it per warp
+            tc::WorkIter peek = wi;
+            int t_, k0_, k1_;
+            uint8_t* stage = peek.next(t_, k0_, k1_) ? nullptr : base + q * kFixupBytes;
             tc::epilogue_work<kBN, kBM>(tmem, q, lane, tile, ntiles_m, kb0 == 0 && kb1 == nkb,
                                         nkb, p_sk, tsk, g, y, y_bf16, M, N, slots, counters,
-                                        accempty(0));
+                                        accempty(0), stage, bar_ptr(fixbar0 + 128u * q),
+                                        kFixupBufs, err);
         }
     }
 

@@ -209,43 +209,177 @@ __device__ __forceinline__ int sk_slot(int c, int64_t t0, int p_sk, int64_t tsk)
 
 // ---- epilogue ----------------------------------------------------------------------------
 
-// y[m0 + j, n] = v[j] * scale for the rows inside M (fp32 or bf16 y)
+// y[m0 + j, n] = v[j] * scale for the rows inside M (fp32 or bf16 y).  A full group of 32
+// rows is stored by one straight run of stores under a single warp-uniform test: a guard
+// per row costs a branch and a reconvergence point per store, which made these stores
+// several times slower.
 __device__ __forceinline__ void store_rows32(void* y, int y_bf16, int64_t M, int64_t N,
                                              int64_t m0, int64_t n, const float (&v)[32],
                                              float scale) {
     if (n >= N) return;
+    const bool full = m0 + 32 <= M;
     if (y_bf16) {
         uint16_t* yp = static_cast<uint16_t*>(y) + m0 * N + n;
+        if (full) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (m0 + j < M) yp[(int64_t)j * N] = f32_to_bf16_rne(v[j] * scale);
+            for (int j = 0; j < 32; ++j) yp[(int64_t)j * N] = f32_to_bf16_rne(v[j] * scale);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (m0 + j < M) yp[(int64_t)j * N] = f32_to_bf16_rne(v[j] * scale);
+        }
     } else {
         float* yp = static_cast<float*>(y) + m0 * N + n;
+        if (full) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (m0 + j < M) yp[(int64_t)j * N] = v[j] * scale;
+            for (int j = 0; j < 32; ++j) yp[(int64_t)j * N] = v[j] * scale;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (m0 + j < M) yp[(int64_t)j * N] = v[j] * scale;
+        }
+    }
+}
+
+// A stream-K slot holds a partial tile as [lane quarter q][x row c][W row within the
+// quarter]: the quarter's 32 x rows from c0 on are one contiguous 4 KB chunk, written by the
+// warp of that quarter with one 128-byte line per store.
+template <int BM>
+__device__ __forceinline__ size_t slot_chunk(int q, int c0) {
+    return ((size_t)q * BM + c0) * 32;
+}
+
+// The fix-up of one tile quarter through shared memory.  The partials of the tile's other
+// segments stream into `nbuf` 4 KB chunk buffers at `stage` by bulk copies, each buffer with
+// its own mbarrier (`bars`, initialised with the kernel's barriers), up to nbuf chunks in
+// flight; for every 32 x rows the partials are added in segment order (the CTA's own from
+// TMEM when own_tmem), then stored to y.  Only for the CTA's last work item, when every MMA
+// of the CTA has completed and the stage ring is idle.
+template <int BN, int BM>
+__device__ __forceinline__ void fixup_staged(uint32_t taddr, bool own_tmem, int q, int lane,
+                                             int mb, int cf, int cl, int64_t t0, int p_sk,
+                                             int64_t tsk, const float* slots, uint8_t* stage,
+                                             uint64_t* bars, int nbuf, float scale, void* y,
+                                             int y_bf16, int M, int N, int64_t n, uint32_t* err) {
+    constexpr size_t kSlotFloats = (size_t)BN * BM;
+    const int me = blockIdx.x;
+    const int64_t rows_left = (int64_t)M - (int64_t)mb * BM;
+    const int nrow = rows_left >= BM ? BM / 32 : (int)((rows_left + 31) / 32);
+    const int nother = cl - cf + 1 - (own_tmem ? 1 : 0);
+    const int total = nrow * nother;
+    float* bufs = reinterpret_cast<float*>(stage);
+    // chunk k: x rows 32 (k / nother) .. + 31 of the (k % nother)-th other segment
+    auto issue = [&](int k) {
+        if (lane != 0) return;
+        const int ci = k / nother;
+        int cs = cf + k % nother;
+        if (own_tmem && cs >= me) ++cs;
+        const int b = k % nbuf;
+        mbar_arrive_expect_tx(bars + b, 4096);
+        bulk_g2s(bufs + (size_t)b * 1024,
+                 slots + (size_t)sk_slot(cs, t0, p_sk, tsk) * kSlotFloats + slot_chunk<BM>(q, ci * 32),
+                 4096, bars + b);
+    };
+    const int pre = total < nbuf ? total : nbuf;
+    for (int k = 0; k < pre; ++k) issue(k);
+    int k = 0;  // next chunk to read
+    bool ok = true;
+#pragma unroll 1
+    for (int ci = 0; ci < nrow && ok; ++ci) {
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+#pragma unroll 1
+        for (int cs = cf; cs <= cl; ++cs) {
+            float v[32];
+            if (own_tmem && cs == me) {
+                uint32_t u[32];
+                tmem_ld32(taddr + (uint32_t)(ci * 32), u);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
+            } else {
+                const int b = k % nbuf;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(bars + b, (uint32_t)(k / nbuf) & 1u,
+                                                  kWaitLimitNs))) {
+                    ok = false;
+                    break;
+                }
+                const float* src = bufs + (size_t)b * 1024;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = src[j * 32 + lane];
+                if (k + nbuf < total) {
+                    // the buffer is read before the copy that refills it is issued
+                    __syncwarp();
+                    fence_proxy_async_smem();
+                    issue(k + nbuf);
+                }
+                ++k;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] += v[j];
+        }
+        if (ok) store_rows32(y, y_bf16, M, N, (int64_t)mb * BM + ci * 32, n, acc, scale);
+    }
+    if (!ok) {
+        if (lane == 0 && err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+        // the copies in flight land before the CTA moves on to exit
+        const int issued = k + nbuf < total ? k + nbuf : total;
+        for (int i = k; i < issued; ++i)
+            mbar_wait_bounded(bars + i % nbuf, (uint32_t)(i / nbuf) & 1u, kWaitLimitNs);
     }
 }
 
 // One work item's epilogue for one epilogue warp: TMEM lane quarter q holds W rows
-// q*32 .. q*32+31 of the tile, columns 0 .. BM-1 the tile's x rows.  A whole tile goes to y;
-// a stream-K segment goes to this CTA's fp32 slot, and the arrival that completes the
+// q*32 .. q*32+31 of the tile, columns 0 .. BM-1 the tile's x rows.  A whole tile goes to y.
+// A stream-K segment goes to this CTA's fp32 slot, and the arrival that completes the
 // quarter's count (one counter per tile quarter, wrapping back to zero) adds the quarter's
-// partials in segment order and writes y.  The accumulator is released (accempty) as soon
-// as it has been read.
+// partials in segment order and writes y.  On the CTA's last work item (`stage` not null:
+// this warp's share of the idle stage ring, nbuf chunk buffers with their mbarriers at
+// `fixbars`) a segment that finds every
+// other segment of its tile already counted skips its slot: it keeps its partial in TMEM
+// and adds it in its place in the order, the other partials streamed in through shared
+// memory.  The order of the additions is the same on every path, so results are
+// deterministic.  The accumulator is released (accempty) as soon as it has been read.
 template <int BN, int BM>
 __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int tile,
                                               int ntiles_m, bool whole, int nkb, int p_sk,
                                               int64_t tsk, float scale, void* y, int y_bf16,
                                               int M, int N, float* slots, uint32_t* counters,
-                                              uint32_t accempty) {
+                                              uint32_t accempty, uint8_t* stage,
+                                              uint64_t* fixbars, int nbuf, uint32_t* err) {
+    static_assert(BN == 128, "four lane quarters of 32 W rows");
     constexpr size_t kSlotFloats = (size_t)BN * BM;
     const int nb = tile / ntiles_m, mb = tile % ntiles_m;
     const int nl = q * 32 + lane;
     const int64_t n = (int64_t)nb * BN + nl;
     const uint32_t taddr = acc + ((uint32_t)(q * 32) << 16);
     const int64_t t0 = (int64_t)tile * nkb;
-    float* mine = whole ? nullptr : slots + (size_t)sk_slot(blockIdx.x, t0, p_sk, tsk) * kSlotFloats;
+    int cf = 0, cl = 0;
+    unsigned nseg = 1;
+    if (!whole) {
+        cf = sk_cta_of(t0, p_sk, tsk);
+        cl = sk_cta_of(t0 + nkb - 1, p_sk, tsk);
+        nseg = (unsigned)(cl - cf + 1);
+        if (stage) {
+            unsigned seen = 0;
+            if (lane == 0) seen = ld_acquire_gpu(&counters[tile * 4 + q]);
+            if (__shfl_sync(0xffffffffu, seen, 0) == nseg - 1) {
+                // every other partial is in its slot; the count goes back to zero for the
+                // next call (no other segment touches it again)
+                if (lane == 0) counters[tile * 4 + q] = 0u;
+                fixup_staged<BN, BM>(taddr, true, q, lane, mb, cf, cl, t0, p_sk, tsk, slots,
+                                     stage, fixbars, nbuf, scale, y, y_bf16, M, N, n, err);
+                fence_before();
+                __syncwarp();
+                if (lane == 0) arrive(accempty);
+                return;
+            }
+        }
+    }
+    float* mine = whole ? nullptr
+                        : slots + (size_t)sk_slot(blockIdx.x, t0, p_sk, tsk) * kSlotFloats +
+                              slot_chunk<BM>(q, 0) + lane;
 #pragma unroll 1
     for (int c0 = 0; c0 < BM; c0 += 32) {
         uint32_t u[32];
@@ -256,23 +390,25 @@ __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int
         if (whole) {
             store_rows32(y, y_bf16, M, N, (int64_t)mb * BM + c0, n, v, scale);
         } else {
-            // partial tile: fp32 slot, [x row within tile][W row within tile]
 #pragma unroll
-            for (int j = 0; j < 32; ++j) mine[(c0 + j) * BN + nl] = v[j];
+            for (int j = 0; j < 32; ++j) mine[(size_t)(c0 + j) * 32] = v[j];
         }
     }
     fence_before();
     __syncwarp();
     if (lane == 0) arrive(accempty);
     if (whole) return;
-    const int cf = sk_cta_of(t0, p_sk, tsk), cl = sk_cta_of(t0 + nkb - 1, p_sk, tsk);
-    const unsigned nseg = (unsigned)(cl - cf + 1);
     __threadfence();
     __syncwarp();
     unsigned old = 0;
     if (lane == 0) old = atomicInc(&counters[tile * 4 + q], nseg - 1);
     if (__shfl_sync(0xffffffffu, old, 0) != nseg - 1) return;
     __threadfence();
+    if (stage) {
+        fixup_staged<BN, BM>(taddr, false, q, lane, mb, cf, cl, t0, p_sk, tsk, slots, stage,
+                             fixbars, nbuf, scale, y, y_bf16, M, N, n, err);
+        return;
+    }
     // 32 rows of the quarter at a time, every partial's 32 loads in flight together; the
     // partials are added in segment order
 #pragma unroll 1
@@ -285,10 +421,10 @@ __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int
 #pragma unroll 1
         for (int cs = cf; cs <= cl; ++cs) {
             const float* sp = slots + (size_t)sk_slot(cs, t0, p_sk, tsk) * kSlotFloats +
-                              (size_t)c0 * BN + nl;
+                              slot_chunk<BM>(q, c0) + lane;
             float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __ldcg(sp + (size_t)j * BN);
+            for (int j = 0; j < 32; ++j) v[j] = __ldcg(sp + (size_t)j * 32);
 #pragma unroll
             for (int j = 0; j < 32; ++j) accv[j] += v[j];
         }
