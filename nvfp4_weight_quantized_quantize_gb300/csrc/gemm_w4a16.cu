@@ -121,14 +121,18 @@ constexpr int kXchPitch = 33;
 
 // Epilogue of one whole tile of the fused gate/up variant.  TMEM lanes 0..63 hold gate
 // columns 64 nb + l of h, lanes 64..127 the up columns; warps q = 0, 1 read gate
-// (their 32 lanes each), warps q = 2, 3 up, for the same 32 columns of h (q & 1).  Per 32
-// accumulator columns (32 rows m of x):
-//   - the gate warps round gw * acc to bf16 (the gate/up GEMM's output) and write
-//     silu(gate) into their exchange tile, [m][i];
-//   - the up warps round their values the same way and overwrite each entry with
-//     h = silu(g) * u; then lane l takes row m = l of the tile -- the 32 columns of h it
-//     holds are two whole 16-element blocks -- and quantizes both with the quantizer's
-//     one-thread block rule and the static global scale: 16 bytes of codes, 2 scale bytes.
+// (their 32 lanes each), warps q = 2, 3 up, for the same 32 columns of h (q & 1).  Each
+// gate/up warp pair shares an exchange tile [m][i] and splits the work in halves.  Per 32
+// accumulator columns (32 rows m of x), values first rounded to bf16 as gw * acc (the
+// gate/up GEMM's output):
+//   1. the gate warp takes silu of rows 0..15 itself and hands rows 16..31 of raw gate to
+//      the up warp through the tile;
+//   2. the up warp forms h = silu(g) * u for rows 16..31; the gate warp puts its silu
+//      values of rows 0..15 in the tile;
+//   3. the up warp multiplies rows 0..15 by their up values;
+//   4. lane l of each warp quantizes one 16-element block of row m = l -- columns 0..15
+//      by the gate warp, 16..31 by the up warp -- with the quantizer's one-thread block
+//      rule and the static global scale: 8 bytes of codes and a scale byte each.
 // Rows past M get no codes; their scale bytes inside the last 128-row block are zero.
 __device__ __forceinline__ void epilogue_silu_quant(uint32_t acc, int q, int lane, int tile,
                                                     int ntiles_m, float gw, const FuseArgs& fa,
@@ -138,47 +142,54 @@ __device__ __forceinline__ void epilogue_silu_quant(uint32_t acc, int q, int lan
     const float g = *fa.gh;
     const int64_t cp4 = (fa.I / 16 + 3) / 4;
     const int m_pad = (M + 127) / 128 * 128;
+    const bool gate = q < 2;
+    const int hb = gate ? 0 : 1;                // the 16-column block this warp quantizes
     const int ibase = nb * 64 + (q & 1) * 32;   // this warp pair's 32 columns of h
     float* xw = xch + (q & 1) * 32 * kXchPitch;
 #pragma unroll 1
     for (int c0 = 0; c0 < kBM; c0 += 32) {
         uint32_t u[32];
         tc::tmem_ld32(taddr + c0, u);
-        if (q < 2) {
+        float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                xw[j * kXchPitch + lane] =
-                    silu_f32(bf16_to_f32(f32_to_bf16_rne(__uint_as_float(u[j]) * gw)));
+        for (int j = 0; j < 32; ++j) v[j] = bf16_to_f32(f32_to_bf16_rne(__uint_as_float(u[j]) * gw));
+        if (gate) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = silu_f32(v[j]);
+#pragma unroll
+            for (int j = 16; j < 32; ++j) xw[j * kXchPitch + lane] = v[j];
         }
         named_bar_sync(1, 128);
-        if (q >= 2) {
+        if (gate) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float up = bf16_to_f32(f32_to_bf16_rne(__uint_as_float(u[j]) * gw));
-                xw[j * kXchPitch + lane] = __fmul_rn(xw[j * kXchPitch + lane], up);
-            }
-            __syncwarp();
-            const int m = mb * kBM + c0 + lane;
-            if (m < m_pad) {
-                uint32_t code[4], s8[2];
+            for (int j = 0; j < 16; ++j) xw[j * kXchPitch + lane] = v[j];
+        } else {
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    float t[16];
+            for (int j = 16; j < 32; ++j)
+                xw[j * kXchPitch + lane] = __fmul_rn(silu_f32(xw[j * kXchPitch + lane]), v[j]);
+        }
+        named_bar_sync(1, 128);
+        if (!gate) {
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) t[k] = xw[lane * kXchPitch + 16 * hb + k];
-                    s8[hb] = quantize_block16(t, g, code[2 * hb], code[2 * hb + 1]);
-                }
-                // the two blocks are scale columns ibase/16 and ibase/16 + 1, adjacent bytes
-                // of one 4-column group of the atom
-                uint16_t* sp = reinterpret_cast<uint16_t*>(
-                    fa.hs + swizzle_offset(m, ibase / 16, cp4));
-                if (m < M) {
-                    *reinterpret_cast<uint4*>(fa.hq + (int64_t)m * (fa.I / 2) + ibase / 2) =
-                        make_uint4(code[0], code[1], code[2], code[3]);
-                    *sp = (uint16_t)(s8[0] | (s8[1] << 8));
-                } else {
-                    *sp = 0;
-                }
+            for (int j = 0; j < 16; ++j)
+                xw[j * kXchPitch + lane] = __fmul_rn(xw[j * kXchPitch + lane], v[j]);
+        }
+        named_bar_sync(1, 128);
+        const int m = mb * kBM + c0 + lane;
+        if (m < m_pad) {
+            float t[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) t[k] = xw[lane * kXchPitch + 16 * hb + k];
+            uint32_t lo, hi;
+            const uint32_t s8 = quantize_block16(t, g, lo, hi);
+            // the block is scale column ibase/16 + hb of the atom
+            uint8_t* sp = fa.hs + swizzle_offset(m, ibase / 16 + hb, cp4);
+            if (m < M) {
+                *reinterpret_cast<uint2*>(fa.hq + (int64_t)m * (fa.I / 2) + ibase / 2 + 8 * hb) =
+                    make_uint2(lo, hi);
+                *sp = (uint8_t)s8;
+            } else {
+                *sp = 0;
             }
         }
         named_bar_sync(1, 128);

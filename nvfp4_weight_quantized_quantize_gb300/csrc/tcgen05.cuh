@@ -268,21 +268,34 @@ __device__ __forceinline__ void fixup_staged(uint32_t taddr, bool own_tmem, int 
     const int nother = cl - cf + 1 - (own_tmem ? 1 : 0);
     const int total = nrow * nother;
     float* bufs = reinterpret_cast<float*>(stage);
-    // chunk k: x rows 32 (k / nother) .. + 31 of the (k % nother)-th other segment
-    auto issue = [&](int k) {
-        if (lane != 0) return;
-        const int ci = k / nother;
-        int cs = cf + k % nother;
-        if (own_tmem && cs >= me) ++cs;
-        const int b = k % nbuf;
-        mbar_arrive_expect_tx(bars + b, 4096);
-        bulk_g2s(bufs + (size_t)b * 1024,
-                 slots + (size_t)sk_slot(cs, t0, p_sk, tsk) * kSlotFloats + slot_chunk<BM>(q, ci * 32),
-                 4096, bars + b);
+    // this quarter's part of segment cs's slot: the tile's first segment may be its CTA's
+    // second slot; every later segment starts its CTA's range (the first slot)
+    const float* q_base = slots + (size_t)q * BM * 32;
+    const float* first_seg = q_base + (size_t)sk_slot(cf, t0, p_sk, tsk) * kSlotFloats;
+    auto seg_src = [&](int cs) {
+        return cs == cf ? first_seg : q_base + (size_t)(2 * cs) * kSlotFloats;
+    };
+    // the chunk stream, in the order it is read: x rows 32 ci .. of every other segment
+    int is_ci = 0, is_cs = (own_tmem && cf == me) ? cf + 1 : cf, is_b = 0, issued = 0;
+    auto issue_next = [&]() {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bars + is_b, 4096);
+            bulk_g2s(bufs + (size_t)is_b * 1024, seg_src(is_cs) + (size_t)is_ci * 32 * 32, 4096,
+                     bars + is_b);
+        }
+        ++issued;
+        if (++is_b == nbuf) is_b = 0;
+        if (++is_cs == me && own_tmem) ++is_cs;
+        if (is_cs > cl) {
+            ++is_ci;
+            is_cs = (own_tmem && cf == me) ? cf + 1 : cf;
+        }
     };
     const int pre = total < nbuf ? total : nbuf;
-    for (int k = 0; k < pre; ++k) issue(k);
-    int k = 0;  // next chunk to read
+#pragma unroll 1
+    for (int k = 0; k < pre; ++k) issue_next();
+    int rb = 0, nread = 0;
+    uint32_t rph = 0;
     bool ok = true;
 #pragma unroll 1
     for (int ci = 0; ci < nrow && ok; ++ci) {
@@ -298,23 +311,27 @@ __device__ __forceinline__ void fixup_staged(uint32_t taddr, bool own_tmem, int 
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(u[j]);
             } else {
-                const int b = k % nbuf;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait_bounded(bars + b, (uint32_t)(k / nbuf) & 1u,
-                                                  kWaitLimitNs))) {
+                bool landed = mbar_try_wait(bars + rb, rph);
+                if (!__all_sync(0xffffffffu, landed))
+                    landed = mbar_wait_bounded(bars + rb, rph, kWaitLimitNs);
+                if (!__all_sync(0xffffffffu, landed)) {
                     ok = false;
                     break;
                 }
-                const float* src = bufs + (size_t)b * 1024;
+                const float* src = bufs + (size_t)rb * 1024 + lane;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = src[j * 32 + lane];
-                if (k + nbuf < total) {
+                for (int j = 0; j < 32; ++j) v[j] = src[j * 32];
+                if (issued < total) {
                     // the buffer is read before the copy that refills it is issued
                     __syncwarp();
                     fence_proxy_async_smem();
-                    issue(k + nbuf);
+                    issue_next();
                 }
-                ++k;
+                ++nread;
+                if (++rb == nbuf) {
+                    rb = 0;
+                    rph ^= 1u;
+                }
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[j] += v[j];
@@ -323,10 +340,17 @@ __device__ __forceinline__ void fixup_staged(uint32_t taddr, bool own_tmem, int 
     }
     if (!ok) {
         if (lane == 0 && err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
-        // the copies in flight land before the CTA moves on to exit
-        const int issued = k + nbuf < total ? k + nbuf : total;
-        for (int i = k; i < issued; ++i)
-            mbar_wait_bounded(bars + i % nbuf, (uint32_t)(i / nbuf) & 1u, kWaitLimitNs);
+        // the copies in flight land before the CTA moves on to exit: the unread ones, from
+        // buffer rb on
+        int b = rb;
+        uint32_t ph = rph;
+        for (int i = nread; i < issued; ++i) {
+            mbar_wait_bounded(bars + b, ph, kWaitLimitNs);
+            if (++b == nbuf) {
+                b = 0;
+                ph ^= 1u;
+            }
+        }
     }
 }
 
