@@ -155,7 +155,7 @@ __device__ __forceinline__ void epilogue_silu_quant(uint32_t acc, int q, int lan
         for (int j = 0; j < 32; ++j) v[j] = bf16_to_f32(f32_to_bf16_rne(__uint_as_float(u[j]) * gw));
         if (gate) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = silu_f32(v[j]);
+            for (int j = 0; j < 16; ++j) v[j] = silu_f32_nobranch(v[j]);
 #pragma unroll
             for (int j = 16; j < 32; ++j) xw[j * kXchPitch + lane] = v[j];
         }
@@ -166,7 +166,7 @@ __device__ __forceinline__ void epilogue_silu_quant(uint32_t acc, int q, int lan
         } else {
 #pragma unroll
             for (int j = 16; j < 32; ++j)
-                xw[j * kXchPitch + lane] = __fmul_rn(silu_f32(xw[j * kXchPitch + lane]), v[j]);
+                xw[j * kXchPitch + lane] = __fmul_rn(silu_f32_nobranch(xw[j * kXchPitch + lane]), v[j]);
         }
         named_bar_sync(1, 128);
         if (!gate) {

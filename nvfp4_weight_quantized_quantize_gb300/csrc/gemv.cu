@@ -428,7 +428,9 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
                 float pv = fmaf(sc.x, a[0] + a[1], sc.y * (a[2] + a[3])) * u1 * u2;
 #pragma unroll
                 for (int o = G / 2; o > 0; o >>= 1) pv += __shfl_xor_sync(0xffffffffu, pv, o);
-                if ((lane % G) == 0) *sl = pv;
+                // the butterfly leaves the same sum in all G lanes of the row (each pairwise
+                // add is commutative), so every lane stores it: no predicate in the loop
+                *sl = pv;
                 wp += wstep;
                 sp += sstep;
                 sl += slstep;

@@ -241,6 +241,10 @@ __device__ __forceinline__ void store_rows32(void* y, int y_bf16, int64_t M, int
     }
 }
 
+// How long the first segment of a stream-K tile waits, on its CTA's last item, for the
+// tile's other segments before it writes its own partial like them
+constexpr uint64_t kOwnerWaitNs = 20000;
+
 // A stream-K slot holds a partial tile as [lane quarter q][x row c][W row within the
 // quarter]: the quarter's 32 x rows from c0 on are one contiguous 4 KB chunk, written by the
 // warp of that quarter with one 128-byte line per store.
@@ -360,10 +364,10 @@ __device__ __forceinline__ void fixup_staged(uint32_t taddr, bool own_tmem, int 
 // quarter's count (one counter per tile quarter, wrapping back to zero) adds the quarter's
 // partials in segment order and writes y.  On the CTA's last work item (`stage` not null:
 // this warp's share of the idle stage ring, nbuf chunk buffers with their mbarriers at
-// `fixbars`) a segment that finds every
-// other segment of its tile already counted skips its slot: it keeps its partial in TMEM
-// and adds it in its place in the order, the other partials streamed in through shared
-// memory.  The order of the additions is the same on every path, so results are
+// `fixbars`) a segment that finds every other segment of its tile already counted (the
+// tile's first segment waits up to kOwnerWaitNs for that) skips its slot: it keeps its
+// partial in TMEM and adds it in its place in the order, the other partials streamed in
+// through shared memory.  The order of the additions is the same on every path, so results are
 // deterministic.  The accumulator is released (accempty) as soon as it has been read.
 template <int BN, int BM>
 __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int tile,
@@ -387,7 +391,21 @@ __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int
         nseg = (unsigned)(cl - cf + 1);
         if (stage) {
             unsigned seen = 0;
-            if (lane == 0) seen = ld_acquire_gpu(&counters[tile * 4 + q]);
+            if (lane == 0) {
+                const uint32_t* cnt = &counters[tile * 4 + q];
+                seen = ld_acquire_gpu(cnt);
+                // The tile's first segment waits a little for the others to be counted
+                // rather than writing its own slot: on a CTA's last item the others end at
+                // about the same time (the stream-K ranges are balanced).  The wait is
+                // bounded; when it runs out the segment takes the ordinary path below.
+                if (seen != nseg - 1 && (int)blockIdx.x == cf) {
+                    const uint64_t w0 = globaltimer_ns();
+                    while (seen != nseg - 1 && globaltimer_ns() - w0 < kOwnerWaitNs) {
+                        __nanosleep(64);
+                        seen = ld_acquire_gpu(cnt);
+                    }
+                }
+            }
             if (__shfl_sync(0xffffffffu, seen, 0) == nseg - 1) {
                 // every other partial is in its slot; the count goes back to zero for the
                 // next call (no other segment touches it again)

@@ -1,7 +1,6 @@
-// silu on the device for a list of bf16 inputs, through the library's own silu_f32 (the
-// function the activation quantizer and the fused gate/up epilogue call), and through
-// CUDA's correctly rounded division on the same exp as a second opinion.  Test
-// infrastructure: built and loaded by tests/test_gpu_silu.py.
+// silu on the device for a list of bf16 inputs, through the library's own two forms:
+// silu_f32 (the activation quantizer's) and silu_f32_nobranch (the fused gate/up
+// epilogue's).  Test infrastructure: built and loaded by tests/test_gpu_silu.py.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -10,18 +9,18 @@
 
 namespace {
 
-__global__ void silu_list(const uint16_t* g, float* out, float* out_div, int n) {
+__global__ void silu_list(const uint16_t* g, float* out, float* out_nb, int n) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const float x = nvfp4::bf16_to_f32(g[i]);
     out[i] = nvfp4::silu_f32(x);
-    out_div[i] = __fdiv_rn(x, __fadd_rn(1.0f, nvfp4::exp_cody_waite(-x)));
+    out_nb[i] = nvfp4::silu_f32_nobranch(x);
 }
 
 }  // namespace
 
 // host arrays in and out; returns a cudaError_t
-extern "C" int device_silu(const uint16_t* g, float* out, float* out_div, int n) {
+extern "C" int device_silu(const uint16_t* g, float* out, float* out_nb, int n) {
     uint16_t* dg = nullptr;
     float* d_out = nullptr;
     cudaError_t e = cudaMalloc(&dg, (size_t)n * 2);
@@ -32,7 +31,7 @@ extern "C" int device_silu(const uint16_t* g, float* out, float* out_div, int n)
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = cudaMemcpy(out, d_out, (size_t)n * 4, cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess) e = cudaMemcpy(out_div, d_out + n, (size_t)n * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(out_nb, d_out + n, (size_t)n * 4, cudaMemcpyDeviceToHost);
     cudaFree(dg);
     cudaFree(d_out);
     return (int)e;

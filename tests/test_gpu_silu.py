@@ -2,10 +2,11 @@
 
 Every caller hands silu a bf16 value (the gate half of a bf16 gate_up tensor, or the
 fused gate/up epilogue's bf16-rounded gate), so the 65,536 bf16 bit patterns are all
-the inputs it can see.  The device silu (the Cody-Waite exp, then a branch-free division
-by P. Markstein's reciprocal-and-remainder method) must give the oracle's
-orc_silu_mul_f32(g, 1) bit for bit on every one of them, infinities and NaN included,
-and agree with CUDA's correctly rounded division applied to the same exp.
+the inputs it can see.  Both device forms -- silu_f32 (the Cody-Waite exp, then CUDA's
+correctly rounded division) and silu_f32_nobranch (the exp's ends selected rather than
+branched to, then a branch-free division by P. Markstein's reciprocal-and-remainder
+method) -- must give the oracle's orc_silu_mul_f32(g, 1) bit for bit on every one of
+them, infinities and NaN included.
 """
 import ctypes
 import os
@@ -38,21 +39,23 @@ def silu_lib():
     return lib
 
 
+def _check(out, want, gf, what):
+    nan_w, nan_o = np.isnan(want), np.isnan(out)
+    assert np.array_equal(nan_w, nan_o), "%s: NaN pattern differs" % what
+    ok = ~nan_w
+    bad = np.nonzero(out[ok].view(np.uint32) != want[ok].view(np.uint32))[0]
+    assert bad.size == 0, "%s: %d inputs differ; first g = %r: device %r oracle %r" % (
+        what, bad.size, float(gf[ok][bad[0]]), float(out[ok][bad[0]]), float(want[ok][bad[0]]))
+
+
 def test_silu_every_bf16_input(silu_lib):
     g = np.arange(65536, dtype=np.uint32).astype(np.uint16)
     n = g.size
     out = np.empty(n, np.float32)
-    out_div = np.empty(n, np.float32)
-    rc = silu_lib.device_silu(g.ctypes.data, out.ctypes.data, out_div.ctypes.data, n)
+    out_nb = np.empty(n, np.float32)
+    rc = silu_lib.device_silu(g.ctypes.data, out.ctypes.data, out_nb.ctypes.data, n)
     assert rc == 0
     gf = (g.astype(np.uint32) << 16).view(np.float32)
     want = np.array([oracle.silu_mul_f32(float(v), 1.0) for v in gf], dtype=np.float32)
-    nan_w, nan_o = np.isnan(want), np.isnan(out)
-    assert np.array_equal(nan_w, nan_o), "NaN pattern differs"
-    ok = ~nan_w
-    bad = np.nonzero(out[ok].view(np.uint32) != want[ok].view(np.uint32))[0]
-    assert bad.size == 0, "%d inputs differ; first g = %r: device %r oracle %r" % (
-        bad.size, float(gf[ok][bad[0]]), float(out[ok][bad[0]]), float(want[ok][bad[0]]))
-    # CUDA's division on the same exp: same bits wherever the input is finite
-    fin = np.isfinite(gf)
-    assert np.array_equal(out[fin].view(np.uint32), out_div[fin].view(np.uint32))
+    _check(out, want, gf, "silu_f32")
+    _check(out_nb, want, gf, "silu_f32_nobranch")
