@@ -329,12 +329,17 @@ nvfp4_status nvfp4_linear_nvfp4_x(const uint8_t* x_packed, const uint8_t* x_scal
  *                     ceil(M/128)*128 * ceil(I/64)*4.
  *   flags             0 or NVFP4_STATIC_WEIGHTS (as for nvfp4_linear).
  *   workspace         >= nvfp4_workspace_bytes(2, M, K, I, 0) bytes; first 4 bytes the
- *                     error word; zeroed once when allocated.
+ *                     error word, then (fused path) the stream-K counters and partial
+ *                     tiles of the GEMM's last partial wave, or (other shapes) the
+ *                     linear's workspace and gu; zeroed once when allocated (the kernels
+ *                     leave the counters at zero).
  * Alignment: x, the weights, h_packed, h_scales_swizzled, workspace 16 bytes; the global
  * scales 4 bytes.
  * Dispatch: M > 16 with I % 128 == 0 runs one tcgen05 GEMM whose tiles pair 64 gate rows
  * with the 64 matching up rows; its epilogue rounds both to bf16, forms h and quantizes it
- * (nothing but the codes and scales reaches memory).  Other shapes write gu into the
+ * (nothing but the codes and scales reaches memory).  The tiles of its last partial wave
+ * are split over K across CTAs (stream-K): their fp32 partials go to the workspace and
+ * the CTA that completes a tile adds them in a fixed order before the activation.  Other shapes write gu into the
  * workspace with nvfp4_linear's kernels and quantize it with nvfp4_silu_mul_quantize's.
  */
 nvfp4_status nvfp4_linear_silu_mul_quantize(const void* x, int64_t M, int64_t K,

@@ -119,12 +119,12 @@ struct FuseArgs {
 // row and a warp reading a column both touch 32 distinct banks.
 constexpr int kXchPitch = 33;
 
-// Epilogue of one whole tile of the fused gate/up variant.  TMEM lanes 0..63 hold gate
-// columns 64 nb + l of h, lanes 64..127 the up columns; warps q = 0, 1 read gate
-// (their 32 lanes each), warps q = 2, 3 up, for the same 32 columns of h (q & 1).  Each
-// gate/up warp pair shares an exchange tile [m][i] and splits the work in halves.  Per 32
-// accumulator columns (32 rows m of x), values first rounded to bf16 as gw * acc (the
-// gate/up GEMM's output):
+// The fused gate/up epilogue for 32 accumulator columns (32 rows m of x) of a tile.  TMEM
+// lanes 0..63 hold gate columns 64 nb + l of h, lanes 64..127 the up columns; warps q = 0, 1
+// hold gate (their 32 lanes each), warps q = 2, 3 up, for the same 32 columns of h (q & 1).
+// `a` is this warp's raw fp32 accumulator for rows c0 .. c0 + 31 (one value per row, for its
+// lane's column).  Each gate/up warp pair shares an exchange tile [m][i] and splits the
+// work in halves, all values first rounded to bf16 as gw * acc (the gate/up GEMM's output):
 //   1. the gate warp takes silu of rows 0..15 itself and hands rows 16..31 of raw gate to
 //      the up warp through the tile;
 //   2. the up warp forms h = silu(g) * u for rows 16..31; the gate warp puts its silu
@@ -133,70 +133,142 @@ constexpr int kXchPitch = 33;
 //   4. lane l of each warp quantizes one 16-element block of row m = l -- columns 0..15
 //      by the gate warp, 16..31 by the up warp -- with the quantizer's one-thread block
 //      rule and the static global scale: 8 bytes of codes and a scale byte each.
-// Rows past M get no codes; their scale bytes inside the last 128-row block are zero.
+// Rows past M get no codes; their scale bytes inside the last 128-row block are zero.  All
+// four epilogue warps call it for the same c0 (it meets at named barrier 1).
+__device__ __forceinline__ void fused_rows32(const float (&a)[32], int q, int lane, int mb,
+                                             int c0, int ibase, float gw, float g,
+                                             const FuseArgs& fa, float* xw, int M, int m_pad,
+                                             int64_t cp4) {
+    const bool gate = q < 2;
+    const int hb = gate ? 0 : 1;  // the 16-column block this warp quantizes
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = bf16_to_f32(f32_to_bf16_rne(a[j] * gw));
+    if (gate) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = silu_f32_nobranch(v[j]);
+#pragma unroll
+        for (int j = 16; j < 32; ++j) xw[j * kXchPitch + lane] = v[j];
+    }
+    named_bar_sync(1, 128);
+    if (gate) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) xw[j * kXchPitch + lane] = v[j];
+    } else {
+#pragma unroll
+        for (int j = 16; j < 32; ++j)
+            xw[j * kXchPitch + lane] = __fmul_rn(silu_f32_nobranch(xw[j * kXchPitch + lane]), v[j]);
+    }
+    named_bar_sync(1, 128);
+    if (!gate) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            xw[j * kXchPitch + lane] = __fmul_rn(xw[j * kXchPitch + lane], v[j]);
+    }
+    named_bar_sync(1, 128);
+    const int m = mb * kBM + c0 + lane;
+    if (m < m_pad) {
+        float t[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) t[k] = xw[lane * kXchPitch + 16 * hb + k];
+        uint32_t lo, hi;
+        const uint32_t s8 = quantize_block16(t, g, lo, hi);
+        // the block is scale column ibase/16 + hb of the atom
+        uint8_t* sp = fa.hs + swizzle_offset(m, ibase / 16 + hb, cp4);
+        if (m < M) {
+            *reinterpret_cast<uint2*>(fa.hq + (int64_t)m * (fa.I / 2) + ibase / 2 + 8 * hb) =
+                make_uint2(lo, hi);
+            *sp = (uint8_t)s8;
+        } else {
+            *sp = 0;
+        }
+    }
+    named_bar_sync(1, 128);
+}
+
+// Epilogue of one whole tile of the fused gate/up variant (see fused_rows32).
 __device__ __forceinline__ void epilogue_silu_quant(uint32_t acc, int q, int lane, int tile,
                                                     int ntiles_m, float gw, const FuseArgs& fa,
-                                                    float* xch, int M, uint32_t accempty) {
+                                                    float* xch, int M) {
     const int nb = tile / ntiles_m, mb = tile % ntiles_m;
     const uint32_t taddr = acc + ((uint32_t)(q * 32) << 16);
     const float g = *fa.gh;
     const int64_t cp4 = (fa.I / 16 + 3) / 4;
     const int m_pad = (M + 127) / 128 * 128;
-    const bool gate = q < 2;
-    const int hb = gate ? 0 : 1;                // the 16-column block this warp quantizes
     const int ibase = nb * 64 + (q & 1) * 32;   // this warp pair's 32 columns of h
     float* xw = xch + (q & 1) * 32 * kXchPitch;
 #pragma unroll 1
     for (int c0 = 0; c0 < kBM; c0 += 32) {
         uint32_t u[32];
         tc::tmem_ld32(taddr + c0, u);
-        float v[32];
+        float a[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = bf16_to_f32(f32_to_bf16_rne(__uint_as_float(u[j]) * gw));
-        if (gate) {
+        for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(u[j]);
+        fused_rows32(a, q, lane, mb, c0, ibase, gw, g, fa, xw, M, m_pad, cp4);
+    }
+}
+
+// Epilogue of a stream-K segment of a fused tile.  Each warp writes its quarter of the
+// partial accumulator to the CTA's slot (the layout of tc::epilogue_work) and releases
+// the accumulator; the four warps then count the segment once for the tile (one counter
+// per tile, wrapping back to zero).  The CTA whose count completes the tile sums every
+// segment's partials in segment order (a fixed order: deterministic) 32 rows at a time and
+// runs the fused activation on the sums.  *last is a shared word the four warps meet on.
+__device__ __forceinline__ void epilogue_silu_quant_sk(uint32_t acc, int q, int lane, int tile,
+                                                       int ntiles_m, int nkb, int p_sk,
+                                                       int64_t tsk, float gw,
+                                                       const FuseArgs& fa, float* xch, int M,
+                                                       uint32_t accempty, float* slots,
+                                                       uint32_t* counters,
+                                                       volatile uint32_t* last) {
+    constexpr size_t kSlotFloats = (size_t)kBN * kBM;
+    const uint32_t taddr = acc + ((uint32_t)(q * 32) << 16);
+    const int64_t t0 = (int64_t)tile * nkb;
+    const int cf = tc::sk_cta_of(t0, p_sk, tsk), cl = tc::sk_cta_of(t0 + nkb - 1, p_sk, tsk);
+    float* mine = slots + (size_t)tc::sk_slot(blockIdx.x, t0, p_sk, tsk) * kSlotFloats +
+                  tc::slot_chunk<kBM>(q, 0) + lane;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBM; c0 += 32) {
+        uint32_t u[32];
+        tc::tmem_ld32(taddr + c0, u);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = silu_f32_nobranch(v[j]);
-#pragma unroll
-            for (int j = 16; j < 32; ++j) xw[j * kXchPitch + lane] = v[j];
-        }
-        named_bar_sync(1, 128);
-        if (gate) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xw[j * kXchPitch + lane] = v[j];
-        } else {
-#pragma unroll
-            for (int j = 16; j < 32; ++j)
-                xw[j * kXchPitch + lane] = __fmul_rn(silu_f32_nobranch(xw[j * kXchPitch + lane]), v[j]);
-        }
-        named_bar_sync(1, 128);
-        if (!gate) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                xw[j * kXchPitch + lane] = __fmul_rn(xw[j * kXchPitch + lane], v[j]);
-        }
-        named_bar_sync(1, 128);
-        const int m = mb * kBM + c0 + lane;
-        if (m < m_pad) {
-            float t[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) t[k] = xw[lane * kXchPitch + 16 * hb + k];
-            uint32_t lo, hi;
-            const uint32_t s8 = quantize_block16(t, g, lo, hi);
-            // the block is scale column ibase/16 + hb of the atom
-            uint8_t* sp = fa.hs + swizzle_offset(m, ibase / 16 + hb, cp4);
-            if (m < M) {
-                *reinterpret_cast<uint2*>(fa.hq + (int64_t)m * (fa.I / 2) + ibase / 2 + 8 * hb) =
-                    make_uint2(lo, hi);
-                *sp = (uint8_t)s8;
-            } else {
-                *sp = 0;
-            }
-        }
-        named_bar_sync(1, 128);
+        for (int j = 0; j < 32; ++j) mine[(size_t)(c0 + j) * 32] = __uint_as_float(u[j]);
     }
     tc::fence_before();
     __syncwarp();
     if (lane == 0) tc::arrive(accempty);
+    __threadfence();
+    named_bar_sync(1, 128);  // all four quarters are in the slot
+    if (q == 0 && lane == 0)
+        *last = atomicInc(&counters[tile * 4], (unsigned)(cl - cf)) == (unsigned)(cl - cf);
+    named_bar_sync(1, 128);
+    const bool is_last = *last != 0;
+    named_bar_sync(1, 128);  // every warp has read the flag before it is written again
+    if (!is_last) return;
+    __threadfence();
+    const int nb = tile / ntiles_m, mb = tile % ntiles_m;
+    const float g = *fa.gh;
+    const int64_t cp4 = (fa.I / 16 + 3) / 4;
+    const int m_pad = (M + 127) / 128 * 128;
+    const int ibase = nb * 64 + (q & 1) * 32;
+    float* xw = xch + (q & 1) * 32 * kXchPitch;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBM; c0 += 32) {
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = 0.0f;
+#pragma unroll 1
+        for (int cs = cf; cs <= cl; ++cs) {
+            const float* sp = slots + (size_t)tc::sk_slot(cs, t0, p_sk, tsk) * kSlotFloats +
+                              tc::slot_chunk<kBM>(q, c0) + lane;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __ldcg(sp + (size_t)j * 32);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a[j] += v[j];
+        }
+        fused_rows32(a, q, lane, mb, c0, ibase, gw, g, fa, xw, M, m_pad, cp4);
+    }
 }
 
 template <bool kFuse>
@@ -347,8 +419,19 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 // (any warp's failed wait stops all four)
                 if (named_bar_red_or(1, 128, !ok)) break;
                 tc::fence_after();
-                epilogue_silu_quant(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m, g, fa,
-                                    reinterpret_cast<float*>(base + L::kOffXch), M, accempty(b));
+                if (kb0 == 0 && kb1 == nkb) {
+                    epilogue_silu_quant(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m, g,
+                                        fa, reinterpret_cast<float*>(base + L::kOffXch), M);
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::arrive(accempty(b));
+                } else
+                    epilogue_silu_quant_sk(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m,
+                                           nkb, p_sk, tsk, g, fa,
+                                           reinterpret_cast<float*>(base + L::kOffXch), M,
+                                           accempty(b), slots, counters,
+                                           reinterpret_cast<volatile uint32_t*>(
+                                               base + L::kOffMisc + 8));
             } else {
                 if (!ok) break;
                 tc::fence_after();
@@ -476,16 +559,13 @@ bool gemm_w4a16_silu_takes(int64_t M, int64_t I, const DevInfo& dev) {
 
 cudaError_t launch_gemm_w4a16_silu(const uint16_t* x, int M, int K, const uint8_t* wq,
                                    const uint8_t* wsz, const float* gw, int I, const float* gh,
-                                   uint8_t* hq, uint8_t* hs, uint32_t* err, cudaStream_t stream,
-                                   const DevInfo& dev) {
+                                   uint8_t* hq, uint8_t* hs, uint8_t* workspace,
+                                   cudaStream_t stream, const DevInfo& dev) {
     if (!gemm_w4a16_silu_takes(M, I, dev)) return cudaErrorInvalidConfiguration;
-    // whole tiles only (each tile needs gate and up complete before the activation):
-    // 64-column pairs of h x 256 rows of x, persistent CTAs
-    GemmPlan p;
-    p.nkb = (K + kBK - 1) / kBK;
-    p.ntiles_m = (M + kBM - 1) / kBM;
-    p.ntiles = (I / 64) * p.ntiles_m;
-    p.grid = p.ntiles < dev.sm_count ? p.ntiles : dev.sm_count;
+    // tiles of 64-column pairs of h (64 gate + 64 up rows of W) x 256 rows of x, persistent
+    // CTAs; the last partial wave goes stream-K (the tile count and the split of the plain
+    // GEMM on 2I rows)
+    const GemmPlan p = gemm_w4a16_plan(M, K, 2 * (int64_t)I, dev.sm_count);
     CUtensorMap mx, mw;
     cudaError_t e = tc::make_map_2d(&mx, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (uint64_t)K,
                                     (uint64_t)M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -500,9 +580,13 @@ cudaError_t launch_gemm_w4a16_silu(const uint16_t* x, int M, int K, const uint8_
     fa.gh = gh;
     fa.hq = hq;
     fa.hs = hs;
+    uint32_t* err = reinterpret_cast<uint32_t*>(workspace);
+    uint32_t* counters = reinterpret_cast<uint32_t*>(workspace + kGemmHeaderBytes);
+    float* slots = reinterpret_cast<float*>(workspace + kGemmHeaderBytes +
+                                            tc::counters_bytes(p.ntiles));
     gemm_w4a16_kernel<true><<<p.grid, kThreads, Smem<true>::kBytes, stream>>>(
-        mx, mw, wsz, gw, nullptr, 1, M, 2 * I, p.nkb, p.ntiles_m, p.ntiles, 0, 0, 0, err,
-        nullptr, nullptr, fa, current_wait_cfg());
+        mx, mw, wsz, gw, nullptr, 1, M, 2 * I, p.nkb, p.ntiles_m, p.ntiles, p.ntiles_sk, p.p_sk,
+        p.tsk, err, counters, slots, fa, current_wait_cfg());
     return cudaGetLastError();
 }
 

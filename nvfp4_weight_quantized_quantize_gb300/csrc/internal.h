@@ -112,8 +112,8 @@ cudaError_t launch_gemm_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
 bool gemm_w4a16_silu_takes(int64_t M, int64_t I, const DevInfo& dev);
 cudaError_t launch_gemm_w4a16_silu(const uint16_t* x, int M, int K, const uint8_t* wq,
                                    const uint8_t* wsz, const float* gw, int I, const float* gh,
-                                   uint8_t* hq, uint8_t* hs, uint32_t* err, cudaStream_t stream,
-                                   const DevInfo& dev);
+                                   uint8_t* hq, uint8_t* hs, uint8_t* workspace,
+                                   cudaStream_t stream, const DevInfo& dev);
 
 // M > 16 W4A4 GEMM (block-scaled tcgen05.mma, kind::mxf4nvf4).  xq [M, K/2] and xsz (scale
 // atoms of x) and gx come from the quantizer; wsz: the atom part of W's repacked scales.

@@ -120,8 +120,9 @@ W4A4Layout w4a4_layout(int64_t M, int64_t K, int64_t N) {
 
 constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
-// nvfp4_linear_silu_mul_quantize's workspace: the fused GEMM needs only the error word;
-// otherwise the linear's own workspace (error word first), then gu bf16 [M, 2I]
+// nvfp4_linear_silu_mul_quantize's workspace: the fused GEMM's (error word, stream-K
+// counters and partial tiles, as the W4A16 GEMM's on 2I rows); otherwise the linear's own
+// workspace (error word first), then gu bf16 [M, 2I]
 struct SiluLayout {
     bool fused;
     size_t gu, total;
@@ -132,7 +133,7 @@ SiluLayout silu_layout(int64_t M, int64_t K, int64_t I) {
     L.fused = M > kGemvMaxM && I % 128 == 0;
     if (L.fused) {
         L.gu = 0;
-        L.total = kHeaderBytes;
+        L.total = gemm_w4a16_workspace_bytes(M, K, 2 * I);
         return L;
     }
     const size_t lin = M <= kGemvMaxM ? kHeaderBytes : gemm_w4a16_workspace_bytes(M, K, 2 * I);
@@ -419,8 +420,7 @@ NVFP4_API nvfp4_status nvfp4_linear_silu_mul_quantize(
         if (!gemm_w4a16_silu_takes(M, I, d)) return NVFP4_ERR_UNSUPPORTED;
         return from_cuda(launch_gemm_w4a16_silu(xb, (int)M, (int)K, w_packed, w_scales_swizzled,
                                                 w_global_scale, (int)I, h_global_scale,
-                                                h_packed, h_scales_swizzled,
-                                                reinterpret_cast<uint32_t*>(ws), stream, d));
+                                                h_packed, h_scales_swizzled, ws, stream, d));
     }
     uint16_t* gu = reinterpret_cast<uint16_t*>(ws + L.gu);
     const int N = (int)(2 * I);

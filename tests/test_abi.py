@@ -205,7 +205,9 @@ def test_linear_silu_mul_quantize_rejects(lib):
 
 def test_linear_silu_mul_quantize_workspace_sizes():
     # fused (M > 16, I % 128 == 0): the error word alone; otherwise room for gu [M, 2I] bf16
-    assert nv.nvfp4_workspace_bytes(2, 512, 5120, 17408) == 256
+    # fused path: the GEMM's stream-K state on 2I rows
+    assert nv.nvfp4_workspace_bytes(2, 512, 5120, 17408) == \
+        nv.nvfp4_workspace_bytes(1, 512, 5120, 2 * 17408, nv.NVFP4_W4A16)
     assert nv.nvfp4_workspace_bytes(2, 4, 5120, 17408) >= 256 + 4 * 2 * 17408 * 2
     assert nv.nvfp4_workspace_bytes(2, 40, 64, 96) >= 40 * 2 * 96 * 2
     assert nv.nvfp4_workspace_bytes(2, 40, 64, 24) == 2 ** 64 - 1
