@@ -167,10 +167,14 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
     for (int u = 0; u < U; ++u) {
         const int c = cbase + 4 * u;
         const bool ok = g < M && c < rowchunks;
-        const uint16_t* xp = x + (int64_t)g * K + 32 * c;
+        const uint4* xp = reinterpret_cast<const uint4*>(x + (int64_t)g * K + 32 * c);
+        // the chunk's 64 bytes in four 16-byte loads (x is 16-byte aligned, K % 32 == 0)
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            raw[u][j] = ok ? *reinterpret_cast<const uint2*>(xp + 4 * j) : make_uint2(0u, 0u);
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = ok ? xp[q] : make_uint4(0u, 0u, 0u, 0u);
+            raw[u][2 * q] = make_uint2(v.x, v.y);
+            raw[u][2 * q + 1] = make_uint2(v.z, v.w);
+        }
     }
     if constexpr (kXQ) {
         // W4A4 with a static activation scale: each chunk's two blocks quantized here
