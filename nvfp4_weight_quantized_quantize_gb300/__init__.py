@@ -31,7 +31,7 @@ EXPORTS = ("nvfp4_quantize", "nvfp4_repack", "nvfp4_linear", "nvfp4_repack_bytes
            "nvfp4_status_str", "nvfp4_encode_elements", "nvfp4_quantize_noalloc",
            "nvfp4_last_cuda_error", "nvfp4_quantize_fp8_block128", "nvfp4_silu_mul_quantize",
            "nvfp4_linear_nvfp4_x", "nvfp4_linear_silu_mul_quantize",
-           "nvfp4_debug_expire_waits")
+           "nvfp4_debug_expire_waits", "nvfp4_debug_w4a4_kernel")
 
 
 class Nvfp4Error(RuntimeError):
@@ -67,6 +67,7 @@ def load(path: str = LIB_PATH):
         "nvfp4_quantize_noalloc": (I, [P, I, I64, I64, P, P, P, P]),
         "nvfp4_last_cuda_error": (ctypes.c_char_p, []),
         "nvfp4_debug_expire_waits": (None, [I]),
+        "nvfp4_debug_w4a4_kernel": (None, [I]),
         "nvfp4_quantize_fp8_block128": (I, [P, P, I64, I64, P, P, P, P, SZ, P]),
         "nvfp4_silu_mul_quantize": (I, [P, I64, I64, P, P, SZ, P, P, P, SZ, P]),
         "nvfp4_linear_nvfp4_x": (I, [P, P, P, I64, I64, P, P, P, I64, P, I, I, P, SZ, P]),
@@ -259,6 +260,16 @@ def nvfp4_debug_expire_waits(on: bool) -> None:
     """Test switch: the calling thread's next nvfp4_linear kernels make a bounded wait run
     out (see include/nvfp4.h)."""
     load().nvfp4_debug_expire_waits(1 if on else 0)
+
+
+W4A4_KERNELS = {"auto": 0, "one_cta": 1, "pair": 2, "pair2": 3}
+
+
+def nvfp4_debug_w4a4_kernel(which: str) -> None:
+    """Test switch: the kernel of the calling thread's W4A4 GEMMs at M > 16 -- "auto" (the
+    default, the one-CTA kernel), "one_cta", "pair" (CTA pairs) or "pair2" (clusters of two
+    pairs sharing x by multicast); see include/nvfp4.h."""
+    load().nvfp4_debug_w4a4_kernel(W4A4_KERNELS[which])
 
 
 def nvfp4_encode_elements(inp: torch.Tensor, e2m1_out: torch.Tensor | None,

@@ -442,7 +442,8 @@ gemm_w4a16_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 tc::epilogue_work<kBN, kBM>(tmem + (uint32_t)(b * kBM), q, lane, tile, ntiles_m,
                                             kb0 == 0 && kb1 == nkb, nkb, p_sk, tsk, g, y, y_bf16,
                                             M, N, slots, counters, accempty(b), stage,
-                                            bar_ptr(fixbar0 + 128u * q), kFixupBufs, err);
+                                            bar_ptr(fixbar0 + 128u * q), kFixupBufs,
+                                            tc::SkUnit{(int)blockIdx.x, 0, 1}, err);
             }
         }
     } else {

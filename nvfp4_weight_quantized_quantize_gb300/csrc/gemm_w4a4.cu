@@ -194,6 +194,95 @@ __device__ __forceinline__ void quantize_x_all(const QxArgs& qa, int M, float g)
     }
 }
 
+// The kQuantX prologue, run by every thread of every CTA after the CTA's barriers and TMEM
+// are set up: g_x (the static scale, or the amax of all of x through one grid-wide barrier,
+// then amax / 2688), then this CTA's share of x quantized and counted done.  Returns g_x;
+// a failed grid barrier sets abort_flag (the GEMM roles then stop at once).
+template <int kNumWarps>
+__device__ __forceinline__ float quantize_x_prologue(const QxArgs& qa, int M, const WaitCfg& dbg,
+                                                     uint32_t* err, volatile int* abort_flag) {
+    __shared__ int qx_fail;
+    __shared__ float red[kNumWarps];
+    __shared__ float g_sh;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) qx_fail = 0;
+    float g = 1.0f;
+    if (qa.gx_static) {
+        g = *qa.gx_static;
+    } else {
+        // amax of x: a partial per CTA, a grid barrier, then every CTA folds them
+        float am = 0.0f;
+        const int64_t nvec = (int64_t)M * qa.K / 8;
+        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+        const uint4* xv = reinterpret_cast<const uint4*>(qa.x);
+        for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < nvec;
+             i0 += 8 * stride) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                v[u] = i0 + u * stride < nvec ? __ldg(xv + i0 + u * stride)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    am = fmaxf(am, fmaxf(fabsf(bf16_to_f32(w[j] & 0xFFFFu)),
+                                         fabsf(bf16_to_f32(w[j] >> 16))));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) red[warp] = am;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float r = red[0];
+            for (int i = 1; i < kNumWarps; ++i) r = fmaxf(r, red[i]);
+            qa.partials[blockIdx.x] = r;
+            if (!grid_barrier(qa.sync, dbg.wait_ns)) {
+                if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+                qx_fail = 1;
+            }
+        }
+        __syncwarp();  // warp 0 converged (thread 0 spun alone) before the block barrier
+        __syncthreads();
+        if (!qx_fail) {
+            // every CTA's partial (read from L2: other CTAs wrote them in this kernel)
+            float m = 0.0f;
+            for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x)
+                m = fmaxf(m, __ldcg(qa.partials + i));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            __syncthreads();
+            if (lane == 0) red[warp] = m;
+            __syncthreads();
+            float r = red[0];
+            for (int i = 1; i < kNumWarps; ++i) r = fmaxf(r, red[i]);
+            g = global_scale_from_amax(r);
+        }
+    }
+    if (threadIdx.x == 0) {
+        g_sh = g;
+        if (blockIdx.x == 0) *qa.gx_out = g;
+    }
+    if (!qx_fail) {
+        quantize_x_all(qa, M, g);
+        // this CTA's share is written: publish it to the async proxy, then count it
+        fence_proxy_async_global();
+        __syncthreads();
+        // (with the test switch on, CTA 0 withholds its count: every producer's wait for the
+        // count runs out)
+        if (threadIdx.x == 0 && !(dbg.stall && blockIdx.x == 0)) {
+            __threadfence();
+            atomicAdd(qa.sync + 3, 1u);
+        }
+    }
+    __syncthreads();
+    if (qx_fail && threadIdx.x == 0) *abort_flag = 1;
+    __syncthreads();
+    return g_sh;
+}
+
 template <bool kQuantX>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
@@ -245,88 +334,10 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
     const uint32_t tmem = *tmem_slot;
 
     // ---- x quantized in-kernel (kQuantX): every CTA quantizes a share of x and counts
-    // itself done; the producer waits for the count to reach the grid before its first
-    // load of x ----
-    __shared__ float gx_sh;
-    if constexpr (kQuantX) {
-        __shared__ int qx_fail;
-        if (threadIdx.x == 0) qx_fail = 0;
-        float g = 1.0f;
-        if (qa.gx_static) {
-            g = *qa.gx_static;
-        } else {
-            // amax of x: a partial per CTA, a grid barrier, then every CTA folds them
-            float am = 0.0f;
-            const int64_t nvec = (int64_t)M * qa.K / 8;
-            const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-            const uint4* xv = reinterpret_cast<const uint4*>(qa.x);
-            for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < nvec;
-                 i0 += 8 * stride) {
-                uint4 v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    v[u] = i0 + u * stride < nvec ? __ldg(xv + i0 + u * stride)
-                                                  : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        am = fmaxf(am, fmaxf(fabsf(bf16_to_f32(w[j] & 0xFFFFu)),
-                                             fabsf(bf16_to_f32(w[j] >> 16))));
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-            __shared__ float red[kThreads / 32];
-            if (lane == 0) red[warp] = am;
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                float r = red[0];
-                for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
-                qa.partials[blockIdx.x] = r;
-                if (!grid_barrier(qa.sync, dbg.wait_ns)) {
-                    if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
-                    qx_fail = 1;
-                }
-            }
-            __syncwarp();  // warp 0 converged (thread 0 spun alone) before the block barrier
-            __syncthreads();
-            if (!qx_fail) {
-                // every CTA's partial (read from L2: other CTAs wrote them in this kernel)
-                float m = 0.0f;
-                for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x)
-                    m = fmaxf(m, __ldcg(qa.partials + i));
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                __syncthreads();
-                if (lane == 0) red[warp] = m;
-                __syncthreads();
-                float r = red[0];
-                for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
-                g = global_scale_from_amax(r);
-            }
-        }
-        if (threadIdx.x == 0) {
-            gx_sh = g;
-            if (blockIdx.x == 0) *qa.gx_out = g;
-        }
-        if (!qx_fail) {
-            quantize_x_all(qa, M, g);
-            // this CTA's share is written: publish it to the async proxy, then count it
-            fence_proxy_async_global();
-            __syncthreads();
-            // (with the test switch on, CTA 0 withholds its count: every producer's wait
-            // for the count runs out)
-            if (threadIdx.x == 0 && !(dbg.stall && blockIdx.x == 0)) {
-                __threadfence();
-                atomicAdd(qa.sync + 3, 1u);
-            }
-        }
-        __syncthreads();
-        if (qx_fail && threadIdx.x == 0) *abort_flag = 1;
-        __syncthreads();
-    }
+    // itself done; the TMA producer waits for the count to reach the grid before its
+    // first load of x ----
+    float gx_in = 1.0f;
+    if constexpr (kQuantX) gx_in = quantize_x_prologue<kThreads / 32>(qa, M, dbg, err, abort_flag);
 
     // scale atoms of K step kb: 4, or fewer at the end of K
     auto atoms_of = [&](int kb) { return min(4, natoms_row - 4 * kb); };
@@ -471,7 +482,7 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
     } else {
         // ---------------- epilogue ----------------
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const float g = *gw * (kQuantX ? gx_sh : *gx);
+        const float g = *gw * (kQuantX ? gx_in : *gx);
         int lt = 0;
         tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk);
         int tile, kb0, kb1;
@@ -487,7 +498,8 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             tc::epilogue_work<kBN, kBM>(tmem, q, lane, tile, ntiles_m, kb0 == 0 && kb1 == nkb,
                                         nkb, p_sk, tsk, g, y, y_bf16, M, N, slots, counters,
                                         accempty(0), stage, bar_ptr(fixbar0 + 128u * q),
-                                        kFixupBufs, err);
+                                        kFixupBufs, tc::SkUnit{(int)blockIdx.x, 0, 1},
+                                        err);
         }
     }
 
@@ -509,6 +521,344 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
         }
     }
+}
+
+// ---- CTA-pair kernel ---------------------------------------------------------------------
+//
+// A cluster of kPairs CTA pairs (two SMs each) computes a (kPairs x 256) (W) x 256 (x) tile
+// with M = 256 block-scaled MMAs (tcgen05.mma.cta_group::2): in each pair the even CTA
+// issues the MMAs, the MMA's A is split by rows across the pair's two CTAs and B by N.  CTA
+// (pair p, rank r) holds W rows (4 nb + 2 p + r) x 128 .. +128 of the cluster tile nb and
+// half r of the tile's x rows; per K step of 256 it takes in 38 KB: 16 KB of W codes, 16 KB
+// of x codes, 2 KB of W scale atoms and the 4 KB of scale atoms of all 256 x rows, which
+// every CTA's TMEM must hold.  The one-CTA kernel takes in 54 KB for the same MMA work.
+// With two pairs per cluster (kPairs = 2) the pairs share the x tile: the x codes and the
+// x scale atoms each CTA needs are loaded once for the cluster and multicast, so the
+// cluster reads 30 KB per CTA and K step from L2 rather than 38.
+//
+// Every copy is a TMA load that lands in shared memory at the same offset in each CTA it
+// is for and completes on the stage barrier of that CTA's pair's even CTA, which expects
+// both CTAs' bytes.  One thread of each even CTA moves the stage's scale atoms from both
+// CTAs' shared memory into their TMEM (tcgen05.cp.cta_group::2, in order ahead of the MMAs
+// that read them) and issues the four MMAs; its commit releases the stage in every CTA of
+// the cluster (each stage barrier counts one release per pair, since every CTA's stage
+// receives bytes that CTAs of both pairs load).  Each CTA's TMEM holds the fp32
+// accumulator of its own 128 W rows x the tile's 256 x rows (columns 0..255) and the
+// scales of the stages in flight.
+//
+// Warp roles per CTA:
+//   warp 0      TMA producer (every CTA; all wait on their own stage barriers, which the
+//               even CTAs' MMA commits release together);
+//   warp 1      TMEM allocation (both CTAs of a pair together), MMA issue (even CTAs);
+//   warps 2-9   epilogue: lane quarter (warp & 3), x-row half (warp - 2) / 4.  A whole tile
+//               is read out of TMEM into registers (128 columns per warp) and the
+//               accumulator released before the stores, so the next tile's MMAs overlap
+//               them; a stream-K segment is written by the first half's warps (the
+//               shared stream-K epilogue, per 128-row part of the tile), the second
+//               half's warps release at once.
+namespace pairk {
+
+constexpr int kBM = 256;   // x rows per tile (MMA N), 128 loaded by each CTA of a pair
+constexpr int kBK = 256;   // K per stage
+constexpr int kStages = 5;
+constexpr int kThreads = 10 * 32;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kTmemSf = kBM;
+constexpr uint32_t kSfColsPerStage = 48;
+constexpr uint32_t kABytes = 128 * kBK / 2;       // 16 KB: this CTA's W rows
+constexpr uint32_t kBBytes = 128 * kBK / 2;       // 16 KB: this CTA's half of the x rows
+constexpr uint32_t kAtomBytes = 512;
+constexpr uint32_t kSfaBytes = 4 * kAtomBytes;    // W atoms of the CTA's 128 rows
+constexpr uint32_t kSfbBytes = 8 * kAtomBytes;    // x atoms of both 128-row blocks [rb][j]
+constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kABytes;
+constexpr uint32_t kOffSfa = kOffB + kStages * kBBytes;
+constexpr uint32_t kOffSfb = kOffSfa + kStages * kSfaBytes;
+constexpr uint32_t kOffBar = kOffSfb + kStages * kSfbBytes;
+constexpr uint32_t kFixBars = 4 * 16;
+constexpr uint32_t kNumBars = 2 * kStages + 3 + kFixBars;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
+static_assert(kTmemSf + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+constexpr uint32_t kFixupBytes = (kOffBar / 4) & ~127u;
+constexpr int kFixupBufs = (int)(kFixupBytes / 4096) < 16 ? (int)(kFixupBytes / 4096) : 16;
+static_assert(kFixupBufs >= 2, "fix-up staging");
+// block-scaled kind, E2M1 A and B, UE4M3 scales, K-major, fp32 D, M = 256 (the pair), N = 256
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kBM >> 3) << 17) |
+                            ((uint32_t)(256 >> 4) << 24);
+// how long a producer waits at exit for copies it issued that no MMA consumed (after an
+// abort): far longer than any copy takes to land
+constexpr uint64_t kDrainNs = 1000000;
+
+}  // namespace pairk
+
+template <bool kQuantX, int kPairs>
+__global__ void __launch_bounds__(pairk::kThreads, 1)
+gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                      const __grid_constant__ CUtensorMap tmap_x,
+                      const __grid_constant__ CUtensorMap tmap_sw,
+                      const __grid_constant__ CUtensorMap tmap_sx, const float* __restrict__ gw,
+                      const float* __restrict__ gx, void* __restrict__ y, int y_bf16, int M,
+                      int N, int nkb, int natoms_row, int ntiles_m, int ntiles, int ntiles_sk,
+                      int p_sk, int64_t tsk, uint32_t* __restrict__ err,
+                      uint32_t* __restrict__ counters, float* __restrict__ slots, QxArgs qa,
+                      WaitCfg dbg) {
+    // this kernel's constants (the one-CTA kernel's share the names)
+    constexpr int kBM = pairk::kBM, kBK = pairk::kBK, kStages = pairk::kStages;
+    constexpr int kThreads = pairk::kThreads, kTmemCols = pairk::kTmemCols;
+    constexpr int kFixupBufs = pairk::kFixupBufs;
+    constexpr uint32_t kTmemSf = pairk::kTmemSf, kSfColsPerStage = pairk::kSfColsPerStage;
+    constexpr uint32_t kABytes = pairk::kABytes, kBBytes = pairk::kBBytes;
+    constexpr uint32_t kAtomBytes = pairk::kAtomBytes, kSfaBytes = pairk::kSfaBytes;
+    constexpr uint32_t kSfbBytes = pairk::kSfbBytes, kStageBytes = pairk::kStageBytes;
+    constexpr uint32_t kOffA = pairk::kOffA, kOffB = pairk::kOffB, kOffSfa = pairk::kOffSfa;
+    constexpr uint32_t kOffSfb = pairk::kOffSfb, kOffBar = pairk::kOffBar;
+    constexpr uint32_t kOffMisc = pairk::kOffMisc, kFixBars = pairk::kFixBars;
+    constexpr uint32_t kFixupBytes = pairk::kFixupBytes, kIdesc = pairk::kIdesc;
+    constexpr uint64_t kDrainNs = pairk::kDrainNs;
+    constexpr int kCtas = 2 * kPairs;                        // CTAs per cluster
+    constexpr uint16_t kAll = (uint16_t)((1u << kCtas) - 1);
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_s - raw_s);
+    const uint32_t bar0 = base_s + kOffBar;
+    auto full = [&](int s) { return bar0 + 8u * s; };              // even CTAs' are used
+    auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+    const uint32_t accfull = bar0 + 8u * (2 * kStages);
+    const uint32_t accempty = bar0 + 8u * (2 * kStages + 1);      // even CTAs' are used
+    const uint32_t drain = bar0 + 8u * (2 * kStages + 2);
+    const uint32_t fixbar0 = bar0 + 8u * (2 * kStages + 3);
+    auto bar_ptr = [&](uint32_t a) { return reinterpret_cast<uint64_t*>(base + (a - base_s)); };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t cr = tc::cluster_rank();            // rank in the cluster
+    const uint32_t rank = cr & 1u;                     // rank in the pair
+    const uint32_t leader = cr & ~1u;                  // the pair's even CTA
+    const int pp = (int)(cr >> 1);                     // the pair in the cluster
+    const uint16_t pair_mask = (uint16_t)(3u << leader);
+    const int unit = (int)(blockIdx.x / kCtas), nunits = (int)(gridDim.x / kCtas);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_ptr(full(s)), 1);
+            mbar_init(bar_ptr(empty(s)), kPairs);  // one release from each pair's issuer
+        }
+        mbar_init(bar_ptr(accfull), 1);
+        mbar_init(bar_ptr(accempty), 16);  // 8 epilogue warps in each CTA of the pair
+        mbar_init(bar_ptr(drain), 1);
+        for (uint32_t i = 0; i < kFixBars; ++i) mbar_init(bar_ptr(fixbar0 + 8u * i), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::tmem_alloc_pair(base_s + kOffMisc, kTmemCols);
+    tc::fence_before();
+    tc::cluster_sync();  // every CTA's barriers initialised, TMEM allocated
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    float gx_in = 1.0f;
+    if constexpr (kQuantX) gx_in = quantize_x_prologue<kThreads / 32>(qa, M, dbg, err, abort_flag);
+
+    auto atoms_of = [&](int kb) { return min(4, natoms_row - 4 * kb); };
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int it = 0, issued = 0;
+            tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk, unit, nunits);
+            int tile, kb0, kb1;
+            if constexpr (kQuantX) {
+                if (!*abort_flag && !wait_counter(qa.sync + 3, gridDim.x, dbg.wait_ns)) {
+                    if (err) atomicOr(err, NVFP4_DEVERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                fence_proxy_async_global();
+            }
+            while (!*abort_flag && wi.next(tile, kb0, kb1)) {
+                const int nb = tile / ntiles_m, mb = tile % ntiles_m;
+                const int wrb = (int)(nb * kCtas + cr);  // this CTA's 128-row block of W
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (it >= kStages &&
+                        !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err,
+                                           dbg.wait_ns))
+                        break;
+                    const uint32_t fb = tc::peer_addr(full(s), leader);
+                    if (rank == 0) mbar_arrive_expect_tx(bar_ptr(full(s)), 2 * kStageBytes);
+                    tc::tma_load_2d_pair(base_s + kOffA + s * kABytes, &tmap_w, kb * (kBK / 2),
+                                         wrb * 128, fb);
+                    tc::tma_load_2d_pair(base_s + kOffSfa + s * kSfaBytes, &tmap_sw, 0,
+                                         wrb * natoms_row + 4 * kb, fb);
+                    // x rows of the tile: half `rank` of them, 128 rows; the x scale atoms of
+                    // both 128-row blocks, 4 per block (atoms past K or past the tensor's rows
+                    // read as zero or as a neighbour's, which no MMA reads or whose outputs
+                    // are masked)
+                    const uint32_t b_dst = base_s + kOffB + s * kBBytes;
+                    const uint32_t sb_dst = base_s + kOffSfb + s * kSfbBytes;
+                    if constexpr (kPairs == 1) {
+                        tc::tma_load_2d_pair(b_dst, &tmap_x, kb * (kBK / 2),
+                                             mb * kBM + (int)rank * 128, fb);
+                        tc::tma_load_2d_pair(sb_dst, &tmap_sx, 0, (2 * mb) * natoms_row + 4 * kb,
+                                             fb);
+                        tc::tma_load_2d_pair(sb_dst + 4 * kAtomBytes, &tmap_sx, 0,
+                                             (2 * mb + 1) * natoms_row + 4 * kb, fb);
+                    } else {
+                        // shared by the two pairs: pair pp loads 64 of the 128 x rows for the
+                        // CTAs of rank `rank` in both pairs, and 2 of the 4 atoms of x row
+                        // block `rank` for every CTA
+                        const uint16_t same_rank = (uint16_t)((1u << rank) | (1u << (2 + rank)));
+                        tc::tma_load_2d_pair_mc(b_dst + pp * (kBBytes / 2), &tmap_x,
+                                                kb * (kBK / 2), mb * kBM + (int)rank * 128 + pp * 64,
+                                                fb, same_rank);
+                        tc::tma_load_2d_pair_mc(sb_dst + rank * 4 * kAtomBytes + pp * 2 * kAtomBytes,
+                                                &tmap_sx, 0,
+                                                (2 * mb + (int)rank) * natoms_row + 4 * kb + 2 * pp,
+                                                fb, kAll);
+                    }
+                    issued = it + 1;
+                }
+            }
+            // Before the CTA moves on to exit, the copies it issued have landed: an even
+            // CTA sees its stage barriers complete, an odd CTA sees its stages released
+            // (consumed); after an abort neither may come, and the wait ends after kDrainNs,
+            // far longer than a copy takes.
+            const uint64_t t0 = globaltimer_ns();
+            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i) {
+                const uint64_t el = globaltimer_ns() - t0;
+                if (el >= kDrainNs) break;
+                const uint32_t b = rank == 0 ? full(i % kStages) : empty(i % kStages);
+                mbar_wait_bounded(bar_ptr(b), (i / kStages) & 1, kDrainNs - el);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issue (even CTAs) ----------------
+        if (rank == 0 && lane == 0) {
+            int it = 0, lt = 0;
+            tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk, unit, nunits);
+            int tile, kb0, kb1;
+            for (; !*abort_flag && wi.next(tile, kb0, kb1); ++lt) {
+                if (lt >= 1 &&
+                    !tc::wait_or_abort(accempty, (lt - 1) & 1, abort_flag, err, dbg.wait_ns))
+                    break;
+                tc::fence_after();
+                bool ok = true;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % kStages;
+                    if (!tc::wait_or_abort(full(s), (it / kStages) & 1, abort_flag, err,
+                                           dbg.wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const int na = atoms_of(kb);
+                    const uint32_t sf = tmem + kTmemSf + (uint32_t)s * kSfColsPerStage;
+                    const uint32_t sa = base_s + kOffSfa + s * kSfaBytes;
+                    const uint32_t sb = base_s + kOffSfb + s * kSfbBytes;
+                    // scale atoms into both CTAs' TMEM: W atom j at columns 4j, x atom j of
+                    // row block 0 / 1 at 16 + 8j / 16 + 8j + 4
+                    for (int j = 0; j < na; ++j) {
+                        tc::cp_atom_pair(sf + 4 * j, tc::atom_desc(sa + j * kAtomBytes));
+                        tc::cp_atom_pair(sf + 16 + 8 * j, tc::atom_desc(sb + j * kAtomBytes));
+                        tc::cp_atom_pair(sf + 16 + 8 * j + 4,
+                                         tc::atom_desc(sb + (4 + j) * kAtomBytes));
+                    }
+                    const uint32_t a_s = base_s + kOffA + s * kABytes;
+                    const uint32_t b_s = base_s + kOffB + s * kBBytes;
+                    for (int j = 0; j < na; ++j)
+                        tc::mma_mxf4nvf4_pair(tmem, tc::sw128_desc(a_s + j * 32),
+                                              tc::sw128_desc(b_s + j * 32), kIdesc, sf + 4 * j,
+                                              sf + 16 + 8 * j, (kb != kb0 || j != 0) ? 1u : 0u);
+                    tc::commit_pair_mc(empty(s), kAll);
+                }
+                if (!ok) break;
+                // (with the test switch on, the accumulator is never marked full: every
+                // epilogue's wait runs out)
+                if (!(dbg.stall && !kQuantX)) tc::commit_pair_mc(accfull, pair_mask);
+            }
+            // MMAs in flight complete before TMEM is freed
+            tc::commit_pair(drain);
+            mbar_wait_bounded(bar_ptr(drain), 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;          // TMEM lane quarter this warp may access
+        const int h = (warp - 2) >> 2;   // x-row half of the tile
+        const float g = *gw * (kQuantX ? gx_in : *gx);
+        const tc::SkUnit u{unit, (int)cr, kCtas};
+        const uint32_t acc_empty = rank == 0 ? accempty : tc::peer_addr(accempty, leader);
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+        int lt = 0;
+        tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk, unit, nunits);
+        int tile, kb0, kb1;
+        for (; wi.next(tile, kb0, kb1); ++lt) {
+            if (!__all_sync(0xffffffffu,
+                            tc::wait_or_abort(accfull, lt & 1, abort_flag, err, dbg.wait_ns)))
+                break;
+            tc::fence_after();
+            if (kb0 == 0 && kb1 == nkb) {
+                const int nb = tile / ntiles_m, mb = tile % ntiles_m;
+                const int64_t n = ((int64_t)nb * kCtas + cr) * 128 + q * 32 + lane;
+                const int64_t m0 = (int64_t)mb * kBM + h * 128;
+                uint32_t v[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tc::tmem_ld32(taddr + h * 128 + c * 32, v[c]);
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::release_acc(acc_empty, u);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (m0 + c * 32 >= M) break;
+                    float f[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[c][j]);
+                    tc::store_rows32(y, y_bf16, M, N, m0 + c * 32, n, f, g);
+                }
+            } else if (h == 1) {
+                __syncwarp();
+                if (lane == 0) tc::release_acc(acc_empty, u);
+            } else {
+                // on the CTA's last item the stage ring is idle: a quarter of it per warp
+                tc::WorkIter peek = wi;
+                int t_, k0_, k1_;
+                uint8_t* stage = peek.next(t_, k0_, k1_) ? nullptr : base + q * kFixupBytes;
+                tc::epilogue_work<128, kBM>(tmem, q, lane, tile, ntiles_m, false, nkb, p_sk, tsk,
+                                            g, y, y_bf16, M, N, slots, counters, acc_empty, stage,
+                                            bar_ptr(fixbar0 + 128u * q), kFixupBufs, u, err);
+            }
+        }
+    }
+
+    tc::fence_before();
+    __syncthreads();
+    tc::cluster_sync();  // no CTA of the cluster exits while another may still address it
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc_pair(tmem, kTmemCols);
+    }
+    if constexpr (kQuantX) {
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(qa.sync + 2, 1u) == gridDim.x - 1) {
+                atomicExch(qa.sync + 3, 0u);
+                atomicExch(qa.sync, 0u);
+                atomicExch(qa.sync + 2, 0u);
+            }
+        }
+    }
+}
+
+// Stream-K state of every W4A4 kernel: counters sized for the two-pair kernel's tiles (four
+// 128-row parts per tile; at least the other kernels' counts), then the largest of the
+// kernels' partial-tile slots.  Every kernel leaves the counters zero.
+size_t counter_region(int64_t M, int64_t N) {
+    return tc::counters_bytes(4 * ((N + 511) / 512) * ((M + 255) / 256));
 }
 
 template <bool kQuantX>
@@ -541,7 +891,7 @@ cudaError_t launch(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M
     if (e != cudaSuccess) return e;
     const int natoms_row = (K + 63) / 64;  // scale atoms per 128-row block
     uint32_t* counters = reinterpret_cast<uint32_t*>(sk_state);
-    float* slots = reinterpret_cast<float*>(sk_state + tc::counters_bytes(p.ntiles));
+    float* slots = reinterpret_cast<float*>(sk_state + counter_region(M, N));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
     cfg.blockDim = dim3(kThreads);
@@ -561,10 +911,141 @@ cudaError_t launch(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// ---- pair kernel host side ----
+
+template <bool kQuantX, int kPairs>
+cudaError_t configure_pair(const DevInfo& dev) {
+    static std::atomic<uint64_t> configured{0};
+    const uint64_t bit = 1ull << (dev.device & 63);
+    if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(gemm_w4a4_pair_kernel<kQuantX, kPairs>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)pairk::kSmemBytes);
+    if (e == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// Clusters of kPairs CTA pairs the device holds at once (one CTA per SM); 0 when it cannot
+// co-schedule them
+template <bool kQuantX, int kPairs>
+int pair_units(const DevInfo& dev) {
+    static std::atomic<int> units[64];  // 0: not queried yet, else units + 1
+    std::atomic<int>& slot = units[dev.device & 63];
+    const int c = slot.load(std::memory_order_acquire);
+    if (c) return c - 1;
+    int n = 0;
+    if (dev.smem_optin >= pairk::kSmemBytes &&
+        configure_pair<kQuantX, kPairs>(dev) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * kPairs);
+        cfg.blockDim = dim3(pairk::kThreads);
+        cfg.dynamicSmemBytes = pairk::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2 * kPairs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_w4a4_pair_kernel<kQuantX, kPairs>, &cfg) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+    }
+    slot.store(n + 1, std::memory_order_release);
+    return n;
+}
+
+template <bool kQuantX, int kPairs>
+cudaError_t launch_pair(int units, const uint8_t* xq, const uint8_t* xsz, const float* gx, int M,
+                        int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
+                        void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
+                        const QxArgs& qa, cudaStream_t stream) {
+    constexpr int kBM = pairk::kBM, kBK = pairk::kBK;
+    constexpr int kThreads = pairk::kThreads;
+    constexpr uint32_t kSmemBytes = pairk::kSmemBytes;
+    const GemmPlan p = tc::make_plan(M, K, N, units, 256 * kPairs, kBM, kBK);
+    const int natoms_row = (K + 63) / 64;
+    CUtensorMap mw, mx, msw, msx;
+    cudaError_t e = tc::make_map_2d(&mw, wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2,
+                                    (uint64_t)N, kBK / 2, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    // x codes: a CTA's 128 rows, or the 64 of them each pair of a two-pair cluster loads
+    e = tc::make_map_2d(&mx, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)M,
+                        kBK / 2, 128 / kPairs, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+    // scale atoms as rows of 128 32-bit words: row (row block * natoms_row + atom); W: the
+    // 4 atoms of a K step, x: 4 (or the 2 each pair loads)
+    e = tc::make_map_2d(&msw, wsz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 128,
+                        (uint64_t)((N + 127) / 128) * natoms_row, 128, 4,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    e = tc::make_map_2d(&msx, xsz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 128,
+                        (uint64_t)((M + 127) / 128) * natoms_row, 128, 4 / kPairs,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    uint32_t* counters = reinterpret_cast<uint32_t*>(sk_state);
+    float* slots = reinterpret_cast<float*>(sk_state + counter_region(M, N));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * kPairs * p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2 * kPairs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = kQuantX ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_w4a4_pair_kernel<kQuantX, kPairs>, mw, mx, msw, msx, gw, gx,
+                           y, y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, p.ntiles_m, p.ntiles,
+                           p.ntiles_sk, p.p_sk, p.tsk, err, counters, slots, qa,
+                           current_wait_cfg());
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// The CTA-pair kernels, where the calling thread asks for them (w4a4_pair_mode: 1 single
+// pairs, 2 clusters of two pairs, else single pairs); *launched stays false for the one-CTA
+// kernel (the default: it is the fastest of the three on this hardware) or when the device
+// cannot hold the clusters
+template <bool kQuantX>
+cudaError_t launch_pair_any(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M, int K,
+                            const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
+                            void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
+                            const QxArgs& qa, cudaStream_t stream, const DevInfo& dev,
+                            bool* launched) {
+    *launched = false;
+    const int mode = w4a4_pair_mode();
+    if (mode == 0) return cudaSuccess;
+    const int u2 = mode == 2 ? pair_units<kQuantX, 2>(dev) : 0;
+    if (u2 > 0) {
+        *launched = true;
+        return launch_pair<kQuantX, 2>(u2, xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16, err,
+                                       sk_state, qa, stream);
+    }
+    const int u1 = pair_units<kQuantX, 1>(dev);
+    if (u1 > 0) {
+        *launched = true;
+        return launch_pair<kQuantX, 1>(u1, xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16, err,
+                                       sk_state, qa, stream);
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 size_t gemm_w4a4_stream_k_bytes(int64_t M, int64_t K, int64_t N) {
-    return tc::stream_k_bytes(M, K, N, kBN, kBM, kBK);
+    size_t slots = 0;
+    for (int bn : {kBN, 256, 512}) {
+        const size_t b = tc::stream_k_bytes(M, K, N, bn, kBM, kBK) -
+                         tc::counters_bytes(((N + bn - 1) / bn) * ((M + kBM - 1) / kBM));
+        if (b > slots) slots = b;
+    }
+    return counter_region(M, N) + slots;
 }
 
 size_t gemm_w4a4_sync_bytes(int64_t) { return 256; }
@@ -573,6 +1054,10 @@ cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float*
                              int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
                              void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
                              cudaStream_t stream, const DevInfo& dev) {
+    bool launched = false;
+    const cudaError_t e = launch_pair_any<false>(xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16,
+                                                 err, sk_state, QxArgs{}, stream, dev, &launched);
+    if (launched) return e;
     return launch<false>(xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16, err, sk_state, QxArgs{},
                          stream, dev);
 }
@@ -591,6 +1076,13 @@ cudaError_t launch_gemm_w4a4_quant_x(const uint16_t* x, const float* gx_static, 
     qa.xq = xq;
     qa.xs = xsz;
     qa.K = K;
+    bool launched = false;
+    const cudaError_t e = launch_pair_any<true>(xq, xsz, gx_out, M, K, wq, wsz, gw, N, y, y_bf16,
+                                                err, sk_state, qa, stream, dev, &launched);
+    // a device that refuses a cooperative launch of CTA clusters (or cannot hold them all)
+    // takes the one-CTA kernel
+    if (launched && e == cudaSuccess) return e;
+    if (launched) cudaGetLastError();
     return launch<true>(xq, xsz, gx_out, M, K, wq, wsz, gw, N, y, y_bf16, err, sk_state, qa,
                         stream, dev);
 }

@@ -150,6 +150,7 @@ int query_device(DevInfo* out) { return (int)current_device(out); }
 
 namespace {
 thread_local bool t_expire_waits = false;
+thread_local int t_w4a4_pair_mode = 0;
 constexpr uint64_t kDebugWaitNs = 200000;  // 200 us
 }  // namespace
 
@@ -161,6 +162,8 @@ WaitCfg current_wait_cfg() {
     }
     return w;
 }
+
+int w4a4_pair_mode() { return t_w4a4_pair_mode; }
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -490,6 +493,10 @@ NVFP4_API nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t
 }
 
 NVFP4_API void nvfp4_debug_expire_waits(int on) { t_expire_waits = on != 0; }
+
+NVFP4_API void nvfp4_debug_w4a4_kernel(int which) {
+    t_w4a4_pair_mode = which == 2 ? 1 : which == 3 ? 2 : 0;
+}
 
 NVFP4_API const char* nvfp4_last_cuda_error(void) {
     return cudaGetErrorString(t_last_cuda_error);

@@ -136,6 +136,112 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
+// ---- CTA pairs (cta_group::2) ---------------------------------------------------------------
+// A pair is a cluster of two CTAs.  TMEM is allocated by one warp in each CTA together (the
+// same columns in both).  The even CTA issues M = 256 MMAs: A rows 0..127 come from its
+// shared memory and 128..255 from its peer's (same offset), B's N rows are split the same
+// way, and each CTA's TMEM receives its own 128 rows of D.  Scale atoms reach both CTAs'
+// TMEM by tcgen05.cp from the same thread, ahead of the MMAs that read them.  TMA loads of
+// either CTA land in the issuing CTA's shared memory and complete on the even CTA's
+// barrier.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// every thread of both CTAs of the cluster
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+
+// the shared::cluster address of this CTA's shared address `saddr` in CTA `rank`
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// TMA tile load into this CTA's shared memory, completing on the mbarrier at shared::cluster
+// address cbar (the even CTA's)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0,
+                                                 int c1, uint32_t cbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(cbar)
+        : "memory");
+}
+
+// The same load issued for several CTAs of the cluster (ctaMask): the box lands at the
+// same shared-memory offset in each, and each completes on the mbarrier at the same offset
+// in its own pair's even CTA (cbar: that barrier in the issuing CTA's pair)
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, int c0,
+                                                    int c1, uint32_t cbar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster.cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(cbar), "h"(mask)
+        : "memory");
+}
+
+// one 512-byte scale atom (32 rows of 16 bytes) from each CTA's shared memory into its own
+// TMEM: atom row i to lane 32 q + i of every lane quarter q, four columns
+__device__ __forceinline__ uint64_t atom_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128 >> 4) << 16;     // leading byte offset
+    d |= (uint64_t)(128 >> 4) << 32;     // stride byte offset
+    d |= (uint64_t)1 << 46;              // descriptor version
+    return d;
+}
+__device__ __forceinline__ void cp_atom_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// block-scaled pair MMA, E2M1 operands, UE4M3 scales per 16 elements, fp32 accumulate
+__device__ __forceinline__ void mma_mxf4nvf4_pair(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                                  uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// arrive (once) on the mbarrier at shared::cluster address cbar (this CTA's or the peer's)
+// when every pair operation this thread issued so far completes
+__device__ __forceinline__ void commit_pair(uint32_t cbar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(cbar)
+        : "memory");
+}
+
+// arrive (once) on the mbarrier at shared offset `bar` in every CTA of ctaMask when every
+// pair operation this thread issued so far completes
+__device__ __forceinline__ void commit_pair_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
+        : "memory");
+}
+
 // ---- bounded waits -----------------------------------------------------------------------
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -152,6 +258,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 
 __device__ __forceinline__ void arrive(uint32_t bar) {
     mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bar)));
+}
+
+// arrive on an mbarrier by its shared::cluster address (this CTA's or its peer's)
+__device__ __forceinline__ void arrive_cluster(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
 // ---- persistent work split ---------------------------------------------------------------
@@ -181,10 +292,10 @@ struct WorkIter {
     }
 };
 
+// The work of unit c of nunits: a CTA (c = blockIdx.x), or a CTA pair sharing its tiles.
 __device__ __forceinline__ WorkIter make_iter(int ntiles, int nkb, int ntiles_sk, int p_sk,
-                                              int64_t tsk) {
+                                              int64_t tsk, int c, int nunits) {
     WorkIter w;
-    const int c = blockIdx.x;
     if (c < p_sk) {
         w.i = (int64_t)c * tsk / p_sk;
         w.i_end = (int64_t)(c + 1) * tsk / p_sk;
@@ -194,12 +305,18 @@ __device__ __forceinline__ WorkIter make_iter(int ntiles, int nkb, int ntiles_sk
     w.dp = ntiles_sk + c;
     w.ntiles = ntiles;
     w.nkb = nkb;
-    w.stride = gridDim.x;
+    w.stride = nunits;
     return w;
 }
 
-// stream-K bookkeeping: the CTA whose range holds iteration i, and the slot CTA c uses for
-// its partial of the tile starting at iteration t0 (2c: its first segment, 2c + 1: its last)
+__device__ __forceinline__ WorkIter make_iter(int ntiles, int nkb, int ntiles_sk, int p_sk,
+                                              int64_t tsk) {
+    return make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk, blockIdx.x, gridDim.x);
+}
+
+// stream-K bookkeeping: the unit whose range holds iteration i, and the slot unit c uses
+// for its partial of the tile starting at iteration t0 (2c: its first segment, 2c + 1: its
+// last; a unit of two CTAs has a pair of slots per segment, one per CTA half)
 __device__ __forceinline__ int sk_cta_of(int64_t i, int p_sk, int64_t tsk) {
     return (int)(((i + 1) * p_sk - 1) / tsk);
 }
@@ -241,6 +358,26 @@ __device__ __forceinline__ void store_rows32(void* y, int y_bf16, int64_t M, int
     }
 }
 
+// Where a CTA's stream-K state lives: its unit (the CTA itself, or the cluster of CTA
+// pairs whose CTAs hold the nhalves 128-row parts of every tile's W rows), and which part
+// it holds.  Unit c's partial of a tile goes to slot (sk_slot(c, ...) * nhalves + half);
+// the tile's counters are (tile * nhalves + half) * 4 + quarter.
+struct SkUnit {
+    int me = 0;
+    int half = 0;
+    int nhalves = 1;
+};
+
+// Release of an accumulator to the MMA issuer: a plain arrive in a one-CTA unit; from a
+// pair's odd CTA an arrive on its even CTA's barrier (its TMEM reads, ordered by the
+// caller's tcgen05 fence, come before the issuer's next MMAs into it)
+__device__ __forceinline__ void release_acc(uint32_t accempty, const SkUnit& u) {
+    if (u.nhalves >= 2 && (u.half & 1))
+        arrive_cluster(accempty);
+    else
+        arrive(accempty);
+}
+
 // How long the first segment of a stream-K tile waits, on its CTA's last item, for the
 // tile's other segments before it writes its own partial like them
 constexpr uint64_t kOwnerWaitNs = 20000;
@@ -264,9 +401,10 @@ __device__ __forceinline__ void fixup_staged(uint32_t taddr, bool own_tmem, int 
                                              int mb, int cf, int cl, int64_t t0, int p_sk,
                                              int64_t tsk, const float* slots, uint8_t* stage,
                                              uint64_t* bars, int nbuf, float scale, void* y,
-                                             int y_bf16, int M, int N, int64_t n, uint32_t* err) {
+                                             int y_bf16, int M, int N, int64_t n, SkUnit u,
+                                             uint32_t* err) {
     constexpr size_t kSlotFloats = (size_t)BN * BM;
-    const int me = blockIdx.x;
+    const int me = u.me;
     const int64_t rows_left = (int64_t)M - (int64_t)mb * BM;
     const int nrow = rows_left >= BM ? BM / 32 : (int)((rows_left + 31) / 32);
     const int nother = cl - cf + 1 - (own_tmem ? 1 : 0);
@@ -275,9 +413,11 @@ __device__ __forceinline__ void fixup_staged(uint32_t taddr, bool own_tmem, int 
     // this quarter's part of segment cs's slot: the tile's first segment may be its CTA's
     // second slot; every later segment starts its CTA's range (the first slot)
     const float* q_base = slots + (size_t)q * BM * 32;
-    const float* first_seg = q_base + (size_t)sk_slot(cf, t0, p_sk, tsk) * kSlotFloats;
+    const float* first_seg =
+        q_base + ((size_t)sk_slot(cf, t0, p_sk, tsk) * u.nhalves + u.half) * kSlotFloats;
     auto seg_src = [&](int cs) {
-        return cs == cf ? first_seg : q_base + (size_t)(2 * cs) * kSlotFloats;
+        return cs == cf ? first_seg
+                        : q_base + ((size_t)(2 * cs) * u.nhalves + u.half) * kSlotFloats;
     };
     // the chunk stream, in the order it is read: x rows 32 ci .. of every other segment
     int is_ci = 0, is_cs = (own_tmem && cf == me) ? cf + 1 : cf, is_b = 0, issued = 0;
@@ -359,7 +499,10 @@ __device__ __forceinline__ void fixup_staged(uint32_t taddr, bool own_tmem, int 
 }
 
 // One work item's epilogue for one epilogue warp: TMEM lane quarter q holds W rows
-// q*32 .. q*32+31 of the tile, columns 0 .. BM-1 the tile's x rows.  A whole tile goes to y.
+// q*32 .. q*32+31 of the CTA's BN rows of the tile (the half u.half of a pair's 2 BN rows),
+// columns 0 .. BM-1 the tile's x rows.  `accempty` is the mbarrier that releases the
+// accumulator: this CTA's, or for a pair's odd CTA the even CTA's (a shared::cluster
+// address).  A whole tile goes to y.
 // A stream-K segment goes to this CTA's fp32 slot, and the arrival that completes the
 // quarter's count (one counter per tile quarter, wrapping back to zero) adds the quarter's
 // partials in segment order and writes y.  On the CTA's last work item (`stage` not null:
@@ -375,12 +518,13 @@ __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int
                                               int64_t tsk, float scale, void* y, int y_bf16,
                                               int M, int N, float* slots, uint32_t* counters,
                                               uint32_t accempty, uint8_t* stage,
-                                              uint64_t* fixbars, int nbuf, uint32_t* err) {
+                                              uint64_t* fixbars, int nbuf, SkUnit u,
+                                              uint32_t* err) {
     static_assert(BN == 128, "four lane quarters of 32 W rows");
     constexpr size_t kSlotFloats = (size_t)BN * BM;
     const int nb = tile / ntiles_m, mb = tile % ntiles_m;
     const int nl = q * 32 + lane;
-    const int64_t n = (int64_t)nb * BN + nl;
+    const int64_t n = ((int64_t)nb * u.nhalves + u.half) * BN + nl;
     const uint32_t taddr = acc + ((uint32_t)(q * 32) << 16);
     const int64_t t0 = (int64_t)tile * nkb;
     int cf = 0, cl = 0;
@@ -392,13 +536,13 @@ __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int
         if (stage) {
             unsigned seen = 0;
             if (lane == 0) {
-                const uint32_t* cnt = &counters[tile * 4 + q];
+                const uint32_t* cnt = &counters[(tile * u.nhalves + u.half) * 4 + q];
                 seen = ld_acquire_gpu(cnt);
                 // The tile's first segment waits a little for the others to be counted
                 // rather than writing its own slot: on a CTA's last item the others end at
                 // about the same time (the stream-K ranges are balanced).  The wait is
                 // bounded; when it runs out the segment takes the ordinary path below.
-                if (seen != nseg - 1 && (int)blockIdx.x == cf) {
+                if (seen != nseg - 1 && u.me == cf) {
                     const uint64_t w0 = globaltimer_ns();
                     while (seen != nseg - 1 && globaltimer_ns() - w0 < kOwnerWaitNs) {
                         __nanosleep(64);
@@ -409,18 +553,19 @@ __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int
             if (__shfl_sync(0xffffffffu, seen, 0) == nseg - 1) {
                 // every other partial is in its slot; the count goes back to zero for the
                 // next call (no other segment touches it again)
-                if (lane == 0) counters[tile * 4 + q] = 0u;
+                if (lane == 0) counters[(tile * u.nhalves + u.half) * 4 + q] = 0u;
                 fixup_staged<BN, BM>(taddr, true, q, lane, mb, cf, cl, t0, p_sk, tsk, slots,
-                                     stage, fixbars, nbuf, scale, y, y_bf16, M, N, n, err);
+                                     stage, fixbars, nbuf, scale, y, y_bf16, M, N, n, u, err);
                 fence_before();
                 __syncwarp();
-                if (lane == 0) arrive(accempty);
+                if (lane == 0) release_acc(accempty, u);
                 return;
             }
         }
     }
     float* mine = whole ? nullptr
-                        : slots + (size_t)sk_slot(blockIdx.x, t0, p_sk, tsk) * kSlotFloats +
+                        : slots + ((size_t)sk_slot(u.me, t0, p_sk, tsk) * u.nhalves + u.half) *
+                                      kSlotFloats +
                               slot_chunk<BM>(q, 0) + lane;
 #pragma unroll 1
     for (int c0 = 0; c0 < BM; c0 += 32) {
@@ -438,17 +583,17 @@ __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int
     }
     fence_before();
     __syncwarp();
-    if (lane == 0) arrive(accempty);
+    if (lane == 0) release_acc(accempty, u);
     if (whole) return;
     __threadfence();
     __syncwarp();
     unsigned old = 0;
-    if (lane == 0) old = atomicInc(&counters[tile * 4 + q], nseg - 1);
+    if (lane == 0) old = atomicInc(&counters[(tile * u.nhalves + u.half) * 4 + q], nseg - 1);
     if (__shfl_sync(0xffffffffu, old, 0) != nseg - 1) return;
     __threadfence();
     if (stage) {
         fixup_staged<BN, BM>(taddr, false, q, lane, mb, cf, cl, t0, p_sk, tsk, slots, stage,
-                             fixbars, nbuf, scale, y, y_bf16, M, N, n, err);
+                             fixbars, nbuf, scale, y, y_bf16, M, N, n, u, err);
         return;
     }
     // 32 rows of the quarter at a time, every partial's 32 loads in flight together; the
@@ -462,7 +607,8 @@ __device__ __forceinline__ void epilogue_work(uint32_t acc, int q, int lane, int
         for (int j = 0; j < 32; ++j) accv[j] = 0.0f;
 #pragma unroll 1
         for (int cs = cf; cs <= cl; ++cs) {
-            const float* sp = slots + (size_t)sk_slot(cs, t0, p_sk, tsk) * kSlotFloats +
+            const float* sp = slots + ((size_t)sk_slot(cs, t0, p_sk, tsk) * u.nhalves + u.half) *
+                                          kSlotFloats +
                               slot_chunk<BM>(q, c0) + lane;
             float v[32];
 #pragma unroll

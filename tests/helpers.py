@@ -1,4 +1,6 @@
 """Shared test helpers: moving oracle outputs to the device and the linear tolerance."""
+import contextlib
+
 import numpy as np
 import torch
 
@@ -68,3 +70,15 @@ def upload_weights(wq: np.ndarray, ws: np.ndarray, gw: float, K: int):
     nv.nvfp4_repack(d_ws, K, d_swz)
     d_g = torch.tensor([gw], dtype=torch.float32, device="cuda")
     return d_wq, d_swz, d_g
+
+
+@contextlib.contextmanager
+def w4a4_kernel(which: str):
+    """Run the W4A4 GEMM (M > 16) on the given kernel: "auto" (the one-CTA kernel),
+    "one_cta", "pair" or "pair2"."""
+    import nvfp4_weight_quantized_quantize_gb300 as nv
+    nv.nvfp4_debug_w4a4_kernel(which)
+    try:
+        yield
+    finally:
+        nv.nvfp4_debug_w4a4_kernel("auto")

@@ -13,7 +13,7 @@ import torch
 
 import nvfp4_weight_quantized_quantize_gb300 as nv
 import oracle
-from helpers import to_dev, upload_weights
+from helpers import to_dev, upload_weights, w4a4_kernel
 from synth import make_inputs, random_gate_up, random_nvfp4_weights, random_x
 
 pytestmark = pytest.mark.gpu
@@ -55,9 +55,13 @@ def guarded(shape, dtype):
     (3, 5152, 1001, "w4a16"), (8, 2080, 129, "w4a16"), (5, 17440, 301, "w4a16"),
     (13, 1056, 257, "w4a16"), (16, 17408, 199, "w4a16"), (17, 1056, 300, "w4a16"),
     (300, 2080, 257, "w4a16"), (40, 1056, 129, "w4a4"), (300, 5152, 641, "w4a4"),
-    (3, 1056, 77, "w4a4"), (12, 2080, 300, "w4a4"),
+    (3, 1056, 77, "w4a4"), (12, 2080, 300, "w4a4"), (300, 5152, 641, "w4a4-pair2"),
+    (40, 1056, 129, "w4a4-pair2"), (520, 2080, 1300, "w4a4"), (300, 5152, 641, "w4a4-pair"),
+    (520, 2080, 1300, "w4a4-pair"), (700, 1056, 1500, "w4a4"),
 ])
 def test_linear_writes_only_its_outputs(M, K, N, mode):
+    kernel = mode.split("-")[1] if "-" in mode else "auto"
+    mode = mode.split("-")[0]
     x = random_x(M, K, seed=M * 7 + K)
     wq, ws, gw = random_nvfp4_weights(N, K, seed=N)
     d_wq, d_swz, d_g = upload_weights(wq, ws, gw, K)
@@ -68,8 +72,9 @@ def test_linear_writes_only_its_outputs(M, K, N, mode):
     wsb = nv.nvfp4_workspace_bytes(1, M, K, N, m)
     gw_, work = guarded((wsb,), torch.uint8)
     work.zero_()
-    nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, mode=mode, workspace=work,
-                    static_weights=(N % 2 == 1))
+    with w4a4_kernel(kernel):
+        nv.nvfp4_linear(d_x, d_wq, d_swz, d_g, y, mode=mode, workspace=work,
+                        static_weights=(N % 2 == 1))
     torch.cuda.synchronize()
     assert nv.nvfp4_workspace_error(work) == 0
     gy.check("y")

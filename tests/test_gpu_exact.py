@@ -26,7 +26,8 @@ once, so the kernel's fp32 y must equal the oracle's fp64 result rounded to fp32
          (K / 32 < 64);
   2 <= M <= 8: the skinny kernel, and the mma.sync kernel where K exceeds its ring;
   9 <= M <= 16: two skinny passes, and the mma.sync kernel at large K;
-  M > 16: the tcgen05 W4A16 GEMM (with stream-K tails) and the block-scaled W4A4 GEMM;
+  M > 16: the tcgen05 W4A16 GEMM (with stream-K tails) and the block-scaled W4A4 GEMM
+         (the one-CTA kernel, and the CTA-pair kernels);
   W4A4 at small M (pre-pass, and the static-scale fused kernels), and the linear on
   NVFP4 activations.
 """
@@ -36,7 +37,7 @@ import torch
 
 import nvfp4_weight_quantized_quantize_gb300 as nv
 import oracle
-from helpers import to_dev, upload_weights
+from helpers import to_dev, upload_weights, w4a4_kernel
 from synth import sparse_block_x, structured_nvfp4_weights
 
 pytestmark = pytest.mark.gpu
@@ -144,6 +145,8 @@ def test_w4a16_gemm_exact_sampled(M, K, N):
     (40, 5120, 1000, None),       # block-scaled tcgen05 GEMM
     (200, 17408, 600, None),
     (64, 5120, 640, 2.0 ** -5),
+    (300, 2080, 777, None),       # CTA-pair tiles: ragged M and N, partial scale atoms
+    (520, 2048, 2304, None),      # three x tiles of the pair kernel, all stream-K
 ])
 def test_w4a4_exact(M, K, N, gx):
     x = sparse_block_x(M, K, seed=3 * M + K)
@@ -155,9 +158,28 @@ def test_w4a4_exact(M, K, N, gx):
                       "w4a4 M%d K%d N%d" % (M, K, N))
 
 
-@pytest.mark.parametrize("M,K,N", [(1, 5120, 2000), (7, 5120, 900), (16, 2048, 300),
-                                   (100, 17408, 640)])
-def test_linear_nvfp4_x_exact(M, K, N):
+@pytest.mark.parametrize("M,K,N", [(40, 5120, 1000), (200, 17408, 600), (64, 5120, 640),
+                                   (300, 2080, 777)])
+@pytest.mark.parametrize("gx", [None, 2.0 ** -5], ids=["dyn", "static"])
+@pytest.mark.parametrize("kernel", ["pair", "pair2"])
+def test_w4a4_exact_pair_kernels(M, K, N, gx, kernel):
+    # the CTA-pair block-scaled kernels: single pairs, and clusters of two pairs that share
+    # the x tile by multicast
+    x = sparse_block_x(M, K, seed=3 * M + K)
+    wq, ws, gw = structured_nvfp4_weights(N, K, seed=5 * N + K)
+    with w4a4_kernel(kernel):
+        y = linear(x, wq, ws, gw, K, torch.float32, mode="w4a4", gx=gx)
+    y_ref, _, _, _, gxo = oracle.linear_w4a4(x, wq, ws, gw, gx)
+    assert_bits_equal(y, expected_bits(y_ref, torch.float32, np.float64(gxo) * gw),
+                      "w4a4 %s M%d K%d N%d" % (kernel, M, K, N))
+
+
+@pytest.mark.parametrize("M,K,N,kernel", [(1, 5120, 2000, "auto"), (7, 5120, 900, "auto"),
+                                          (16, 2048, 300, "auto"), (100, 17408, 640, "auto"),
+                                          (100, 17408, 640, "pair2"), (300, 1056, 300, "auto"),
+                                          (300, 1056, 300, "pair2"), (300, 1056, 300, "pair"),
+                                          (600, 2048, 1100, "pair2")])
+def test_linear_nvfp4_x_exact(M, K, N, kernel):
     x = sparse_block_x(M, K, seed=11 * M + K)
     xq, xs, gx = oracle.quantize(x)
     wq, ws, gw = structured_nvfp4_weights(N, K, seed=13 * N + K)
@@ -166,8 +188,9 @@ def test_linear_nvfp4_x_exact(M, K, N):
     y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
     work = torch.zeros(nv.nvfp4_workspace_bytes(1, M, K, N, nv.NVFP4_W4A4), dtype=torch.uint8,
                        device="cuda")
-    nv.nvfp4_linear_nvfp4_x(to_dev(xq), d_xs, torch.tensor([gx], device="cuda"), d_wq, d_swz,
-                            d_g, y, work)
+    with w4a4_kernel(kernel):
+        nv.nvfp4_linear_nvfp4_x(to_dev(xq), d_xs, torch.tensor([gx], device="cuda"), d_wq,
+                                d_swz, d_g, y, work)
     torch.cuda.synchronize()
     assert nv.nvfp4_workspace_error(work) == 0
     y_ref = oracle_pairs_all(oracle.linear_w4a4_pairs, M, N, xq, xs, gx, wq, ws, gw)
