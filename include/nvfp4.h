@@ -399,12 +399,11 @@ void nvfp4_debug_expire_waits(int on);
 
 /* Test switch; never set in production.  Chooses, for calls from the calling thread, the
  * kernel of the W4A4 GEMM at M > 16 (nvfp4_linear in W4A4 mode, nvfp4_linear_nvfp4_x):
- * 0 or 1 the one-CTA tensor-core kernel (the default, the fastest on this hardware); 2
- * CTA pairs on two SMs (tcgen05 cta_group::2, 256 x 256 tiles); 3 clusters of two CTA pairs
- * that share the x tile by TMA multicast (512 x 256 tiles).  A device that cannot hold the
- * chosen clusters runs the one-CTA kernel.  Every kernel satisfies the same tolerance;
- * their stream-K splits differ, so outputs can differ in the last bits where a tile's K
- * steps are summed in different groups.  Host-only; the switch is per thread. */
+ * 0 or 1 the one-CTA tensor-core kernel (the default, the faster on this hardware); 2 CTA
+ * pairs on two SMs (tcgen05 cta_group::2, 256 x 256 tiles; a device that cannot co-schedule
+ * CTA pairs runs the one-CTA kernel).  Both satisfy the same tolerance; their stream-K
+ * splits differ, so outputs can differ in the last bits where a tile's K steps are summed
+ * in different groups.  Host-only; the switch is per thread. */
 void nvfp4_debug_w4a4_kernel(int which);
 
 /*

@@ -525,37 +525,32 @@ gemm_w4a4_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
 // ---- CTA-pair kernel ---------------------------------------------------------------------
 //
-// A cluster of kPairs CTA pairs (two SMs each) computes a (kPairs x 256) (W) x 256 (x) tile
-// with M = 256 block-scaled MMAs (tcgen05.mma.cta_group::2): in each pair the even CTA
-// issues the MMAs, the MMA's A is split by rows across the pair's two CTAs and B by N.  CTA
-// (pair p, rank r) holds W rows (4 nb + 2 p + r) x 128 .. +128 of the cluster tile nb and
-// half r of the tile's x rows; per K step of 256 it takes in 38 KB: 16 KB of W codes, 16 KB
-// of x codes, 2 KB of W scale atoms and the 4 KB of scale atoms of all 256 x rows, which
-// every CTA's TMEM must hold.  The one-CTA kernel takes in 54 KB for the same MMA work.
-// With two pairs per cluster (kPairs = 2) the pairs share the x tile: the x codes and the
-// x scale atoms each CTA needs are loaded once for the cluster and multicast, so the
-// cluster reads 30 KB per CTA and K step from L2 rather than 38.
+// A pair of CTAs on two SMs computes a 256 (W) x 256 (x) tile with M = 256 block-scaled
+// MMAs (tcgen05.mma.cta_group::2): the even CTA issues the MMAs, the MMA's A is split by
+// rows across the two CTAs and B by N.  CTA rank r holds W rows (2 nb + r) x 128 .. +128 of
+// tile nb and half r of the tile's x rows; per K step of 256 it takes in 38 KB: 16 KB of W
+// codes, 16 KB of x codes, 2 KB of W scale atoms and the 4 KB of scale atoms of all 256 x
+// rows, which both CTAs' TMEM must hold.  The one-CTA kernel takes in 54 KB for the same
+// MMA work.
 //
-// Every copy is a TMA load that lands in shared memory at the same offset in each CTA it
-// is for and completes on the stage barrier of that CTA's pair's even CTA, which expects
-// both CTAs' bytes.  One thread of each even CTA moves the stage's scale atoms from both
-// CTAs' shared memory into their TMEM (tcgen05.cp.cta_group::2, in order ahead of the MMAs
-// that read them) and issues the four MMAs; its commit releases the stage in every CTA of
-// the cluster (each stage barrier counts one release per pair, since every CTA's stage
-// receives bytes that CTAs of both pairs load).  Each CTA's TMEM holds the fp32
+// Every copy is a TMA load that lands in the issuing CTA's shared memory and completes on
+// the even CTA's stage barrier, which expects both CTAs' bytes.  One thread of the even CTA
+// moves the stage's scale atoms from both CTAs' shared memory into their TMEM
+// (tcgen05.cp.cta_group::2, in order ahead of the MMAs that read them) and issues the four
+// MMAs; its commits release the stage in both CTAs.  Each CTA's TMEM holds the fp32
 // accumulator of its own 128 W rows x the tile's 256 x rows (columns 0..255) and the
 // scales of the stages in flight.
 //
 // Warp roles per CTA:
-//   warp 0      TMA producer (every CTA; all wait on their own stage barriers, which the
-//               even CTAs' MMA commits release together);
-//   warp 1      TMEM allocation (both CTAs of a pair together), MMA issue (even CTAs);
+//   warp 0      TMA producer (both CTAs, in step: both wait on their own stage barriers,
+//               which the even CTA's MMA commits release together);
+//   warp 1      TMEM allocation (both CTAs together), MMA issue (even CTA);
 //   warps 2-9   epilogue: lane quarter (warp & 3), x-row half (warp - 2) / 4.  A whole tile
 //               is read out of TMEM into registers (128 columns per warp) and the
 //               accumulator released before the stores, so the next tile's MMAs overlap
 //               them; a stream-K segment is written by the first half's warps (the
-//               shared stream-K epilogue, per 128-row part of the tile), the second
-//               half's warps release at once.
+//               shared stream-K epilogue, per CTA half), the second half's warps release
+//               at once.
 namespace pairk {
 
 constexpr int kBM = 256;   // x rows per tile (MMA N), 128 loaded by each CTA of a pair
@@ -594,7 +589,7 @@ constexpr uint64_t kDrainNs = 1000000;
 
 }  // namespace pairk
 
-template <bool kQuantX, int kPairs>
+template <bool kQuantX>
 __global__ void __launch_bounds__(pairk::kThreads, 1)
 gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
                       const __grid_constant__ CUtensorMap tmap_x,
@@ -618,18 +613,16 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
     constexpr uint32_t kOffMisc = pairk::kOffMisc, kFixBars = pairk::kFixBars;
     constexpr uint32_t kFixupBytes = pairk::kFixupBytes, kIdesc = pairk::kIdesc;
     constexpr uint64_t kDrainNs = pairk::kDrainNs;
-    constexpr int kCtas = 2 * kPairs;                        // CTAs per cluster
-    constexpr uint16_t kAll = (uint16_t)((1u << kCtas) - 1);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_s - raw_s);
     const uint32_t bar0 = base_s + kOffBar;
-    auto full = [&](int s) { return bar0 + 8u * s; };              // even CTAs' are used
+    auto full = [&](int s) { return bar0 + 8u * s; };              // even CTA's is used
     auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
     const uint32_t accfull = bar0 + 8u * (2 * kStages);
-    const uint32_t accempty = bar0 + 8u * (2 * kStages + 1);      // even CTAs' are used
+    const uint32_t accempty = bar0 + 8u * (2 * kStages + 1);      // even CTA's is used
     const uint32_t drain = bar0 + 8u * (2 * kStages + 2);
     const uint32_t fixbar0 = bar0 + 8u * (2 * kStages + 3);
     auto bar_ptr = [&](uint32_t a) { return reinterpret_cast<uint64_t*>(base + (a - base_s)); };
@@ -637,16 +630,12 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t cr = tc::cluster_rank();            // rank in the cluster
-    const uint32_t rank = cr & 1u;                     // rank in the pair
-    const uint32_t leader = cr & ~1u;                  // the pair's even CTA
-    const int pp = (int)(cr >> 1);                     // the pair in the cluster
-    const uint16_t pair_mask = (uint16_t)(3u << leader);
-    const int unit = (int)(blockIdx.x / kCtas), nunits = (int)(gridDim.x / kCtas);
+    const uint32_t rank = tc::cluster_rank();
+    const int unit = (int)(blockIdx.x >> 1), nunits = (int)(gridDim.x >> 1);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_ptr(full(s)), 1);
-            mbar_init(bar_ptr(empty(s)), kPairs);  // one release from each pair's issuer
+            mbar_init(bar_ptr(empty(s)), 1);
         }
         mbar_init(bar_ptr(accfull), 1);
         mbar_init(bar_ptr(accempty), 16);  // 8 epilogue warps in each CTA of the pair
@@ -657,7 +646,7 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
     if (warp == 1) tc::tmem_alloc_pair(base_s + kOffMisc, kTmemCols);
     tc::fence_before();
-    tc::cluster_sync();  // every CTA's barriers initialised, TMEM allocated
+    tc::cluster_sync();  // both CTAs' barriers initialised, TMEM allocated
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -681,14 +670,14 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
             }
             while (!*abort_flag && wi.next(tile, kb0, kb1)) {
                 const int nb = tile / ntiles_m, mb = tile % ntiles_m;
-                const int wrb = (int)(nb * kCtas + cr);  // this CTA's 128-row block of W
+                const int wrb = 2 * nb + (int)rank;  // this CTA's 128-row block of W
                 for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const int s = it % kStages;
                     if (it >= kStages &&
                         !tc::wait_or_abort(empty(s), ((it / kStages) - 1) & 1, abort_flag, err,
                                            dbg.wait_ns))
                         break;
-                    const uint32_t fb = tc::peer_addr(full(s), leader);
+                    const uint32_t fb = tc::peer_addr(full(s), 0);
                     if (rank == 0) mbar_arrive_expect_tx(bar_ptr(full(s)), 2 * kStageBytes);
                     tc::tma_load_2d_pair(base_s + kOffA + s * kABytes, &tmap_w, kb * (kBK / 2),
                                          wrb * 128, fb);
@@ -698,33 +687,17 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
                     // both 128-row blocks, 4 per block (atoms past K or past the tensor's rows
                     // read as zero or as a neighbour's, which no MMA reads or whose outputs
                     // are masked)
-                    const uint32_t b_dst = base_s + kOffB + s * kBBytes;
                     const uint32_t sb_dst = base_s + kOffSfb + s * kSfbBytes;
-                    if constexpr (kPairs == 1) {
-                        tc::tma_load_2d_pair(b_dst, &tmap_x, kb * (kBK / 2),
-                                             mb * kBM + (int)rank * 128, fb);
-                        tc::tma_load_2d_pair(sb_dst, &tmap_sx, 0, (2 * mb) * natoms_row + 4 * kb,
-                                             fb);
-                        tc::tma_load_2d_pair(sb_dst + 4 * kAtomBytes, &tmap_sx, 0,
-                                             (2 * mb + 1) * natoms_row + 4 * kb, fb);
-                    } else {
-                        // shared by the two pairs: pair pp loads 64 of the 128 x rows for the
-                        // CTAs of rank `rank` in both pairs, and 2 of the 4 atoms of x row
-                        // block `rank` for every CTA
-                        const uint16_t same_rank = (uint16_t)((1u << rank) | (1u << (2 + rank)));
-                        tc::tma_load_2d_pair_mc(b_dst + pp * (kBBytes / 2), &tmap_x,
-                                                kb * (kBK / 2), mb * kBM + (int)rank * 128 + pp * 64,
-                                                fb, same_rank);
-                        tc::tma_load_2d_pair_mc(sb_dst + rank * 4 * kAtomBytes + pp * 2 * kAtomBytes,
-                                                &tmap_sx, 0,
-                                                (2 * mb + (int)rank) * natoms_row + 4 * kb + 2 * pp,
-                                                fb, kAll);
-                    }
+                    tc::tma_load_2d_pair(base_s + kOffB + s * kBBytes, &tmap_x, kb * (kBK / 2),
+                                         mb * kBM + (int)rank * 128, fb);
+                    tc::tma_load_2d_pair(sb_dst, &tmap_sx, 0, (2 * mb) * natoms_row + 4 * kb, fb);
+                    tc::tma_load_2d_pair(sb_dst + 4 * kAtomBytes, &tmap_sx, 0,
+                                         (2 * mb + 1) * natoms_row + 4 * kb, fb);
                     issued = it + 1;
                 }
             }
-            // Before the CTA moves on to exit, the copies it issued have landed: an even
-            // CTA sees its stage barriers complete, an odd CTA sees its stages released
+            // Before the CTA moves on to exit, the copies it issued have landed: the even
+            // CTA sees its stage barriers complete, the odd CTA sees its stages released
             // (consumed); after an abort neither may come, and the wait ends after kDrainNs,
             // far longer than a copy takes.
             const uint64_t t0 = globaltimer_ns();
@@ -737,7 +710,7 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------- MMA issue (even CTAs) ----------------
+        // ---------------- MMA issue (even CTA) ----------------
         if (rank == 0 && lane == 0) {
             int it = 0, lt = 0;
             tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk, unit, nunits);
@@ -774,12 +747,16 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         tc::mma_mxf4nvf4_pair(tmem, tc::sw128_desc(a_s + j * 32),
                                               tc::sw128_desc(b_s + j * 32), kIdesc, sf + 4 * j,
                                               sf + 16 + 8 * j, (kb != kb0 || j != 0) ? 1u : 0u);
-                    tc::commit_pair_mc(empty(s), kAll);
+                    tc::commit_pair(empty(s));
+                    tc::commit_pair(tc::peer_addr(empty(s), 1));
                 }
                 if (!ok) break;
                 // (with the test switch on, the accumulator is never marked full: every
                 // epilogue's wait runs out)
-                if (!(dbg.stall && !kQuantX)) tc::commit_pair_mc(accfull, pair_mask);
+                if (!(dbg.stall && !kQuantX)) {
+                    tc::commit_pair(accfull);
+                    tc::commit_pair(tc::peer_addr(accfull, 1));
+                }
             }
             // MMAs in flight complete before TMEM is freed
             tc::commit_pair(drain);
@@ -791,8 +768,8 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
         const int q = warp & 3;          // TMEM lane quarter this warp may access
         const int h = (warp - 2) >> 2;   // x-row half of the tile
         const float g = *gw * (kQuantX ? gx_in : *gx);
-        const tc::SkUnit u{unit, (int)cr, kCtas};
-        const uint32_t acc_empty = rank == 0 ? accempty : tc::peer_addr(accempty, leader);
+        const tc::SkUnit u{unit, (int)rank, 2};
+        const uint32_t acc_empty = rank == 0 ? accempty : tc::peer_addr(accempty, 0);
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
         int lt = 0;
         tc::WorkIter wi = tc::make_iter(ntiles, nkb, ntiles_sk, p_sk, tsk, unit, nunits);
@@ -804,7 +781,7 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
             tc::fence_after();
             if (kb0 == 0 && kb1 == nkb) {
                 const int nb = tile / ntiles_m, mb = tile % ntiles_m;
-                const int64_t n = ((int64_t)nb * kCtas + cr) * 128 + q * 32 + lane;
+                const int64_t n = ((int64_t)nb * 2 + rank) * 128 + q * 32 + lane;
                 const int64_t m0 = (int64_t)mb * kBM + h * 128;
                 uint32_t v[4][32];
 #pragma unroll
@@ -837,7 +814,7 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
 
     tc::fence_before();
     __syncthreads();
-    tc::cluster_sync();  // no CTA of the cluster exits while another may still address it
+    tc::cluster_sync();  // no CTA of the pair exits while the other may still address it
     if (warp == 1) {
         tc::fence_after();
         tc::tmem_dealloc_pair(tmem, kTmemCols);
@@ -854,11 +831,11 @@ gemm_w4a4_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
     }
 }
 
-// Stream-K state of every W4A4 kernel: counters sized for the two-pair kernel's tiles (four
-// 128-row parts per tile; at least the other kernels' counts), then the largest of the
-// kernels' partial-tile slots.  Every kernel leaves the counters zero.
+// Stream-K state of either W4A4 kernel: counters sized for the pair kernel's tiles (two
+// 128-row halves per tile; at least the one-CTA kernel's count), then the larger of the two
+// kernels' partial-tile slots.  Both kernels leave the counters zero.
 size_t counter_region(int64_t M, int64_t N) {
-    return tc::counters_bytes(4 * ((N + 511) / 512) * ((M + 255) / 256));
+    return tc::counters_bytes(2 * ((N + 255) / 256) * ((M + 255) / 256));
 }
 
 template <bool kQuantX>
@@ -913,41 +890,39 @@ cudaError_t launch(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M
 
 // ---- pair kernel host side ----
 
-template <bool kQuantX, int kPairs>
+template <bool kQuantX>
 cudaError_t configure_pair(const DevInfo& dev) {
     static std::atomic<uint64_t> configured{0};
     const uint64_t bit = 1ull << (dev.device & 63);
     if (configured.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(gemm_w4a4_pair_kernel<kQuantX, kPairs>,
+    const cudaError_t e = cudaFuncSetAttribute(gemm_w4a4_pair_kernel<kQuantX>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)pairk::kSmemBytes);
     if (e == cudaSuccess) configured.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
 
-// Clusters of kPairs CTA pairs the device holds at once (one CTA per SM); 0 when it cannot
-// co-schedule them
-template <bool kQuantX, int kPairs>
+// CTA pairs the device holds at once (one CTA per SM); 0 when it cannot co-schedule them
+template <bool kQuantX>
 int pair_units(const DevInfo& dev) {
     static std::atomic<int> units[64];  // 0: not queried yet, else units + 1
     std::atomic<int>& slot = units[dev.device & 63];
     const int c = slot.load(std::memory_order_acquire);
     if (c) return c - 1;
     int n = 0;
-    if (dev.smem_optin >= pairk::kSmemBytes &&
-        configure_pair<kQuantX, kPairs>(dev) == cudaSuccess) {
+    if (dev.smem_optin >= pairk::kSmemBytes && configure_pair<kQuantX>(dev) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * kPairs);
+        cfg.gridDim = dim3(2);
         cfg.blockDim = dim3(pairk::kThreads);
         cfg.dynamicSmemBytes = pairk::kSmemBytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2 * kPairs;
+        attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_w4a4_pair_kernel<kQuantX, kPairs>, &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_w4a4_pair_kernel<kQuantX>, &cfg) !=
             cudaSuccess) {
             cudaGetLastError();
             n = 0;
@@ -957,7 +932,7 @@ int pair_units(const DevInfo& dev) {
     return n;
 }
 
-template <bool kQuantX, int kPairs>
+template <bool kQuantX>
 cudaError_t launch_pair(int units, const uint8_t* xq, const uint8_t* xsz, const float* gx, int M,
                         int K, const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
                         void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
@@ -965,82 +940,71 @@ cudaError_t launch_pair(int units, const uint8_t* xq, const uint8_t* xsz, const 
     constexpr int kBM = pairk::kBM, kBK = pairk::kBK;
     constexpr int kThreads = pairk::kThreads;
     constexpr uint32_t kSmemBytes = pairk::kSmemBytes;
-    const GemmPlan p = tc::make_plan(M, K, N, units, 256 * kPairs, kBM, kBK);
+    const GemmPlan p = tc::make_plan(M, K, N, units, 256, kBM, kBK);
     const int natoms_row = (K + 63) / 64;
     CUtensorMap mw, mx, msw, msx;
     cudaError_t e = tc::make_map_2d(&mw, wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2,
                                     (uint64_t)N, kBK / 2, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    // x codes: a CTA's 128 rows, or the 64 of them each pair of a two-pair cluster loads
     e = tc::make_map_2d(&mx, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, (uint64_t)K / 2, (uint64_t)M,
-                        kBK / 2, 128 / kPairs, CU_TENSOR_MAP_SWIZZLE_128B);
+                        kBK / 2, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    // scale atoms as rows of 128 32-bit words: row (row block * natoms_row + atom); W: the
-    // 4 atoms of a K step, x: 4 (or the 2 each pair loads)
+    // scale atoms as rows of 128 32-bit words: row (row block * natoms_row + atom), the 4
+    // atoms of a K step per box
     e = tc::make_map_2d(&msw, wsz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 128,
                         (uint64_t)((N + 127) / 128) * natoms_row, 128, 4,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     e = tc::make_map_2d(&msx, xsz, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, 128,
-                        (uint64_t)((M + 127) / 128) * natoms_row, 128, 4 / kPairs,
+                        (uint64_t)((M + 127) / 128) * natoms_row, 128, 4,
                         CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     uint32_t* counters = reinterpret_cast<uint32_t*>(sk_state);
     float* slots = reinterpret_cast<float*>(sk_state + counter_region(M, N));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * kPairs * p.grid);
+    cfg.gridDim = dim3(2 * p.grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2 * kPairs;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeCooperative;
     attr[1].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = kQuantX ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_w4a4_pair_kernel<kQuantX, kPairs>, mw, mx, msw, msx, gw, gx,
-                           y, y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, p.ntiles_m, p.ntiles,
+    e = cudaLaunchKernelEx(&cfg, gemm_w4a4_pair_kernel<kQuantX>, mw, mx, msw, msx, gw, gx, y,
+                           y_bf16 ? 1 : 0, M, N, p.nkb, natoms_row, p.ntiles_m, p.ntiles,
                            p.ntiles_sk, p.p_sk, p.tsk, err, counters, slots, qa,
                            current_wait_cfg());
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// The CTA-pair kernels, where the calling thread asks for them (w4a4_pair_mode: 1 single
-// pairs, 2 clusters of two pairs, else single pairs); *launched stays false for the one-CTA
-// kernel (the default: it is the fastest of the three on this hardware) or when the device
-// cannot hold the clusters
+// The CTA-pair kernel, where the calling thread asks for it (w4a4_use_pairs); *launched
+// stays false for the one-CTA kernel (the default: the faster of the two on this hardware)
+// or when the device cannot co-schedule CTA pairs
 template <bool kQuantX>
-cudaError_t launch_pair_any(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M, int K,
-                            const uint8_t* wq, const uint8_t* wsz, const float* gw, int N,
-                            void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
-                            const QxArgs& qa, cudaStream_t stream, const DevInfo& dev,
-                            bool* launched) {
+cudaError_t launch_pair_if_asked(const uint8_t* xq, const uint8_t* xsz, const float* gx, int M,
+                                 int K, const uint8_t* wq, const uint8_t* wsz, const float* gw,
+                                 int N, void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
+                                 const QxArgs& qa, cudaStream_t stream, const DevInfo& dev,
+                                 bool* launched) {
     *launched = false;
-    const int mode = w4a4_pair_mode();
-    if (mode == 0) return cudaSuccess;
-    const int u2 = mode == 2 ? pair_units<kQuantX, 2>(dev) : 0;
-    if (u2 > 0) {
-        *launched = true;
-        return launch_pair<kQuantX, 2>(u2, xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16, err,
-                                       sk_state, qa, stream);
-    }
-    const int u1 = pair_units<kQuantX, 1>(dev);
-    if (u1 > 0) {
-        *launched = true;
-        return launch_pair<kQuantX, 1>(u1, xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16, err,
-                                       sk_state, qa, stream);
-    }
-    return cudaSuccess;
+    if (!w4a4_use_pairs()) return cudaSuccess;
+    const int units = pair_units<kQuantX>(dev);
+    if (units <= 0) return cudaSuccess;
+    *launched = true;
+    return launch_pair<kQuantX>(units, xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16, err,
+                                sk_state, qa, stream);
 }
 
 }  // namespace
 
 size_t gemm_w4a4_stream_k_bytes(int64_t M, int64_t K, int64_t N) {
     size_t slots = 0;
-    for (int bn : {kBN, 256, 512}) {
+    for (int bn : {kBN, 256}) {
         const size_t b = tc::stream_k_bytes(M, K, N, bn, kBM, kBK) -
                          tc::counters_bytes(((N + bn - 1) / bn) * ((M + kBM - 1) / kBM));
         if (b > slots) slots = b;
@@ -1055,7 +1019,7 @@ cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float*
                              void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
                              cudaStream_t stream, const DevInfo& dev) {
     bool launched = false;
-    const cudaError_t e = launch_pair_any<false>(xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16,
+    const cudaError_t e = launch_pair_if_asked<false>(xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16,
                                                  err, sk_state, QxArgs{}, stream, dev, &launched);
     if (launched) return e;
     return launch<false>(xq, xsz, gx, M, K, wq, wsz, gw, N, y, y_bf16, err, sk_state, QxArgs{},
@@ -1077,9 +1041,9 @@ cudaError_t launch_gemm_w4a4_quant_x(const uint16_t* x, const float* gx_static, 
     qa.xs = xsz;
     qa.K = K;
     bool launched = false;
-    const cudaError_t e = launch_pair_any<true>(xq, xsz, gx_out, M, K, wq, wsz, gw, N, y, y_bf16,
+    const cudaError_t e = launch_pair_if_asked<true>(xq, xsz, gx_out, M, K, wq, wsz, gw, N, y, y_bf16,
                                                 err, sk_state, qa, stream, dev, &launched);
-    // a device that refuses a cooperative launch of CTA clusters (or cannot hold them all)
+    // a device that refuses a cooperative launch of CTA pairs (or cannot hold them all)
     // takes the one-CTA kernel
     if (launched && e == cudaSuccess) return e;
     if (launched) cudaGetLastError();

@@ -139,10 +139,9 @@ cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float*
                              void* y, bool y_bf16, uint32_t* err, uint8_t* sk_state,
                              cudaStream_t stream, const DevInfo& dev);
 
-// Which W4A4 GEMM kernel the calling thread uses at M > 16 (nvfp4_debug_w4a4_kernel): 0
-// (default) the one-CTA kernel; 1 single CTA pairs; 2 clusters of two CTA pairs (each
-// falls back to the one-CTA kernel on a device that cannot hold it).
-int w4a4_pair_mode();
+// True while the calling thread asks for the CTA-pair W4A4 GEMM at M > 16
+// (nvfp4_debug_w4a4_kernel); by default the one-CTA kernel runs.
+bool w4a4_use_pairs();
 
 // Wait settings for the launches of the calling thread: the production limits, or (while
 // nvfp4_debug_expire_waits is on) a 200 us limit and the stall switch.

@@ -150,7 +150,7 @@ int query_device(DevInfo* out) { return (int)current_device(out); }
 
 namespace {
 thread_local bool t_expire_waits = false;
-thread_local int t_w4a4_pair_mode = 0;
+thread_local bool t_w4a4_pairs = false;
 constexpr uint64_t kDebugWaitNs = 200000;  // 200 us
 }  // namespace
 
@@ -163,7 +163,7 @@ WaitCfg current_wait_cfg() {
     return w;
 }
 
-int w4a4_pair_mode() { return t_w4a4_pair_mode; }
+bool w4a4_use_pairs() { return t_w4a4_pairs; }
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -494,9 +494,7 @@ NVFP4_API nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t
 
 NVFP4_API void nvfp4_debug_expire_waits(int on) { t_expire_waits = on != 0; }
 
-NVFP4_API void nvfp4_debug_w4a4_kernel(int which) {
-    t_w4a4_pair_mode = which == 2 ? 1 : which == 3 ? 2 : 0;
-}
+NVFP4_API void nvfp4_debug_w4a4_kernel(int which) { t_w4a4_pairs = which == 2; }
 
 NVFP4_API const char* nvfp4_last_cuda_error(void) {
     return cudaGetErrorString(t_last_cuda_error);

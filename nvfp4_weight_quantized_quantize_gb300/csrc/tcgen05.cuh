@@ -187,18 +187,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// The same load issued for several CTAs of the cluster (ctaMask): the box lands at the
-// same shared-memory offset in each, and each completes on the mbarrier at the same offset
-// in its own pair's even CTA (cbar: that barrier in the issuing CTA's pair)
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map, int c0,
-                                                    int c1, uint32_t cbar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(cbar), "h"(mask)
-        : "memory");
-}
-
 // one 512-byte scale atom (32 rows of 16 bytes) from each CTA's shared memory into its own
 // TMEM: atom row i to lane 32 q + i of every lane quarter q, four columns
 __device__ __forceinline__ uint64_t atom_desc(uint32_t saddr) {
@@ -230,15 +218,6 @@ __device__ __forceinline__ void mma_mxf4nvf4_pair(uint32_t d, uint64_t adesc, ui
 __device__ __forceinline__ void commit_pair(uint32_t cbar) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(cbar)
-        : "memory");
-}
-
-// arrive (once) on the mbarrier at shared offset `bar` in every CTA of ctaMask when every
-// pair operation this thread issued so far completes
-__device__ __forceinline__ void commit_pair_mc(uint32_t bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar), "h"(mask)
         : "memory");
 }
 
@@ -358,9 +337,8 @@ __device__ __forceinline__ void store_rows32(void* y, int y_bf16, int64_t M, int
     }
 }
 
-// Where a CTA's stream-K state lives: its unit (the CTA itself, or the cluster of CTA
-// pairs whose CTAs hold the nhalves 128-row parts of every tile's W rows), and which part
-// it holds.  Unit c's partial of a tile goes to slot (sk_slot(c, ...) * nhalves + half);
+// Where a CTA's stream-K state lives: its unit (the CTA itself, or the CTA pair whose two
+// CTAs hold the two 128-row halves of every tile's W rows), and which half it holds.  Unit c's partial of a tile goes to slot (sk_slot(c, ...) * nhalves + half);
 // the tile's counters are (tile * nhalves + half) * 4 + quarter.
 struct SkUnit {
     int me = 0;

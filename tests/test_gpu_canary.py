@@ -55,9 +55,9 @@ def guarded(shape, dtype):
     (3, 5152, 1001, "w4a16"), (8, 2080, 129, "w4a16"), (5, 17440, 301, "w4a16"),
     (13, 1056, 257, "w4a16"), (16, 17408, 199, "w4a16"), (17, 1056, 300, "w4a16"),
     (300, 2080, 257, "w4a16"), (40, 1056, 129, "w4a4"), (300, 5152, 641, "w4a4"),
-    (3, 1056, 77, "w4a4"), (12, 2080, 300, "w4a4"), (300, 5152, 641, "w4a4-pair2"),
-    (40, 1056, 129, "w4a4-pair2"), (520, 2080, 1300, "w4a4"), (300, 5152, 641, "w4a4-pair"),
-    (520, 2080, 1300, "w4a4-pair"), (700, 1056, 1500, "w4a4"),
+    (3, 1056, 77, "w4a4"), (12, 2080, 300, "w4a4"), (300, 5152, 641, "w4a4-pair"),
+    (40, 1056, 129, "w4a4-pair"), (520, 2080, 1300, "w4a4"), (520, 2080, 1300, "w4a4-pair"),
+    (700, 1056, 1500, "w4a4-pair"),
 ])
 def test_linear_writes_only_its_outputs(M, K, N, mode):
     kernel = mode.split("-")[1] if "-" in mode else "auto"

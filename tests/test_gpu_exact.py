@@ -27,7 +27,7 @@ once, so the kernel's fp32 y must equal the oracle's fp64 result rounded to fp32
   2 <= M <= 8: the skinny kernel, and the mma.sync kernel where K exceeds its ring;
   9 <= M <= 16: two skinny passes, and the mma.sync kernel at large K;
   M > 16: the tcgen05 W4A16 GEMM (with stream-K tails) and the block-scaled W4A4 GEMM
-         (the one-CTA kernel, and the CTA-pair kernels);
+         (the one-CTA kernel, and the CTA-pair kernel);
   W4A4 at small M (pre-pass, and the static-scale fused kernels), and the linear on
   NVFP4 activations.
 """
@@ -161,10 +161,9 @@ def test_w4a4_exact(M, K, N, gx):
 @pytest.mark.parametrize("M,K,N", [(40, 5120, 1000), (200, 17408, 600), (64, 5120, 640),
                                    (300, 2080, 777)])
 @pytest.mark.parametrize("gx", [None, 2.0 ** -5], ids=["dyn", "static"])
-@pytest.mark.parametrize("kernel", ["pair", "pair2"])
-def test_w4a4_exact_pair_kernels(M, K, N, gx, kernel):
-    # the CTA-pair block-scaled kernels: single pairs, and clusters of two pairs that share
-    # the x tile by multicast
+def test_w4a4_exact_pair_kernel(M, K, N, gx):
+    # the CTA-pair block-scaled kernel (tcgen05 cta_group::2)
+    kernel = "pair"
     x = sparse_block_x(M, K, seed=3 * M + K)
     wq, ws, gw = structured_nvfp4_weights(N, K, seed=5 * N + K)
     with w4a4_kernel(kernel):
@@ -176,9 +175,9 @@ def test_w4a4_exact_pair_kernels(M, K, N, gx, kernel):
 
 @pytest.mark.parametrize("M,K,N,kernel", [(1, 5120, 2000, "auto"), (7, 5120, 900, "auto"),
                                           (16, 2048, 300, "auto"), (100, 17408, 640, "auto"),
-                                          (100, 17408, 640, "pair2"), (300, 1056, 300, "auto"),
-                                          (300, 1056, 300, "pair2"), (300, 1056, 300, "pair"),
-                                          (600, 2048, 1100, "pair2")])
+                                          (100, 17408, 640, "pair"), (300, 1056, 300, "auto"),
+                                          (300, 1056, 300, "one_cta"), (300, 1056, 300, "pair"),
+                                          (600, 2048, 1100, "pair")])
 def test_linear_nvfp4_x_exact(M, K, N, kernel):
     x = sparse_block_x(M, K, seed=11 * M + K)
     xq, xs, gx = oracle.quantize(x)

@@ -33,7 +33,7 @@ NVFP4_DEVERR_TIMEOUT = 0x1
     (64, 1024, 512, "w4a16", "tcgen05 W4A16 GEMM: no stage is marked dequantized"),
     (64, 1024, 512, "w4a4", "block-scaled GEMM: one CTA never counts its share of x"),
     (64, 1024, 512, "w4a4-pair", "block-scaled CTA-pair GEMM: one CTA never counts"),
-    (300, 2048, 1000, "w4a4-pair2", "two-pair clusters over several tiles: one never counts"),
+    (300, 2048, 1000, "w4a4-pair", "CTA pairs over several tiles: one CTA never counts"),
 ])
 def test_expired_wait_reports_and_recovers(M, K, N, mode, what):
     kernel = mode.split("-")[1] if "-" in mode else "auto"
@@ -78,12 +78,12 @@ def test_expired_wait_reports_and_recovers(M, K, N, mode, what):
     check_tolerance(y_to_f64(y)[pm, pn], y_ref, ab, what)
 
 
-@pytest.mark.parametrize("M,K,N,kernel", [(64, 1024, 512, "auto"), (300, 2048, 1000, "pair2"),
+@pytest.mark.parametrize("M,K,N,kernel", [(64, 1024, 512, "auto"), (300, 2048, 1000, "pair"),
                                           (64, 1024, 512, "pair")])
 def test_expired_wait_nvfp4_x(M, K, N, kernel):
     # the GEMM on NVFP4 activations (no in-kernel quantization): the one-CTA kernel's scale
-    # writers never mark a stage's scales written (the CTA-pair kernels' MMA issuers never
-    # mark an accumulator full), so a wait runs out
+    # writers never mark a stage's scales written (the CTA-pair kernel's MMA issuer never
+    # marks an accumulator full), so a wait runs out
     x = random_x(M, K, seed=M + 3)
     xq, xs, gx = oracle.quantize(x)
     wq, ws, gw = random_nvfp4_weights(N, K, seed=N + 3)
