@@ -909,13 +909,11 @@ cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
     const int64_t atom = (int64_t)((N + 127) / 128 * 128) * ((K / 16 + 3) / 4 * 4);
     const uint8_t* wsz = wsz_all + atom;
     if (M == 1) return launch_m1(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream, dev);
-    if (M <= 8) {
-        bool launched = false;
-        const cudaError_t e = launch_skinny_w4a16(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, err,
-                                                  w_static, stream, dev, &launched);
-        if (e != cudaSuccess || launched) return e;
-        return launch_mma<1>(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, stream, dev);
-    }
+    bool launched = false;
+    const cudaError_t e = launch_skinny_w4a16(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, err,
+                                              w_static, stream, dev, &launched);
+    if (e != cudaSuccess || launched) return e;
+    if (M <= 8) return launch_mma<1>(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, stream, dev);
     return launch_mma<2>(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, stream, dev);
 }
 

@@ -77,11 +77,13 @@ cudaError_t launch_gemv_w4a4_static(const uint16_t* x, int M, int K, const uint8
                                     int N, void* y, bool y_bf16, uint32_t* err, bool w_static,
                                     cudaStream_t stream, const DevInfo& dev, bool* launched);
 
-// Whether launch_skinny_w4a16 takes calls with this K (its ring fits shared memory).
+// Whether launch_skinny_w4a16 takes calls with this K (its ring fits shared memory), for
+// up to 8 tokens and for 9..16 tokens (two token tiles, one pass over W).
 bool skinny_w4a16_takes(int K, const DevInfo& dev);
+bool skinny16_w4a16_takes(int K, const DevInfo& dev);
 
-// 2 <= M <= 8 W4A16 skinny GEMM streaming W through a shared-memory ring, tensor cores
-// for the arithmetic.  wrm: the row-major part of the repacked scales.  Sets *launched
+// 2 <= M <= 16 W4A16 skinny GEMM streaming W through a shared-memory ring, tensor cores
+// for the arithmetic (M <= 8 for the quantizing W4A4 variant).  wrm: the row-major part of the repacked scales.  Sets *launched
 // when it took the call (K small enough for its ring); otherwise the caller falls back.
 cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
                                 const uint8_t* wrm, const float* gw, const float* gx, int N,

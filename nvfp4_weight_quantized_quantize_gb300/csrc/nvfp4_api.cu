@@ -76,14 +76,17 @@ size_t repack_bytes(int64_t rows, int64_t cols) {
     return repack_atom_bytes(rows, cols) + (size_t)((rows * (cols / 16) + 15) / 16 * 16) + 16;
 }
 
-// M <= 16 on the small-M kernels.  The skinny kernel takes at most 8 tokens; where it
-// takes this K, 9 <= M <= 16 runs as tokens 0..7 and then tokens 8..M-1 (the M = 1 GEMV
-// for one): W is streamed twice, the second time partly from L2 and under the first
-// launch.  Each output depends on its own token only, so the split changes no result.
+// M <= 16 on the small-M kernels.  The skinny kernel takes 9 <= M <= 16 in one pass over W
+// (two token tiles) where that ring fits this K; where only its 8-token ring fits, the
+// call runs tokens 0..7 and then tokens 8..M-1 (the M = 1 GEMV for one): W is streamed
+// twice, the second time partly from L2 and under the first launch.  Each output depends
+// on its own token only, so the split changes no result.
 cudaError_t small_m(const uint16_t* x, int M, int K, const uint8_t* wq, const uint8_t* wsz,
                     const float* gw, const float* gx, int N, void* y, bool ybf, uint32_t* err,
                     bool w_static, cudaStream_t stream, const DevInfo& d) {
-    if (M <= 8 || !skinny_w4a16_takes(K, d))
+    // up to 8 tokens, or 9..16 where the skinny kernel takes them in one pass over W (two
+    // token tiles); otherwise 9..16 tokens as two skinny passes of 8 and M - 8
+    if (M <= 8 || !skinny_w4a16_takes(K, d) || skinny16_w4a16_takes(K, d))
         return launch_gemv_w4a16(x, M, K, wq, wsz, gw, gx, N, y, ybf, err, w_static, stream, d);
     const cudaError_t e =
         launch_gemv_w4a16(x, 8, K, wq, wsz, gw, gx, N, y, ybf, err, w_static, stream, d);

@@ -1,4 +1,4 @@
-// skinny.cu -- W4A16 NVFP4 skinny GEMM for 2 <= M <= 8 (MTP verify: drafts + 1 rows of x
+// skinny.cu -- W4A16 NVFP4 skinny GEMM for 2 <= M <= 16 (MTP verify: drafts + 1 rows of x
 // against the same weights).  FlashRT docs/qwen36_usage.md
 // (generate_own_speculative_KN_nvfp4 argument table: verify runs K + 1 tokens at once).
 //
@@ -21,6 +21,10 @@
 //     (deterministic) and writes the 16 rows of y.  No warp waits for another.
 // x values that fp16 cannot hold exactly after the rescale (more than about 2^31 below
 // the token's maximum) make every warp add the exact fp32 residual of its slice.
+// 9 to 16 tokens (NT = 2) take one pass over W: each A fragment (the dequantized,
+// scale-folded weights) feeds two MMAs, tokens 0..7 from registers and tokens 8..15 from
+// the lane's own slots in shared memory (the register file cannot hold both tiles of x);
+// at most 15 consumer warps, so that a thread may keep 128 registers.
 // W4A4 with a static activation scale (the kXQ instantiations): each lane first quantizes
 // its chunks of x to NVFP4 and keeps e2m1 * e4m3, which the rescale carries exactly.
 #include <cuda_fp16.h>
@@ -48,37 +52,56 @@ __host__ __device__ __forceinline__ size_t sk_stage_bytes(int K, int rgs) {
     return ((rows * (K / 2) + rows * (K / 16) + 32) + 127) & ~(size_t)127;
 }
 
-// slot area of one stage: per row group, ngroups partial tiles of 16 rows x 8 tokens (fp32)
-__host__ __device__ __forceinline__ size_t sk_slot_bytes(int ngroups, int rgs) {
-    return (size_t)rgs * ngroups * kSkRows * 8 * 4;
+// slot area of one stage: per row group, ngroups partial tiles of 16 rows x 8 NT tokens
+// (fp32)
+__host__ __device__ __forceinline__ size_t sk_slot_bytes(int ngroups, int rgs, int nt) {
+    return (size_t)rgs * ngroups * kSkRows * 8 * nt * 4;
 }
 
-__host__ __device__ __forceinline__ size_t sk_smem(int K, int ngroups, int stages, int rgs) {
-    return (size_t)stages * (sk_stage_bytes(K, rgs) + sk_slot_bytes(ngroups, rgs)) +
-           (size_t)stages * (8 + 8 + 4 * kSkMaxRgs);  // full, empty barriers; row-group counters
+// the second token tile's B fragments (tokens 8..15), per consumer warp: U x 8 MMAs x 32
+// lanes x 8 bytes
+__host__ __device__ __forceinline__ size_t sk_x2_bytes(int ngroups, int u, int nt) {
+    return nt == 2 ? (size_t)ngroups * u * 8 * 32 * 8 + 16 : 0;  // (+ alignment slack)
 }
 
-template <int U, bool kXQ>
-__global__ void __launch_bounds__(kSkMaxThreads, 1)
+__host__ __device__ __forceinline__ size_t sk_smem(int K, int ngroups, int stages, int rgs,
+                                                   int u, int nt) {
+    return (size_t)stages * (sk_stage_bytes(K, rgs) + sk_slot_bytes(ngroups, rgs, nt)) +
+           (size_t)stages * (8 + 8 + 4 * kSkMaxRgs) +  // full, empty barriers; row-group counters
+           sk_x2_bytes(ngroups, u, nt);
+}
+
+// two token tiles hold twice the accumulators and read the second tile's fragments from
+// shared memory: at most 16 warps, so that each thread may keep 128 registers
+constexpr int kSk2MaxGroups = 15;
+
+template <int U, bool kXQ, int NT>
+__global__ void __launch_bounds__(NT == 2 ? (kSk2MaxGroups + 1) * 32 : kSkMaxThreads, 1)
 skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* __restrict__ wq,
                    const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
                    const float* __restrict__ gx, int N, void* __restrict__ y, int y_bf16,
                    int stages, int rgs, int w_static, uint32_t* __restrict__ err) {
     constexpr int CG = 4 * U;  // 16-byte chunks (32 elements) of K per consumer warp
+    constexpr int TT = 8 * NT;  // tokens of a partial tile
+    static_assert(NT == 1 || !kXQ, "two token tiles only for bf16 x");
     extern __shared__ __align__(128) uint8_t smem[];
     const int rowchunks = K >> 5;
     const int ngroups = (rowchunks + CG - 1) / CG;
     const size_t st_bytes = sk_stage_bytes(K, rgs);
-    const size_t sl_bytes = sk_slot_bytes(ngroups, rgs);
+    const size_t sl_bytes = sk_slot_bytes(ngroups, rgs, NT);
     const int srows = kSkRows * rgs;  // rows of a full stage
     uint8_t* ring = smem;
     float* slots = reinterpret_cast<float*>(smem + (size_t)stages * st_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * (st_bytes + sl_bytes));
     uint64_t* empty = full + stages;
     int* cnt = reinterpret_cast<int*>(empty + stages);
+    // tokens 8..15 (NT = 2): each lane's B fragments, [warp][u][mma j][lane]
+    uint2* x2 = reinterpret_cast<uint2*>(
+        smem + (((size_t)stages * (st_bytes + sl_bytes) + (size_t)stages * (8 + 8 + 4 * kSkMaxRgs) +
+                 15) & ~(size_t)15));
     __shared__ volatile int abort_flag;
-    __shared__ int e_w[kSkMaxGroups][8];    // per consumer warp and token: the exponent
-    __shared__ float u_w[kSkMaxGroups][8];  // and 2^-e
+    __shared__ int e_w[kSkMaxGroups][TT];    // per consumer warp and token: the exponent
+    __shared__ float u_w[kSkMaxGroups][TT];  // and 2^-e
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -161,6 +184,66 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
     // whole of x at the same moment, start on different parts of it
     const int wk = (warp + (int)(blockIdx.x % (unsigned)ngroups)) % ngroups;
     const int cbase = wk * CG + t;  // this lane's first chunk
+    // tokens 8..15 (NT = 2), first, so that their raw values are dead before the first
+    // tile's fragments are built: the same steps as for the first tile below, for token
+    // g + 8; the B fragments go to this lane's slots in shared memory, read back by the same
+    // lane
+    float ua2 = 1.0f, ub2 = 1.0f;
+    bool inexact2_any = false;
+    if constexpr (NT == 2) {
+        uint2 raw[U][8];
+        float am2 = 0.0f, mn2 = __int_as_float(0x7f800000);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = cbase + 4 * u;
+            const bool ok = g + 8 < M && c < rowchunks;
+            const uint4* xp = reinterpret_cast<const uint4*>(x + (int64_t)(g + 8) * K + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 v = ok ? xp[q] : make_uint4(0u, 0u, 0u, 0u);
+                raw[u][2 * q] = make_uint2(v.x, v.y);
+                raw[u][2 * q + 1] = make_uint2(v.z, v.w);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t w2[2] = {raw[u][j].x, raw[u][j].y};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float a = fabsf(bf16_to_f32(w2[h] & 0xFFFFu));
+                    const float b = fabsf(bf16_to_f32(w2[h] >> 16));
+                    am2 = fmaxf(am2, fmaxf(a, b));
+                    if (a > 0.0f) mn2 = fminf(mn2, a);
+                    if (b > 0.0f) mn2 = fminf(mn2, b);
+                }
+            }
+        am2 = fmaxf(am2, __shfl_xor_sync(0xffffffffu, am2, 1));
+        am2 = fmaxf(am2, __shfl_xor_sync(0xffffffffu, am2, 2));
+        mn2 = fminf(mn2, __shfl_xor_sync(0xffffffffu, mn2, 1));
+        mn2 = fminf(mn2, __shfl_xor_sync(0xffffffffu, mn2, 2));
+        const int eg2 = chunk_exponent(am2);
+        inexact2_any = __any_sync(0xffffffffu, times_pow2(mn2, eg2) < 7.62939453125e-06f);
+        {
+            const int em = __shfl_sync(0xffffffffu, eg2, 4 * (lane & 7));
+            if (lane < 8) {
+                e_w[warp][8 + lane] = em;
+                u_w[warp][8 + lane] = times_pow2(1.0f, -em);
+            }
+            __syncwarp();
+        }
+        ua2 = u_w[warp][8 + 2 * t];
+        ub2 = u_w[warp][8 + 2 * t + 1];
+        bool inexact2 = false;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                x2[((warp * U + u) * 8 + j) * 32 + lane] =
+                    make_uint2(to_h2_scaled(raw[u][j].x, eg2, inexact2),
+                               to_h2_scaled(raw[u][j].y, eg2, inexact2));
+    }
     uint2 raw[U][8];
     float am = 0.0f, mn = __int_as_float(0x7f800000);
 #pragma unroll
@@ -214,7 +297,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
     const int eg = chunk_exponent(am);  // token g's exponent in this warp
     // (e2m1 * e4m3 values span less than 2^22: never inexact after the rescale)
     const bool any_inexact =
-        __any_sync(0xffffffffu, !kXQ && times_pow2(mn, eg) < 7.62939453125e-06f);
+        __any_sync(0xffffffffu, !kXQ && times_pow2(mn, eg) < 7.62939453125e-06f) || inexact2_any;
     // every token's exponent and 2^-e in this warp (token m's lanes are 4m .. 4m + 3), in
     // the warp's own shared-memory row
     {
@@ -263,6 +346,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
             const uint8_t* ss = sst + (size_t)(kSkRows * rgi) * rows_sb;
             const bool rga = g < nr, rgb = g + 8 < nr;  // rows past N hold stale bytes
             float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float d2[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // tokens 8..15 (NT = 2)
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int c = cbase + 4 * u;
@@ -297,17 +381,32 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                             "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
                             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(bf[u][j][0]), "r"(bf[u][j][1]));
+                        if constexpr (NT == 2) {
+                            // the same A fragment against tokens 8..15
+                            const uint2 b2 = x2[((warp * U + u) * 8 + j) * 32 + lane];
+                            asm volatile(
+                                "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+                                "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                                : "+f"(d2[0]), "+f"(d2[1]), "+f"(d2[2]), "+f"(d2[3])
+                                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b2.x), "r"(b2.y));
+                        }
                     }
                 }
             }
             // this warp's partial tile of the row group: slot[row][token], row g / g + 8,
-            // tokens 2t, 2t+1
-            float* tiles = slots + ((size_t)s * rgs + rgi) * ngroups * (kSkRows * 8);
-            float* mine = tiles + (size_t)warp * (kSkRows * 8);
-            mine[g * 8 + 2 * t] = d[0] * ua;
-            mine[g * 8 + 2 * t + 1] = d[1] * ub;
-            mine[(g + 8) * 8 + 2 * t] = d[2] * ua;
-            mine[(g + 8) * 8 + 2 * t + 1] = d[3] * ub;
+            // tokens 2t, 2t+1 (and 8 + 2t, 8 + 2t + 1)
+            float* tiles = slots + ((size_t)s * rgs + rgi) * ngroups * (kSkRows * TT);
+            float* mine = tiles + (size_t)warp * (kSkRows * TT);
+            mine[g * TT + 2 * t] = d[0] * ua;
+            mine[g * TT + 2 * t + 1] = d[1] * ub;
+            mine[(g + 8) * TT + 2 * t] = d[2] * ua;
+            mine[(g + 8) * TT + 2 * t + 1] = d[3] * ub;
+            if constexpr (NT == 2) {
+                mine[g * TT + 8 + 2 * t] = d2[0] * ua2;
+                mine[g * TT + 8 + 2 * t + 1] = d2[1] * ub2;
+                mine[(g + 8) * TT + 8 + 2 * t] = d2[2] * ua2;
+                mine[(g + 8) * TT + 8 + 2 * t + 1] = d2[3] * ub2;
+            }
             if (any_inexact) {
                 // exact residual x' - fp16(x') of this warp's K slice (slow path, rare): lane l
                 // takes row l % 16 and tokens l / 16, l / 16 + 2, ...
@@ -326,7 +425,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
                                          e2m1_to_f32(code) * sc, q);
                             }
                         }
-                        mine[r * 8 + m] += q * u_w[warp][m];
+                        mine[r * TT + m] += q * u_w[warp][m];
                     }
                 }
             }
@@ -340,20 +439,23 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
             if (lane == 0) old = atomicAdd(c_rg, 1);
             if (__shfl_sync(0xffffffffu, old, 0) == ngroups - 1) {
                 __threadfence_block();
-                float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float v[4 * NT];
+#pragma unroll
+                for (int i = 0; i < 4 * NT; ++i) v[i] = 0.0f;
                 const float* base = tiles + lane;
 #pragma unroll
                 for (int w = 0; w < kSkMaxGroups; ++w)
                     if (w < ngroups) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) v[i] += base[(size_t)w * (kSkRows * 8) + 32 * i];
+                        for (int i = 0; i < 4 * NT; ++i)
+                            v[i] += base[(size_t)w * (kSkRows * TT) + 32 * i];
                     }
                 __syncwarp();
                 if (lane == 0) *c_rg = 0;
                 const int64_t rbeg = sbeg + kSkRows * rgi;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int e = lane + 32 * i, r = e >> 3, m = e & 7;
+                for (int i = 0; i < 4 * NT; ++i) {
+                    const int e = lane + 32 * i, r = e / TT, m = e % TT;
                     if (r < nr && m < M)
                         store_y(y, (int64_t)m * N + rbeg + r, v[i] * gscale, y_bf16);
                 }
@@ -369,7 +471,7 @@ skinny_pipe_kernel(const uint16_t* __restrict__ x, int M, int K, const uint8_t* 
 
 namespace {
 
-template <int U, bool kXQ>
+template <int U, bool kXQ, int NT>
 cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
                             const uint8_t* wrm, const float* gw, const float* gx, int N, void* y,
                             bool y_bf16, uint32_t* err, bool w_static, cudaStream_t stream,
@@ -391,19 +493,21 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
     int stages = 6;
     for (;;) {
         stages = 6;
-        while (stages > 2 && sk_smem(K, ngroups, stages, rgs) + 2048 > dev.smem_optin) --stages;
-        if (sk_smem(K, ngroups, stages, rgs) + 2048 <= dev.smem_optin || rgs == 1) break;
+        while (stages > 2 && sk_smem(K, ngroups, stages, rgs, U, NT) + 2048 > dev.smem_optin)
+            --stages;
+        if (sk_smem(K, ngroups, stages, rgs, U, NT) + 2048 <= dev.smem_optin || rgs == 1) break;
         --rgs;
     }
-    const size_t smem = sk_smem(K, ngroups, stages, rgs);
+    const size_t smem = sk_smem(K, ngroups, stages, rgs, U, NT);
     if (smem + 2048 > dev.smem_optin) return cudaSuccess;
     static std::atomic<uint64_t> configured{0};
     const uint64_t bit = 1ull << (dev.device & 63);
     if (!(configured.load(std::memory_order_acquire) & bit)) {
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, skinny_pipe_kernel<U, kXQ>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, skinny_pipe_kernel<U, kXQ, NT>);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(skinny_pipe_kernel<U, kXQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(skinny_pipe_kernel<U, kXQ, NT>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(dev.smem_optin - fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
@@ -418,7 +522,7 @@ cudaError_t launch_skinny_u(const uint16_t* x, int M, int K, const uint8_t* wq,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_pipe_kernel<U, kXQ>, x, M, K, wq, wrm, gw, gx, N,
+    cudaError_t e = cudaLaunchKernelEx(&cfg, skinny_pipe_kernel<U, kXQ, NT>, x, M, K, wq, wrm, gw, gx, N,
                                        y, y_bf16 ? 1 : 0, stages, rgs, w_static ? 1 : 0,
                                        err);
     *launched = true;
@@ -432,7 +536,23 @@ bool skinny_w4a16_takes(int K, const DevInfo& dev) {
     const int cg = (rowchunks + 3) / 4 <= kSkMaxGroups ? 4 : 8;  // chunks per warp (U = 1, 2)
     const int ngroups = (rowchunks + cg - 1) / cg;
     if (ngroups > kSkMaxGroups) return false;
-    return sk_smem(K, ngroups, 2, 1) + 2048 <= dev.smem_optin;  // the smallest ring
+    return sk_smem(K, ngroups, 2, 1, cg / 4, 1) + 2048 <= dev.smem_optin;  // the smallest ring
+}
+
+// chunks of K per consumer warp of the two-tile kernel: 8, 12 or 16 (at most
+// kSk2MaxGroups warps); 0 when none fits
+int sk2_chunks_per_warp(int K) {
+    const int rowchunks = K / 32;
+    for (int cg = 8; cg <= 16; cg += 4)
+        if ((rowchunks + cg - 1) / cg <= kSk2MaxGroups) return cg;
+    return 0;
+}
+
+bool skinny16_w4a16_takes(int K, const DevInfo& dev) {
+    const int cg = sk2_chunks_per_warp(K);
+    if (cg == 0) return false;
+    const int ngroups = (K / 32 + cg - 1) / cg;
+    return sk_smem(K, ngroups, 2, 1, cg / 4, 2) + 2048 <= dev.smem_optin;
 }
 
 cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq,
@@ -441,25 +561,40 @@ cudaError_t launch_skinny_w4a16(const uint16_t* x, int M, int K, const uint8_t* 
                                 cudaStream_t stream, const DevInfo& dev, bool* launched,
                                 bool x_quant_static) {
     *launched = false;
-    if (M < 2 || M > 8) return cudaSuccess;
+    if (M < 2 || M > 16 || (x_quant_static && M > 8)) return cudaSuccess;
+    const int rowchunks = K / 32;
     if (x_quant_static) {
-        const int rowchunks = K / 32;
         if ((rowchunks + 3) / 4 <= kSkMaxGroups)
-            return launch_skinny_u<1, true>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
-                                            w_static, stream, dev, launched);
+            return launch_skinny_u<1, true, 1>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                               w_static, stream, dev, launched);
         if ((rowchunks + 7) / 8 <= kSkMaxGroups)
-            return launch_skinny_u<2, true>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
-                                            w_static, stream, dev, launched);
+            return launch_skinny_u<2, true, 1>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                               w_static, stream, dev, launched);
         return cudaSuccess;
     }
-    // at most kSkMaxGroups consumer warps: 4 or 8 chunks of K per warp
-    const int rowchunks = K / 32;
+    // at most kSkMaxGroups consumer warps: 4 or 8 chunks of K per warp; 9..16 tokens in two
+    // token tiles over one pass of W
+    if (M > 8) {
+        switch (sk2_chunks_per_warp(K)) {
+            case 8:
+                return launch_skinny_u<2, false, 2>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                                    w_static, stream, dev, launched);
+            case 12:
+                return launch_skinny_u<3, false, 2>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                                    w_static, stream, dev, launched);
+            case 16:
+                return launch_skinny_u<4, false, 2>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                                    w_static, stream, dev, launched);
+            default:
+                return cudaSuccess;
+        }
+    }
     if ((rowchunks + 3) / 4 <= kSkMaxGroups)
-        return launch_skinny_u<1, false>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, w_static, stream,
-                                  dev, launched);
+        return launch_skinny_u<1, false, 1>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                            w_static, stream, dev, launched);
     if ((rowchunks + 7) / 8 <= kSkMaxGroups)
-        return launch_skinny_u<2, false>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err, w_static, stream,
-                                  dev, launched);
+        return launch_skinny_u<2, false, 1>(x, M, K, wq, wrm, gw, gx, N, y, y_bf16, err,
+                                            w_static, stream, dev, launched);
     return cudaSuccess;
 }
 

@@ -25,7 +25,8 @@ once, so the kernel's fp32 y must equal the oracle's fp64 result rounded to fp32
   M = 1: the pipelined GEMV at G = 8, 16 and 32 lanes per row, and the fallback GEMV
          (K / 32 < 64);
   2 <= M <= 8: the skinny kernel, and the mma.sync kernel where K exceeds its ring;
-  9 <= M <= 16: two skinny passes, and the mma.sync kernel at large K;
+  9 <= M <= 16: the skinny kernel with two token tiles (one pass over W), and the mma.sync
+         kernel at large K;
   M > 16: the tcgen05 W4A16 GEMM (with stream-K tails) and the block-scaled W4A4 GEMM
          (the one-CTA kernel, and the CTA-pair kernel);
   W4A4 at small M (pre-pass, and the static-scale fused kernels), and the linear on
@@ -108,7 +109,10 @@ W4A16_SHAPES = [
     (7, 5120, 6144),    # skinny (verify shape)
     (8, 2080, 129),     # skinny, ragged N
     (5, 17408, 1000),   # mma.sync kernel (K beyond the skinny ring)
-    (12, 5120, 2000),   # two skinny passes
+    (12, 5120, 2000),   # skinny, two token tiles
+    (9, 5120, 6144),    # skinny, two token tiles, one token in the second
+    (16, 1056, 300),    # skinny, two token tiles, 4 chunks per warp
+    (13, 2080, 129),    # skinny, two token tiles, ragged N
     (16, 17408, 500),   # mma.sync kernel, two token tiles
     (40, 5120, 1000),   # tcgen05 GEMM, one x tile, stream-K tail
     (300, 17408, 700),  # tcgen05 GEMM, K = 17408

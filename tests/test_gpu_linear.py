@@ -188,10 +188,12 @@ def test_multiple_k_chunks(M, K, N):
 
 
 @pytest.mark.parametrize("M,K,N,wide", [(5, 256, 39001, False), (7, 512, 31623, False),
-                                        (2, 1024, 24000, False), (7, 256, 39001, True)])
+                                        (2, 1024, 24000, False), (7, 256, 39001, True),
+                                        (12, 512, 31623, False), (16, 256, 39001, True)])
 def test_skinny_stages_of_several_row_groups(M, K, N, wide):
-    # enough rows per CTA that a pipeline stage of the 2..8-token kernel holds two to four
-    # 16-row groups, the last one ragged; the wide-range case takes the exact residual path
+    # enough rows per CTA that a pipeline stage of the skinny kernel holds two to four 16-row
+    # groups, the last one ragged (with one and with two token tiles); the wide-range case
+    # takes the exact residual path
     x, w = make_inputs(M, K, N, seed=500 + M + K)
     if wide:
         xf = x.float()
