@@ -262,12 +262,13 @@ def nvfp4_debug_expire_waits(on: bool) -> None:
     load().nvfp4_debug_expire_waits(1 if on else 0)
 
 
-W4A4_KERNELS = {"auto": 0, "one_cta": 1, "pair": 2}
+W4A4_KERNELS = {"auto": 0, "one_cta": 1, "pair": 2, "prepass": 3}
 
 
 def nvfp4_debug_w4a4_kernel(which: str) -> None:
     """Test switch: the kernel of the calling thread's W4A4 GEMMs at M > 16 -- "auto" (the
-    default, the one-CTA kernel), "one_cta" or "pair" (CTA pairs); see include/nvfp4.h."""
+    default, the one-CTA kernel), "one_cta", "pair" (CTA pairs) or "prepass" (x quantized
+    by the quantizer kernels ahead of the GEMM); see include/nvfp4.h."""
     load().nvfp4_debug_w4a4_kernel(W4A4_KERNELS[which])
 
 

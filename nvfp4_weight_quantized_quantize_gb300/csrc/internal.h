@@ -144,6 +144,9 @@ cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float*
 // True while the calling thread asks for the CTA-pair W4A4 GEMM at M > 16
 // (nvfp4_debug_w4a4_kernel); by default the one-CTA kernel runs.
 bool w4a4_use_pairs();
+// True while the calling thread asks for the quantizer kernels ahead of the W4A4 GEMM at
+// M > 16 instead of the GEMM's in-kernel quantization (nvfp4_debug_w4a4_kernel).
+bool w4a4_prepass_forced();
 
 // Wait settings for the launches of the calling thread: the production limits, or (while
 // nvfp4_debug_expire_waits is on) a 200 us limit and the stall switch.

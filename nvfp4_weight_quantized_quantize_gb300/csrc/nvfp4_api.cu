@@ -154,6 +154,7 @@ int query_device(DevInfo* out) { return (int)current_device(out); }
 namespace {
 thread_local bool t_expire_waits = false;
 thread_local bool t_w4a4_pairs = false;
+thread_local bool t_w4a4_prepass = false;
 constexpr uint64_t kDebugWaitNs = 200000;  // 200 us
 }  // namespace
 
@@ -167,6 +168,7 @@ WaitCfg current_wait_cfg() {
 }
 
 bool w4a4_use_pairs() { return t_w4a4_pairs; }
+bool w4a4_prepass_forced() { return t_w4a4_prepass; }
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -343,7 +345,7 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const W4A4Layout L = w4a4_layout(M, K, N);
     float* gx = reinterpret_cast<float*>(ws + L.gx);
-    if (M > kGemvMaxM) {
+    if (M > kGemvMaxM && !w4a4_prepass_forced()) {
         // one kernel: x quantized by the GEMM's own CTAs, then the block-scaled GEMM
         const cudaError_t e = launch_gemm_w4a4_quant_x(
             xb, x_global_scale, gx, reinterpret_cast<float*>(ws + L.partials),
@@ -497,7 +499,10 @@ NVFP4_API nvfp4_status nvfp4_encode_elements(const float* in, int64_t n, uint8_t
 
 NVFP4_API void nvfp4_debug_expire_waits(int on) { t_expire_waits = on != 0; }
 
-NVFP4_API void nvfp4_debug_w4a4_kernel(int which) { t_w4a4_pairs = which == 2; }
+NVFP4_API void nvfp4_debug_w4a4_kernel(int which) {
+    t_w4a4_pairs = which == 2;
+    t_w4a4_prepass = which == 3;
+}
 
 NVFP4_API const char* nvfp4_last_cuda_error(void) {
     return cudaGetErrorString(t_last_cuda_error);

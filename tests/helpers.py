@@ -75,7 +75,7 @@ def upload_weights(wq: np.ndarray, ws: np.ndarray, gw: float, K: int):
 @contextlib.contextmanager
 def w4a4_kernel(which: str):
     """Run the W4A4 GEMM (M > 16) on the given kernel: "auto" (the one-CTA kernel),
-    "one_cta" or "pair"."""
+    "one_cta", "pair" or "prepass" (x quantized ahead of the GEMM)."""
     import nvfp4_weight_quantized_quantize_gb300 as nv
     nv.nvfp4_debug_w4a4_kernel(which)
     try:

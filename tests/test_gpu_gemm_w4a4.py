@@ -111,3 +111,21 @@ def test_w4a4_workload_sampled():
     pn = np.concatenate([pn, np.arange(wl.N), np.arange(wl.N)])
     y_ref, ab = oracle.linear_w4a4_pairs(xq, xs, gxo, wq, ws, gw, pm, pn)
     check_tolerance(y_to_f64(y)[pm, pn], y_ref, ab, "w4a4 workload")
+
+
+@pytest.mark.parametrize("M,K,N,gx", [(300, 2080, 777, None), (300, 2080, 777, 0.003),
+                                      (2048, 5120, 1000, None)])
+def test_in_kernel_quantization_matches_prepass(M, K, N, gx):
+    # x quantized inside the GEMM's grid and by the quantizer kernels ahead of it (the path
+    # of a device that refuses the cooperative launch): the same codes, scales and g_x,
+    # then the same GEMM, so y is the same to the bit
+    x, w = make_inputs(M, K, N, seed=900 + M, outliers=True)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y1, work1 = run_w4a4(x, wq, ws, gw, K, torch.float32, gx=gx)
+    with w4a4_kernel("prepass"):
+        y2, work2 = run_w4a4(x, wq, ws, gw, K, torch.float32, gx=gx)
+    assert torch.equal(y1, y2)
+    o_xq, o_xs, o_gx = nv.nvfp4_w4a4_workspace_layout(M, K)
+    a, b = work1.cpu().numpy(), work2.cpu().numpy()
+    np.testing.assert_array_equal(a[o_xq:o_xs], b[o_xq:o_xs])
+    assert a[o_gx:o_gx + 4].tobytes() == b[o_gx:o_gx + 4].tobytes()
