@@ -785,6 +785,24 @@ def run_one_workload(name: str, calls: int = 3):
         assert nv.nvfp4_workspace_error(work) == 0
         print("ran %d calls of %s" % (calls, name), flush=True)
         return
+    if name.startswith("verify_a_m"):
+        # the M = 9..16 end of the f4 curve: M tokens against the verify_a weights
+        from synth import random_x
+        M = int(name[len("verify_a_m"):])
+        wl = WORKLOADS["verify_a"]
+        _, w = workload_inputs("verify_a")
+        packed, _, swz, g = nv.quantize_weight(w.cuda())
+        del w
+        xd = random_x(M, wl.K, seed=M).cuda()
+        y = torch.empty(M, wl.N, dtype=torch.bfloat16, device="cuda")
+        work = torch.zeros(nv.nvfp4_workspace_bytes(1, M, wl.K, wl.N), dtype=torch.uint8,
+                           device="cuda")
+        for _ in range(calls):
+            nv.nvfp4_linear(xd, packed, swz, g, y, workspace=work)
+        torch.cuda.synchronize()
+        assert nv.nvfp4_workspace_error(work) == 0
+        print("ran %d calls of %s" % (calls, name), flush=True)
+        return
     wl = WORKLOADS[name]
     x, w = workload_inputs(name)
     packed, _, swz, g = nv.quantize_weight(w.cuda())
@@ -818,7 +836,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only-workload", default=None,
                     help="run a few calls of one workload and exit (for ncu captures): a "
-                         "workload name, fp8_requant or mlp_act")
+                         "workload name, fp8_requant, mlp_act or verify_a_m<M> (M tokens on "
+                         "the verify_a weights)")
     args = ap.parse_args()
     global STATIC_W
     STATIC_W = bool(args.static_weights)
