@@ -343,7 +343,9 @@ def run_e2e(torch, nv, setup, args):
                             workspace=s["ws"], static_weights=STATIC_W)
         yh.copy_(yd, non_blocking=True)
 
-    n = min(args.steps, 2048)
+    # at least 256 steps (a region of several ms), queued behind a device-side sleep like
+    # the headline's region, so that host launch jitter does not enter the figure
+    n = min(max(args.steps, 256), 2048)
     G = min(n, 32)
     while n % G:
         G -= 1
@@ -353,6 +355,7 @@ def run_e2e(torch, nv, setup, args):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    hold_stream(torch)
     t0.record()
     for _ in range(n // G):
         graph.replay()
