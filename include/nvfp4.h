@@ -203,7 +203,10 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *          y = g_x g_w * sum_b sx[m,b] sw[n,b] sum_{k in b} e2m1(qx) e2m1(qw).
  *          With a given x_global_scale and M <= 8, the M = 1 GEMV and the skinny GEMM
  *          quantize x themselves (same codes and scales, no pre-pass); x's codes are
- *          then not written to the workspace.  At M > 16 the tensor-core GEMM quantizes
+ *          then not written to the workspace.  With a dynamic scale at M = 1 (K/32 >= 64)
+ *          the GEMV also quantizes x itself: each CTA reduces x's amax over its own
+ *          lanes, and the grid writes x's codes, scales and g_x to the workspace as the
+ *          quantizer would.  At M > 16 the tensor-core GEMM quantizes
  *          x itself: its CTAs (one per SM, launched cooperatively so that all are
  *          resident) each quantize a share of x into the workspace -- after an amax
  *          pass and one grid-wide barrier when the scale is dynamic -- and count

@@ -237,13 +237,19 @@ __host__ __device__ __forceinline__ size_t pipe_slot_bytes(int rows_max, int ngr
 
 // Each CTA releases the next launch on the stream (programmatic dependent launch) once its
 // producer has issued its last copy, so the next kernel's prologue overlaps this one's tail.
+// W4A4 (kXQ): x is quantized in the kernel with g_x = *gx, or, where gx is null, with the
+// g_x of x's own amax (the quantizer's rule): the CTA's consumer lanes hold all of x
+// between them, so every CTA reduces the amax itself, and CTA 0 also writes x's NVFP4
+// encoding (codes, scale atoms with zero padding, g_x) to xq_out / xs_out / gx_out, as the
+// quantizer kernels would.
 template <int G, bool kXQ>
 __global__ void __launch_bounds__(kPipeMaxThreads, 1)
 gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __restrict__ wq,
                     const uint8_t* __restrict__ wrm, const float* __restrict__ gw,
                     const float* __restrict__ gx, int N, void* __restrict__ y, int y_bf16,
                     int rows_max, int rps, int rfirst, int stages, int w_static,
-                    uint32_t* __restrict__ err, WaitCfg dbg) {
+                    uint32_t* __restrict__ err, WaitCfg dbg, uint8_t* __restrict__ xq_out,
+                    uint8_t* __restrict__ xs_out, float* __restrict__ gx_out) {
     constexpr int L = 32 / G;              // rows per step
     extern __shared__ __align__(128) uint8_t smem[];
     const int rowchunks = K >> 5;          // 16-byte chunks per row
@@ -348,7 +354,56 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     for (int q = 0; q < 4; ++q)
         xv[q] = cvalid ? *reinterpret_cast<const uint4*>(x + 32 * c + 8 * q)
                        : make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (kXQ) quantize_chunk_static(xv, *gx);
+    float gq = 1.0f;  // g_x (kXQ)
+    if constexpr (kXQ) {
+        if (gx) {
+            gq = *gx;
+            quantize_chunk_static(xv, gq);
+        } else {
+            // dynamic g_x: the amax of all of x over the CTA's consumer warps
+            __shared__ float x_amax[kPipeMaxThreads / 32];
+            float am = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t w4[4] = {xv[q].x, xv[q].y, xv[q].z, xv[q].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    am = fmaxf(am, fmaxf(fabsf(bf16_to_f32(w4[j] & 0xFFFFu)),
+                                         fabsf(bf16_to_f32(w4[j] >> 16))));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+            if (lane == 0) x_amax[warp] = am;
+            named_bar_sync(2, nthreads_c);
+            float a = 0.0f;
+            for (int w = 0; w < ngroups; ++w) a = fmaxf(a, x_amax[w]);
+            gq = global_scale_from_amax(a);
+            uint32_t codes[4], s2;
+            quantize_chunk_codes(xv, gq, codes, s2);
+            // x's encoding, spread over the grid.  With one row, scale atom a (512 bytes)
+            // holds row 0's scales of blocks 4a .. 4a + 3 in its first 4 bytes and zeros in
+            // the padding rows: the lane of chunk c = 2a (blocks 4a, 4a + 1) takes the scales
+            // and codes of chunk c + 1 from the next lane, and CTA a % grid writes the atom
+            // and both chunks' codes
+            const uint32_t s2_next = __shfl_down_sync(0xffffffffu, s2, 1);
+            uint32_t codes_next[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) codes_next[q] = __shfl_down_sync(0xffffffffu, codes[q], 1);
+            if (rsub == 0 && (c & 1) == 0 && c < rowchunks &&
+                (unsigned)(c >> 1) % gridDim.x == blockIdx.x) {
+                uint4* atom = reinterpret_cast<uint4*>(xs_out + (size_t)(c >> 1) * 512);
+                atom[0] = make_uint4(s2 | (s2_next << 16), 0u, 0u, 0u);
+#pragma unroll 4
+                for (int i = 1; i < 32; ++i) atom[i] = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(xq_out + 16 * c) =
+                    make_uint4(codes[0], codes[1], codes[2], codes[3]);
+                if (c + 1 < rowchunks)
+                    *reinterpret_cast<uint4*>(xq_out + 16 * (c + 1)) =
+                        make_uint4(codes_next[0], codes_next[1], codes_next[2], codes_next[3]);
+            }
+            if (blockIdx.x == 0 && threadIdx.x == 0) *gx_out = gq;
+        }
+    }
     float am = 0.0f, mn = __int_as_float(0x7f800000);  // max, smallest nonzero
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -490,7 +545,7 @@ gemv_m1_pipe_kernel(const uint16_t* __restrict__ x, int K, const uint8_t* __rest
     }
     named_bar_sync(1, nthreads_c);
     if (abort_flag) return;
-    const float scale = *gw * (gx ? *gx : 1.0f);
+    const float scale = *gw * (kXQ ? gq : (gx ? *gx : 1.0f));
     for (int i = threadIdx.x; i < nrows; i += nthreads_c) {
         float v = 0.0f;
         for (int w = 0; w < ngroups; ++w) v += slots[i * ngroups + w];
@@ -795,7 +850,8 @@ template <int G, bool kXQ>
 cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8_t* wrm,
                         const float* gw, const float* gx, int N, void* y, bool y_bf16,
                         uint32_t* err, bool w_static, cudaStream_t stream, const DevInfo& dev,
-                        bool* launched) {
+                        bool* launched, uint8_t* xq_out = nullptr, uint8_t* xs_out = nullptr,
+                        float* gx_out = nullptr) {
     *launched = false;
     const int rowchunks = K / 32;
     const int ngroups = (rowchunks + G - 1) / G;
@@ -838,7 +894,7 @@ cudaError_t launch_pipe(const uint16_t* x, int K, const uint8_t* wq, const uint8
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemv_m1_pipe_kernel<G, kXQ>, x, K, wq, wrm, gw, gx, N,
                            y, y_bf16 ? 1 : 0, rows_max, rps, rfirst, stages,
-                           w_static ? 1 : 0, err, current_wait_cfg());
+                           w_static ? 1 : 0, err, current_wait_cfg(), xq_out, xs_out, gx_out);
     *launched = true;
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -880,24 +936,27 @@ cudaError_t launch_m1(const uint16_t* x, int K, const uint8_t* wq, const uint8_t
 cudaError_t launch_gemv_w4a4_static(const uint16_t* x, int M, int K, const uint8_t* wq,
                                     const uint8_t* wsz_all, const float* gw, const float* gx,
                                     int N, void* y, bool y_bf16, uint32_t* err, bool w_static,
-                                    cudaStream_t stream, const DevInfo& dev, bool* launched) {
+                                    cudaStream_t stream, const DevInfo& dev, bool* launched,
+                                    uint8_t* xq_out, uint8_t* xs_out, float* gx_out) {
     *launched = false;
     const int64_t atom = (int64_t)((N + 127) / 128 * 128) * ((K / 16 + 3) / 4 * 4);
     const uint8_t* wsz = wsz_all + atom;
-    if (M >= 2)
+    if (M >= 2) {
+        if (!gx) return cudaSuccess;  // a dynamic g_x at M >= 2: the quantizer kernels
         return launch_skinny_w4a16(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static,
                                    stream, dev, launched, true);
+    }
     if (M != 1) return cudaSuccess;
     const int rowchunks = K / 32;
     if (rowchunks >= 8 * 8 && (rowchunks + 7) / 8 <= 31)
         return launch_pipe<8, true>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream,
-                                    dev, launched);
+                                    dev, launched, xq_out, xs_out, gx_out);
     if (rowchunks >= 8 * 16 && (rowchunks + 15) / 16 <= 31)
         return launch_pipe<16, true>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream,
-                                     dev, launched);
+                                     dev, launched, xq_out, xs_out, gx_out);
     if (rowchunks >= 8 * 32 && (rowchunks + 31) / 32 <= 31)
         return launch_pipe<32, true>(x, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static, stream,
-                                     dev, launched);
+                                     dev, launched, xq_out, xs_out, gx_out);
     return cudaSuccess;
 }
 

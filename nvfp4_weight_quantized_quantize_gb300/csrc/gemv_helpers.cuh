@@ -49,13 +49,16 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
     return (code & 8u) ? -v : v;
 }
 
-// exponent e with amax * 2^e in [2^14, 2^15) (0 for amax == 0)
-// W4A4 with a static activation scale g, fused into the small-M kernels: the 32 bf16
-// values of a lane's chunk of x (two 16-element blocks) are quantized to NVFP4 with g, as
-// the quantizer would, and replaced by e2m1(code) * e4m3(scale).  bf16 holds those exactly
-// (at most 5 significant bits, magnitudes in [2^-10, 2688]); g stays out of them and in
-// y's scale.
-__device__ __forceinline__ void quantize_chunk_static(uint4 (&v)[4], float g) {
+// W4A4 with the activation scale g fused into the small-M kernels: the 32 bf16 values of a
+// lane's chunk of x (two 16-element blocks) are quantized to NVFP4 with g, as the
+// quantizer would, and replaced by e2m1(code) * e4m3(scale).  bf16 holds those exactly (at
+// most 5 significant bits, magnitudes in [2^-10, 2688]); g stays out of them and in y's
+// scale.  quantize_chunk_codes also returns the chunk's encoding: codes[0..3] the 32 E2M1
+// codes in the packed byte order (block 0: codes[0..1], block 1: codes[2..3]) and s2 the
+// two block scale bytes (block 0 in the low byte).
+__device__ __forceinline__ void quantize_chunk_codes(uint4 (&v)[4], float g, uint32_t (&codes)[4],
+                                                     uint32_t& s2) {
+    s2 = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         float t[16];
@@ -69,7 +72,11 @@ __device__ __forceinline__ void quantize_chunk_static(uint4 (&v)[4], float g) {
             }
         }
         uint32_t lo, hi;
-        const float s = e4m3_to_f32(quantize_block16(t, g, lo, hi));
+        const uint32_t s8 = quantize_block16(t, g, lo, hi);
+        codes[2 * h] = lo;
+        codes[2 * h + 1] = hi;
+        s2 |= s8 << (8 * h);
+        const float s = e4m3_to_f32(s8);
         uint32_t o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -84,6 +91,12 @@ __device__ __forceinline__ void quantize_chunk_static(uint4 (&v)[4], float g) {
     }
 }
 
+__device__ __forceinline__ void quantize_chunk_static(uint4 (&v)[4], float g) {
+    uint32_t codes[4], s2;
+    quantize_chunk_codes(v, g, codes, s2);
+}
+
+// exponent e with amax * 2^e in [2^14, 2^15) (0 for amax == 0)
 __device__ __forceinline__ int chunk_exponent(float amax) {
     if (!(amax > 0.0f)) return 0;
     int E;

@@ -68,14 +68,18 @@ cudaError_t launch_gemv_w4a16(const uint16_t* x, int M, int K, const uint8_t* wq
 
 constexpr int kGemvMaxM = 16;
 
-// W4A4 at 1 <= M <= 8 with a static activation scale *gx, the quantization of x fused into
-// the M = 1 GEMV or the skinny kernel (bf16 x in, no pre-pass, nothing in the workspace but
-// the error word).  Sets *launched when a fused kernel took the call; otherwise nothing
-// was enqueued and the caller quantizes x first.
+// W4A4 at 1 <= M <= 8 with the quantization of x fused into the M = 1 GEMV or the skinny
+// kernel (bf16 x in, no pre-pass).  With a static activation scale *gx nothing lands in
+// the workspace but the error word; with gx null (M = 1 only: a dynamic scale, from x's
+// own amax) the GEMV also writes x's codes, scale atoms and g_x to xq_out / xs_out /
+// gx_out, as the quantizer would.  Sets *launched when a fused kernel took the call;
+// otherwise nothing was enqueued and the caller quantizes x first.
 cudaError_t launch_gemv_w4a4_static(const uint16_t* x, int M, int K, const uint8_t* wq,
                                     const uint8_t* wsz_all, const float* gw, const float* gx,
                                     int N, void* y, bool y_bf16, uint32_t* err, bool w_static,
-                                    cudaStream_t stream, const DevInfo& dev, bool* launched);
+                                    cudaStream_t stream, const DevInfo& dev, bool* launched,
+                                    uint8_t* xq_out = nullptr, uint8_t* xs_out = nullptr,
+                                    float* gx_out = nullptr);
 
 // Whether launch_skinny_w4a16 takes calls with this K (its ring fits shared memory), for
 // up to 8 tokens and for 9..16 tokens (two token tiles, one pass over W).

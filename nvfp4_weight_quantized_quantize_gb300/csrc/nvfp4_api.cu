@@ -332,19 +332,21 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
                                            w_global_scale, (int)N, y, ybf,
                                            static_cast<uint8_t*>(workspace), stream, d));
     }
-    // W4A4 at M <= 8 with a static activation scale: the quantization of x is fused into
-    // the small-M kernels (no pre-pass; the same codes and scales as below)
-    if (x_global_scale && M <= 8) {
-        bool launched = false;
-        const cudaError_t e = launch_gemv_w4a4_static(
-            xb, (int)M, (int)K, w_packed, w_scales_swizzled, w_global_scale, x_global_scale,
-            (int)N, y, ybf, static_cast<uint32_t*>(workspace), w_static, stream, d, &launched);
-        if (e != cudaSuccess || launched) return from_cuda(e);
-    }
-    // W4A4: quantize x into the workspace (bit-exact with nvfp4_quantize + nvfp4_repack)
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const W4A4Layout L = w4a4_layout(M, K, N);
     float* gx = reinterpret_cast<float*>(ws + L.gx);
+    // W4A4 at M <= 8 with a static activation scale, or at M = 1 with a dynamic one: the
+    // quantization of x is fused into the small-M kernels (no pre-pass; the same codes and
+    // scales as below, which the dynamic M = 1 path also leaves in the workspace)
+    if ((x_global_scale && M <= 8) || (!x_global_scale && M == 1)) {
+        bool launched = false;
+        const cudaError_t e = launch_gemv_w4a4_static(
+            xb, (int)M, (int)K, w_packed, w_scales_swizzled, w_global_scale, x_global_scale,
+            (int)N, y, ybf, static_cast<uint32_t*>(workspace), w_static, stream, d, &launched,
+            ws + L.xq, ws + L.xs, gx);
+        if (e != cudaSuccess || launched) return from_cuda(e);
+    }
+    // W4A4: quantize x into the workspace (bit-exact with nvfp4_quantize + nvfp4_repack)
     if (M > kGemvMaxM && !w4a4_prepass_forced()) {
         // one kernel: x quantized by the GEMM's own CTAs, then the block-scaled GEMM
         const cudaError_t e = launch_gemm_w4a4_quant_x(

@@ -29,8 +29,8 @@ once, so the kernel's fp32 y must equal the oracle's fp64 result rounded to fp32
          kernel at large K;
   M > 16: the tcgen05 W4A16 GEMM (with stream-K tails) and the block-scaled W4A4 GEMM
          (the one-CTA kernel, and the CTA-pair kernel);
-  W4A4 at small M (pre-pass, and the static-scale fused kernels), and the linear on
-  NVFP4 activations.
+  W4A4 at small M (pre-pass, the static-scale fused kernels, and the dynamic-scale M = 1
+  GEMV), and the linear on NVFP4 activations.
 """
 import numpy as np
 import pytest
@@ -141,7 +141,7 @@ def test_w4a16_gemm_exact_sampled(M, K, N):
 
 
 @pytest.mark.parametrize("M,K,N,gx", [
-    (1, 5120, 3000, None),     # pre-pass, then the GEMV on x's exact bf16 value
+    (1, 5120, 3000, None),     # dynamic scale: amax and quantization inside the GEMV
     (3, 5120, 1000, None),
     (1, 5120, 1000, 2.0 ** -5),   # static scale: quantized inside the GEMV
     (5, 5120, 777, 2.0 ** -5),    # static scale: quantized inside the skinny kernel

@@ -88,8 +88,12 @@ def test_zero_weights_and_zero_x():
 
 
 @pytest.mark.parametrize("M,K,N,gx", [(1, 512, 256, None), (7, 1024, 300, None),
-                                      (4, 96, 50, 0.003), (16, 5120, 128, None)])
+                                      (4, 96, 50, 0.003), (16, 5120, 128, None),
+                                      (1, 5120, 1000, None), (1, 17408, 300, None),
+                                      (1, 2080, 77, None)])
 def test_w4a4_small_m(M, K, N, gx):
+    # M = 1 with a dynamic scale and K / 32 >= 64: the GEMV reduces x's amax itself and
+    # leaves x's encoding in the workspace (checked below like the quantizer's)
     x, w = make_inputs(M, K, N, seed=200 + M)
     wq, ws, gw = oracle.quantize(w.numpy())
     y, ws_t = run_linear(x, wq, ws, gw, K, torch.bfloat16, mode="w4a4", gx=gx)
