@@ -406,7 +406,8 @@ void nvfp4_debug_expire_waits(int on);
  * pairs on two SMs (tcgen05 cta_group::2, 256 x 256 tiles; a device that cannot co-schedule
  * CTA pairs runs the one-CTA kernel); 3 the one-CTA kernel with bf16 x quantized by the
  * quantizer kernels ahead of it rather than inside its grid (the path of a device that
- * refuses the GEMM's cooperative launch; the same bits).  Both satisfy the same tolerance; their stream-K
+ * refuses the GEMM's cooperative launch; the same bits), and, at M = 1 with a dynamic
+ * scale, the same quantizer kernels ahead of the GEMV (the same bits).  Both satisfy the same tolerance; their stream-K
  * splits differ, so outputs can differ in the last bits where a tile's K steps are summed
  * in different groups.  Host-only; the switch is per thread. */
 void nvfp4_debug_w4a4_kernel(int which);

@@ -942,7 +942,9 @@ cudaError_t launch_gemv_w4a4_static(const uint16_t* x, int M, int K, const uint8
     const int64_t atom = (int64_t)((N + 127) / 128 * 128) * ((K / 16 + 3) / 4 * 4);
     const uint8_t* wsz = wsz_all + atom;
     if (M >= 2) {
-        if (!gx) return cudaSuccess;  // a dynamic g_x at M >= 2: the quantizer kernels
+        // a dynamic g_x at M >= 2 takes the quantizer kernels: every skinny CTA would
+        // quantize all of x again, which costs more than one pass ahead of the kernel
+        if (!gx) return cudaSuccess;
         return launch_skinny_w4a16(x, M, K, wq, wsz, gw, gx, N, y, y_bf16, err, w_static,
                                    stream, dev, launched, true);
     }

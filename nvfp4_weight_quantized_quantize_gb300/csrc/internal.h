@@ -148,8 +148,9 @@ cudaError_t launch_gemm_w4a4(const uint8_t* xq, const uint8_t* xsz, const float*
 // True while the calling thread asks for the CTA-pair W4A4 GEMM at M > 16
 // (nvfp4_debug_w4a4_kernel); by default the one-CTA kernel runs.
 bool w4a4_use_pairs();
-// True while the calling thread asks for the quantizer kernels ahead of the W4A4 GEMM at
-// M > 16 instead of the GEMM's in-kernel quantization (nvfp4_debug_w4a4_kernel).
+// True while the calling thread asks for the quantizer kernels ahead of the W4A4 kernels
+// (at M > 16, and at M = 1 with a dynamic scale) instead of the kernels' own quantization
+// of x (nvfp4_debug_w4a4_kernel).
 bool w4a4_prepass_forced();
 
 // Wait settings for the launches of the calling thread: the production limits, or (while

@@ -338,7 +338,7 @@ NVFP4_API nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K,
     // W4A4 at M <= 8 with a static activation scale, or at M = 1 with a dynamic one: the
     // quantization of x is fused into the small-M kernels (no pre-pass; the same codes and
     // scales as below, which the dynamic M = 1 path also leaves in the workspace)
-    if ((x_global_scale && M <= 8) || (!x_global_scale && M == 1)) {
+    if ((x_global_scale && M <= 8) || (!x_global_scale && M == 1 && !w4a4_prepass_forced())) {
         bool launched = false;
         const cudaError_t e = launch_gemv_w4a4_static(
             xb, (int)M, (int)K, w_packed, w_scales_swizzled, w_global_scale, x_global_scale,

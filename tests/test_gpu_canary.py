@@ -58,6 +58,7 @@ def guarded(shape, dtype):
     (3, 1056, 77, "w4a4"), (12, 2080, 300, "w4a4"), (300, 5152, 641, "w4a4-pair"),
     (40, 1056, 129, "w4a4-pair"), (520, 2080, 1300, "w4a4"), (520, 2080, 1300, "w4a4-pair"),
     (700, 1056, 1500, "w4a4-pair"), (1, 2080, 300, "w4a4"), (1, 17408, 301, "w4a4"),
+    (5, 2080, 300, "w4a4"), (8, 1056, 129, "w4a4"),
 ])
 def test_linear_writes_only_its_outputs(M, K, N, mode):
     kernel = mode.split("-")[1] if "-" in mode else "auto"

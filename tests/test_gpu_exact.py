@@ -142,7 +142,7 @@ def test_w4a16_gemm_exact_sampled(M, K, N):
 
 @pytest.mark.parametrize("M,K,N,gx", [
     (1, 5120, 3000, None),     # dynamic scale: amax and quantization inside the GEMV
-    (3, 5120, 1000, None),
+    (3, 5120, 1000, None),        # dynamic scale at M >= 2: the quantizer kernels first
     (1, 5120, 1000, 2.0 ** -5),   # static scale: quantized inside the GEMV
     (5, 5120, 777, 2.0 ** -5),    # static scale: quantized inside the skinny kernel
     (13, 2048, 300, 2.0 ** -4),   # static scale, M > 8: pre-pass

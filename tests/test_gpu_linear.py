@@ -90,10 +90,12 @@ def test_zero_weights_and_zero_x():
 @pytest.mark.parametrize("M,K,N,gx", [(1, 512, 256, None), (7, 1024, 300, None),
                                       (4, 96, 50, 0.003), (16, 5120, 128, None),
                                       (1, 5120, 1000, None), (1, 17408, 300, None),
-                                      (1, 2080, 77, None)])
+                                      (1, 2080, 77, None), (4, 5120, 1000, None),
+                                      (8, 2080, 129, None), (2, 96, 50, None)])
 def test_w4a4_small_m(M, K, N, gx):
     # M = 1 with a dynamic scale and K / 32 >= 64: the GEMV reduces x's amax itself and
-    # leaves x's encoding in the workspace (checked below like the quantizer's)
+    # leaves x's encoding in the workspace (checked below like the quantizer's); the
+    # others quantize x ahead of the kernel
     x, w = make_inputs(M, K, N, seed=200 + M)
     wq, ws, gw = oracle.quantize(w.numpy())
     y, ws_t = run_linear(x, wq, ws, gw, K, torch.bfloat16, mode="w4a4", gx=gx)
@@ -293,3 +295,22 @@ def test_wide_n(M, K, N):
     pn = np.concatenate([rng.integers(0, N, 8192), np.tile(edge, M)])
     y_ref, ab = oracle.linear_w4a16_pairs(x, wq, ws, gw, pm, pn)
     check_tolerance(y_to_f64(y)[pm, pn], y_ref, ab, "wide N M%d" % M)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 5120, 1000), (1, 17408, 300), (1, 2080, 129)])
+def test_w4a4_dynamic_small_m_matches_prepass(M, K, N):
+    # x quantized inside the M = 1 GEMV (dynamic scale) and by the quantizer kernels ahead
+    # of it: the same encoding in the workspace and the same y, to the bit
+    from helpers import w4a4_kernel
+    x, w = make_inputs(M, K, N, seed=600 + M)
+    wq, ws, gw = oracle.quantize(w.numpy())
+    y1, ws1 = run_linear(x, wq, ws, gw, K, torch.float32, mode="w4a4")
+    with w4a4_kernel("prepass"):
+        y2, ws2 = run_linear(x, wq, ws, gw, K, torch.float32, mode="w4a4")
+    assert torch.equal(y1, y2)
+    o_xq, o_xs, o_gx = nv.nvfp4_w4a4_workspace_layout(M, K)
+    a, b = ws1.cpu().numpy(), ws2.cpu().numpy()
+    nb = oracle.repack_atom_bytes(M, K)
+    np.testing.assert_array_equal(a[o_xq:o_xq + M * K // 2], b[o_xq:o_xq + M * K // 2])
+    np.testing.assert_array_equal(a[o_xs:o_xs + nb], b[o_xs:o_xs + nb])
+    assert a[o_gx:o_gx + 4].tobytes() == b[o_gx:o_gx + 4].tobytes()
