@@ -234,11 +234,12 @@ nvfp4_status nvfp4_repack(const uint8_t* scales_rowmajor, int64_t rows, int64_t 
  *                      be zero before the first call; every call that completes without
  *                      a device error leaves them zero) and fp32 partial tiles.  After a
  *                      device error (nvfp4_workspace_error != 0), zero-fill it again.
- * Kernels: M = 1 pipelined GEMV; 2 <= M <= 8 streamed skinny GEMM (mma.sync); 9 <= M <=
- * 16 the skinny GEMM on tokens 0..7 and again on the rest where it takes the K, else an
- * mma.sync GEMM reading W from global memory; M > 16 the tcgen05 GEMMs (W4A16: W
- * dequantized to bf16 per tile; W4A4: block-scaled kind::mxf4nvf4).  Results are
- * deterministic.
+ * Kernels: M = 1 pipelined GEMV; 2 <= M <= 8 streamed skinny GEMM (mma.sync);
+ * 9 <= M <= 16 the skinny GEMM with two token tiles in one pass over W where K fits its
+ * warps and shared memory (else two skinny passes, tokens 0..7 and the rest, where one
+ * tile fits, else an mma.sync GEMM reading W from global memory); M > 16 the tcgen05
+ * GEMMs (W4A16: W dequantized to bf16 per tile; W4A4: block-scaled kind::mxf4nvf4).
+ * Results are deterministic.
  */
 nvfp4_status nvfp4_linear(const void* x, int64_t M, int64_t K, const uint8_t* w_packed,
                           const uint8_t* w_scales_swizzled, const float* w_global_scale,
