@@ -122,6 +122,28 @@ def test_quantize_rejects(lib):
     assert _q(lib, wsb=16) == WORKSPACE
 
 
+def _qn(lib, src=16, dt=0, rows=4, cols=32, packed=32, scales=48, g=64):
+    v = lambda a: None if a is None else ctypes.c_void_p(a)
+    return lib.nvfp4_quantize_noalloc(v(src), dt, rows, cols, v(packed), v(scales), v(g),
+                                      None)
+
+
+def test_quantize_noalloc_rejects(lib):
+    # the same host checks as nvfp4_quantize, less the workspace's
+    assert _qn(lib, src=None) == NULL
+    assert _qn(lib, packed=None) == NULL
+    assert _qn(lib, scales=None) == NULL
+    assert _qn(lib, g=None) == NULL
+    assert _qn(lib, dt=7) == DTYPE
+    assert _qn(lib, cols=24) == SHAPE
+    assert _qn(lib, rows=0) == SHAPE
+    assert _qn(lib, cols=8) == SHAPE
+    assert _qn(lib, rows=(1 << 30) + 1) == SHAPE
+    assert _qn(lib, src=17) == ALIGN
+    assert _qn(lib, scales=56) == ALIGN
+    assert _qn(lib, g=66) == ALIGN
+
+
 def _q8(lib, src=16, bs=20, rows=4, cols=32, packed=32, scales=48, g=64, ws=4096,
         wsb=1 << 20):
     v = lambda a: None if a is None else ctypes.c_void_p(a)
