@@ -23,7 +23,11 @@
 //     stage short so that it lands early; consumer warps each own a fixed group of 16-byte
 //     chunks of K and keep their x in registers for the whole kernel; the lanes of a row
 //     reduce by shuffles into per-(row, warp) slots that are added in a fixed order.
-//     Launched as a programmatic dependent; every wait is bounded.
+//     Launched as a programmatic dependent; every wait is bounded.  Its kXQ instantiation
+//     is W4A4 at M = 1: each lane quantizes the x blocks it holds (a given g_x, or one
+//     from x's amax reduced by every CTA, in which case the grid also writes x's codes,
+//     scale atoms and g_x to the workspace, as the quantizer would) and multiplies by
+//     the quantized values.
 //   - gemv_m1_kernel: M = 1 where K is outside the pipelined kernel's range (K / 32 < 64
 //     or > 992):
 //     a grid of 2 x SMs CTAs of 8 warps, (row, K segment) units split evenly over the
