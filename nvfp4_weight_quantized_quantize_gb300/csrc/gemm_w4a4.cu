@@ -34,6 +34,10 @@
 //               2 x 4 of x) from shared memory and stores them to its TMEM lane (keeping
 //               these copies off the MMA thread's in-order tcgen05 queue).
 // Work split, stream-K fixup, bounded waits and error reporting as in the W4A16 GEMM.
+//
+// Further down, a CTA-pair variant of the same GEMM (tcgen05 cta_group::2, 256 x 256
+// tiles), selected per thread with nvfp4_debug_w4a4_kernel: the same bits, but slower than
+// the kernel above at the prefill and W4A4 shapes measured, so not the default.
 #include <cuda.h>
 
 #include <atomic>
