@@ -37,7 +37,8 @@
 //
 // Further down, a CTA-pair variant of the same GEMM (tcgen05 cta_group::2, 256 x 256
 // tiles), selected per thread with nvfp4_debug_w4a4_kernel: the same bits, but slower than
-// the kernel above at the prefill and W4A4 shapes measured, so not the default.
+// the kernel above on the shapes measured (M = 2048 at K 5120, N 17408; the 512-token down
+// projection at K 17408, N 5120), so not the default.
 #include <cuda.h>
 
 #include <atomic>
